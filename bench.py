@@ -1,0 +1,543 @@
+#!/usr/bin/env python
+"""Quantize + GEMM benchmark of one transformer layer's 12 GEMMs on GB300.
+
+Workload ("How to optimize Transformer-based models for low-precision
+training", model configuration and training input): CodonFM-5B, hidden 4096,
+intermediate 16384, micro-batch 31 x sequence 512 = 15,872 tokens; the 12 GEMMs
+are QKV / attention-out / MLP-up / MLP-down x Fprop / Dgrad / Wgrad.  Inputs are
+synthetic bf16 (activations ~N(0,1), weights ~N(0,0.02^2), gradients
+~N(0,(1e-3)^2)), resident in HBM before the timed region.
+
+One step = one layer: for each of the 12 GEMMs, quantize the two operand copies
+it reads (autocast mode: "before every GEMM the inputs are quantized
+dynamically", same page, autocast vs pre-quantize) and run the GEMM, all in
+liblpq's CUDA kernels.  The headline recipe is NVFP4 (1D 16-blocks for
+activations and gradients, 16x16 blocks for weights, random Hadamard transform
+on the Wgrad inputs, stochastic rounding of gradients).  The other recipes and
+the pre-quantize mode (GEMM only) are measured in the same run and reported
+under "recipes".
+
+Usage (the pages' CLI flags are accepted): python bench.py [--gpus N] [--steps K]
+[--warmup W] [--impl lpq|reference] [--recipe nvfp4|mxfp8|fp8_current|
+fp8_delayed|bf16] [--pre-quantize] [--no-fp8] [--no-fp4] ...
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+RECIPES = ["bf16", "fp8_delayed", "fp8_current", "mxfp8", "nvfp4"]
+
+
+def parse():
+    p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--impl", choices=["lpq", "reference"], default="lpq")
+    p.add_argument("--recipe", choices=RECIPES, default="nvfp4")
+    p.add_argument("--pre-quantize", dest="prequant", action="store_true")
+    p.add_argument("--no-fp8", action="store_true", help="skip MXFP8 in the recipe sweep")
+    p.add_argument("--no-fp4", action="store_true", help="skip NVFP4 in the recipe sweep")
+    p.add_argument("--no-sweep", action="store_true", help="time only the headline recipe")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--hidden_size", type=int, default=4096)
+    p.add_argument("--intermediate_size", type=int, default=16384)
+    p.add_argument("--num_attention_heads", type=int, default=32)
+    p.add_argument("--num_hidden_layers", type=int, default=24)
+    p.add_argument("--micro_batch_size", type=int, default=31)
+    p.add_argument("--sequence_length", type=int, default=512)
+    p.add_argument("--seed", type=int, default=0)
+    p.add_argument("-o", "--output", default=None, help="write the per-GEMM table as JSON here")
+    return p.parse_args()
+
+
+# ------------------------------------------------------------------ distributed
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(value, world):
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    t = torch.tensor([float(value)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.idx, self.proc, self.lines = gpu_index, None, []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            threading.Thread(target=self._read, daemon=True).start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = max(mx, float(f[2]))
+            except ValueError:
+                continue
+            for name, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx or None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ layer workload
+class Layer:
+    """Inputs, quantized buffers and outputs of one CodonFM-5B-shaped layer."""
+
+    def __init__(self, args, device):
+        import torch
+        from precision_transformer_gemms_gb300 import lpq, synth
+        self.lpq, self.torch = lpq, torch
+        h, f = args.hidden_size, args.intermediate_size
+        self.M = args.micro_batch_size * args.sequence_length
+        self.shapes = lpq.layer_shapes(h, f, args.micro_batch_size, args.sequence_length,
+                                       args.num_attention_heads, args.num_hidden_layers)
+        self.linears = {"qkv": (h, 3 * h), "attn_out": (h, h), "mlp_up": (h, f), "mlp_down": (f, h)}
+        self.flops = sum(2 * m * k * n for _, _, m, k, n in self.shapes)
+        self.inp = {}
+        base = args.seed
+        for i, (name, (K, N)) in enumerate(self.linears.items()):
+            self.inp[name] = {
+                "X": synth.bf16_normal((self.M, K), synth.ACT_STD, base + 100 * i + synth.SEED_X, device),
+                "W": synth.bf16_normal((N, K), synth.WEIGHT_STD, base + 100 * i + synth.SEED_W, device),
+                "dY": synth.bf16_normal((self.M, N), synth.GRAD_STD, base + 100 * i + synth.SEED_DY, device),
+            }
+        self.out = {}
+        for name, lay, m, k, n in self.shapes:
+            self.out[name] = torch.empty((m, n), dtype=torch.bfloat16, device=device)
+        self.bufs = {}
+        self.states = {}
+        self.device = device
+
+    # quantizer settings per recipe and tensor role: (fmt, flags_extra, scaling)
+    def qcfg(self, recipe, role):
+        L = self.lpq
+        if recipe in ("fp8_current", "fp8_delayed"):
+            fmt = L.FP8_E5M2 if role == "dY" else L.FP8_E4M3
+            return fmt, 0, L.SCALING_DELAYED if recipe == "fp8_delayed" else L.SCALING_CURRENT
+        if recipe == "mxfp8":
+            return L.MXFP8, 0, L.SCALING_CURRENT
+        if recipe == "nvfp4":
+            if role == "W":
+                return L.NVFP4_2D, 0, L.SCALING_CURRENT
+            extra = L.STOCHASTIC if role == "dY" else 0
+            return L.NVFP4, extra, L.SCALING_CURRENT
+        raise ValueError(recipe)
+
+    def buf(self, recipe, lin, role, colwise):
+        key = (recipe, lin, role, colwise)
+        if key not in self.bufs:
+            L = self.lpq
+            x = self.inp[lin][role]
+            R, C = x.shape
+            if recipe == "bf16":
+                t = x.t().contiguous() if colwise else x
+                self.bufs[key] = L.Copy.of_bf16(t, colwise)
+            else:
+                fmt, _, _ = self.qcfg(recipe, role)
+                self.bufs[key] = L.Copy(fmt, C if colwise else R, R if colwise else C, colwise, L.SF_GEMM,
+                                        self.device)
+        return self.bufs[key]
+
+    def state(self, lin, role):
+        if (lin, role) not in self.states:
+            self.states[(lin, role)] = self.lpq.DelayedState(16, self.device)
+        return self.states[(lin, role)]
+
+    def quantize(self, recipe, lin, role, colwise, seed):
+        """One lpq_quantize of one operand copy into its persistent buffer."""
+        L = self.lpq
+        fmt, extra, scaling = self.qcfg(recipe, role)
+        flags = (L.COLWISE if colwise else L.ROWWISE) | extra
+        if recipe == "nvfp4" and colwise and role in ("X", "dY"):
+            flags |= L.RHT_COLWISE  # Wgrad inputs
+        copy = self.buf(recipe, lin, role, colwise)
+        qt = L.QTensor(None if colwise else copy, copy if colwise else None)
+        st = self.state(lin, role) if scaling == L.SCALING_DELAYED else None
+        L.quantize(self.inp[lin][role], fmt, flags, scaling=scaling, seed=seed, rht_seed=1234, state=st, out=qt)
+        if st is not None:
+            L.scale_update(st, copy.amax, L.FMAX[fmt])
+        return copy
+
+    # operands of each pass: (a role, a colwise), (b role, b colwise)
+    PASS = {0: (("X", False), ("W", False)), 1: (("dY", False), ("W", True)), 2: (("dY", True), ("X", True))}
+
+    def gemm_list(self):
+        return [(name, lay, name.rsplit("_", 1)[0]) for name, lay, *_ in self.shapes]
+
+    def prequantize(self, recipe):
+        for _, lay, lin in self.gemm_list():
+            for role, col in self.PASS[lay]:
+                if recipe == "bf16":
+                    self.buf(recipe, lin, role, col)
+                else:
+                    self.quantize(recipe, lin, role, col, seed=0)
+
+    def step(self, recipe, autocast, step_idx=0, events=None):
+        """Enqueue one layer step; `events` (optional) gets (name, kind, ev0, ev1)."""
+        L, torch = self.lpq, self.torch
+        delayed = recipe == "fp8_delayed"
+        for name, lay, lin in self.gemm_list():
+            (ra, ca), (rb, cb) = self.PASS[lay]
+            if recipe != "bf16" and (autocast or delayed):
+                e0 = torch.cuda.Event(enable_timing=True) if events is not None else None
+                if e0:
+                    e0.record()
+                a = self.quantize(recipe, lin, ra, ca, seed=step_idx * 64 + lay)
+                b = self.quantize(recipe, lin, rb, cb, seed=step_idx * 64 + lay + 8)
+                if e0:
+                    e1 = torch.cuda.Event(enable_timing=True)
+                    e1.record()
+                    events.append((name, "quantize", e0, e1))
+            else:
+                a, b = self.buf(recipe, lin, ra, ca), self.buf(recipe, lin, rb, cb)
+            e0 = torch.cuda.Event(enable_timing=True) if events is not None else None
+            if e0:
+                e0.record()
+            L.gemm(lay, a, b, c=self.out[name])
+            if e0:
+                e1 = torch.cuda.Event(enable_timing=True)
+                e1.record()
+                events.append((name, "gemm", e0, e1))
+
+    def kernels_per_step(self, recipe, autocast):
+        """Kernels of liblpq launched by one step (memsets are not kernels of ours)."""
+        n = 12  # GEMMs
+        if recipe == "bf16" or not (autocast or recipe == "fp8_delayed"):
+            return n
+        per_q = {"fp8_current": 2, "fp8_delayed": 2, "mxfp8": 1, "nvfp4": 2}[recipe]  # (amax pass) + tile pass
+        if recipe == "fp8_delayed":
+            per_q = 2  # tile pass + scale update
+        return n + 24 * per_q
+
+    def step_io_bytes(self):
+        """Bytes of the step's bf16 inputs (H2D) and outputs (D2H)."""
+        i = sum(t.numel() * 2 for d in self.inp.values() for t in d.values())
+        o = sum(t.numel() * 2 for t in self.out.values())
+        return i, o
+
+
+def time_steps(layer, recipe, autocast, steps, warmup, world, per_kernel=False):
+    import torch
+    for w in range(warmup):
+        layer.step(recipe, autocast, w)
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    events = [] if per_kernel else None
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for s in range(steps):
+        layer.step(recipe, autocast, warmup + s, events)
+    e1.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    ms = max_over_ranks(ms, world)
+    return ms / steps, events
+
+
+def summarize_events(layer, events, steps):
+    """Per GEMM: mean GEMM ms and quantize ms over the timed steps."""
+    acc = {}
+    for name, kind, a, b in events:
+        acc.setdefault((name, kind), []).append(a.elapsed_time(b))
+    table = {}
+    shp = {n: (m, k, nn) for n, _, m, k, nn in layer.shapes}
+    for name, _, _ in layer.gemm_list():
+        m, k, n = shp[name]
+        g = statistics.mean(acc[(name, "gemm")])
+        q = statistics.mean(acc[(name, "quantize")]) if (name, "quantize") in acc else 0.0
+        table[name] = {"m": m, "k": k, "n": n, "gemm_ms": g, "quant_ms": q,
+                       "gemm_tflops": 2 * m * k * n / (g * 1e-3) / 1e12}
+    return table
+
+
+def measured_peaks():
+    try:
+        return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except Exception:
+        return None
+
+
+# ------------------------------------------------------------------ CPU oracle sample
+def oracle_sample(layer_shapes, M, linears, rows=2, cols=128, slab=16, seed=0):
+    """Times the oracle on a bounded sample of one layer step and projects the
+    step: per GEMM, `rows` x `cols` outputs of the FP64 GEMM (from NVFP4
+    operands) and the NVFP4 quantization of a `slab`-row slab of each operand,
+    both scaled to the full sizes.  Returns (projected seconds per layer, info)."""
+    import numpy as np
+    import oracle as o
+    from precision_transformer_gemms_gb300 import synth
+    t_gemm = t_q = 0.0
+    rng = np.random.default_rng(seed)
+    for name, lay, m, k, n in layer_shapes:
+        xa = synth.host_bits(synth.bf16_normal((rows, k), 1.0, seed + 1, "cpu"))
+        xb = synth.host_bits(synth.bf16_normal((cols, k), 0.02, seed + 2, "cpu"))
+        t0 = time.perf_counter()
+        qa = o.nvfp4(xa, o.NV_ROW)
+        qb = o.nvfp4(xb, o.NV_ROW | o.NV_2D) if cols % 16 == 0 else o.nvfp4(xb, o.NV_ROW)
+        t1 = time.perf_counter()
+        A = o.Operand(o.K_NVFP4, qa["row"], qa["row_sf"], qa["row_ts"])
+        B = o.Operand(o.K_NVFP4, qb["row"], qb["row_sf"], qb["row_ts"])
+        o.gemm(A, B, rows, cols, k)
+        t2 = time.perf_counter()
+        t_gemm += (t2 - t1) * (m * n) / (rows * cols)
+        # two operand copies quantized per GEMM, each of m*k or n*k elements
+        t_q += (t1 - t0) * ((m * k) + (n * k)) / (rows * k + cols * k)
+    return t_gemm + t_q, {"gemm_s": t_gemm, "quant_s": t_q}
+
+
+def run_reference(args, rank, world):
+    """The oracle arm: each step is a bounded sample of the layer workload on
+    the host cores, projected to one layer."""
+    if rank != 0:
+        return
+    import oracle as o
+    from precision_transformer_gemms_gb300 import synth  # noqa: F401
+    h, f = args.hidden_size, args.intermediate_size
+    M = args.micro_batch_size * args.sequence_length
+    lins = [("qkv", h, 3 * h), ("attn_out", h, h), ("mlp_up", h, f), ("mlp_down", f, h)]
+    shapes = []
+    for lin, K, N in lins:
+        shapes += [(f"{lin}_fprop", 0, M, K, N), (f"{lin}_dgrad", 1, M, N, K), (f"{lin}_wgrad", 2, N, M, K)]
+    flops = sum(2 * m * k * n for _, _, m, k, n in shapes)
+    for w in range(args.warmup):
+        oracle_sample(shapes, M, lins, rows=1, cols=32, slab=16, seed=w)
+    proj = []
+    t0 = time.perf_counter()
+    for s in range(args.steps):
+        sec, _ = oracle_sample(shapes, M, lins, rows=1, cols=64, slab=16, seed=args.warmup + s)
+        proj.append(sec)
+    wall = time.perf_counter() - t0
+    sec = statistics.mean(proj)
+    value = flops / sec / 1e12
+    line = {"impl": "reference", "metric": "quantize+GEMM TFLOP/s & % of FP8/FP4 peak; ms/layer (CodonFM-5B shape)",
+            "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": sec * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "CodonFM-5B layer, 12 GEMMs, NVFP4 autocast (M=15872, hidden 4096, "
+                                   "intermediate 16384)", "global_batch": args.micro_batch_size,
+                       "seq_len": args.sequence_length, "parallelism": "replicas"},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": o.num_threads(), "kind": "oracle",
+                             "sample": "per step: per GEMM 1x64 outputs of the FP64 oracle GEMM on NVFP4 operands "
+                                       "and their NVFP4 quantization, projected to the full layer",
+                             "wall_s": wall},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ main arm
+def run_lpq(args, rank, world, local):
+    import torch
+    from precision_transformer_gemms_gb300 import lpq
+    device = f"cuda:{local}"
+    torch.cuda.set_device(local)
+    lpq.lib()
+    layer = Layer(args, device)
+    recipe = args.recipe
+    autocast = not args.prequant
+    if recipe == "fp8_delayed":
+        autocast = True  # delayed scaling needs the amax history: always dynamic
+    layer.prequantize(recipe)  # buffers exist before the timed region (pre-quantize mode reads them)
+    torch.cuda.synchronize()
+
+    # headline: recipe/mode, whole-step CUDA events, K steps
+    clocks = ClockSampler(local)
+    clocks.start()
+    ms_step, _ = time_steps(layer, recipe, autocast, args.steps, args.warmup, world)
+    clk = clocks.stop()
+    # per-kernel durations (same steps, events around each launch)
+    _, events = time_steps(layer, recipe, autocast, max(3, args.steps // 2), 1, world, per_kernel=True)
+    table = summarize_events(layer, events, max(3, args.steps // 2))
+
+    value = layer.flops * world / (ms_step * 1e-3) / 1e12
+    peaks = measured_peaks()
+    gemm_ms = sum(r["gemm_ms"] for r in table.values())
+    quant_ms = sum(r["quant_ms"] for r in table.values())
+    gemm_achieved = layer.flops / (gemm_ms * 1e-3) / 1e12
+    ratio = {"bf16": 1, "fp8_current": 2, "fp8_delayed": 2, "mxfp8": 2, "nvfp4": 6}[recipe]
+    if peaks:
+        peak = peaks["bf16_tflops_sustained"] * ratio
+        peak_src = f"of measured: bf16_tflops_sustained x {ratio} (nominal dense ratio of the format)"
+    else:
+        peak = 1700.0 * ratio
+        peak_src = f"of fallback: 1.7 PFLOP/s bf16 sustained x {ratio}"
+    roof = {"bound": "tensor", "achieved": gemm_achieved, "peak": peak, "unit": "TFLOP/s",
+            "frac": gemm_achieved / peak, "traffic": None, "kernel": f"gemm_kernel ({recipe})",
+            "peak_source": peak_src}
+    hbm = peaks["hbm_gbs"] if peaks else 6800.0
+
+    # recipe sweep (fewer steps each)
+    recipes = {}
+    if not args.no_sweep:
+        sweep = [r for r in RECIPES if not (args.no_fp8 and r == "mxfp8") and not (args.no_fp4 and r == "nvfp4")]
+        k = max(3, args.steps // 4)
+        for r in sweep:
+            layer.prequantize(r)
+            res = {}
+            for mode in ("autocast", "prequant"):
+                ac = mode == "autocast" or r == "fp8_delayed"
+                if r == "bf16":
+                    ac = False
+                ms, _ = time_steps(layer, r, ac, k, 2, world)
+                res[f"{mode}_ms_per_layer"] = ms
+                res[f"{mode}_tflops"] = layer.flops / (ms * 1e-3) / 1e12
+            recipes[r] = res
+            # free this recipe's buffers before the next one
+            for key in [k_ for k_ in layer.bufs if k_[0] == r and r != recipe]:
+                del layer.bufs[key]
+            torch.cuda.empty_cache()
+        if "bf16" in recipes:
+            for r, res in recipes.items():
+                for mode in ("autocast", "prequant"):
+                    res[f"{mode}_speedup_vs_bf16"] = recipes["bf16"]["prequant_ms_per_layer"] / res[f"{mode}_ms_per_layer"]
+
+    # e2e: pinned host inputs -> device, step, outputs -> host, every step
+    e2e = None
+    if not args.no_e2e:
+        host_in = {lin: {r: t.cpu().pin_memory() for r, t in d.items()} for lin, d in layer.inp.items()}
+        host_out = {n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for n, t in layer.out.items()}
+        bi, bo = layer.step_io_bytes()
+        steps = max(3, args.steps // 2)
+
+        def e2e_step(s):
+            for lin, d in layer.inp.items():
+                for r, t in d.items():
+                    t.copy_(host_in[lin][r], non_blocking=True)
+            layer.step(recipe, autocast, s)
+            for n, t in layer.out.items():
+                host_out[n].copy_(t, non_blocking=True)
+
+        for w in range(2):
+            e2e_step(w)
+        torch.cuda.synchronize()
+        barrier(world)
+        t0 = time.perf_counter()
+        for s in range(steps):
+            e2e_step(100 + s)
+        torch.cuda.synchronize()
+        barrier(world)
+        dt = max_over_ranks((time.perf_counter() - t0) / steps, world)
+        e2e = {"value": layer.flops * world / dt / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": bi,
+               "d2h_bytes_per_step": bo, "ms_per_step": dt * 1e3}
+        del host_in, host_out
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        import oracle as o
+        lins = [(n, K, N) for n, (K, N) in layer.linears.items()]
+        shapes = [(n, lay, m, k, nn) for n, lay, m, k, nn in layer.shapes]
+        t0 = time.perf_counter()
+        sec, info = oracle_sample(shapes, layer.M, lins, rows=2, cols=128, slab=16)
+        wall = time.perf_counter() - t0
+        cpu = {"value": layer.flops / sec / 1e12, "unit": "TFLOP/s", "cores": o.num_threads(), "kind": "oracle",
+               "sample": "per GEMM 2x128 outputs of the FP64 oracle GEMM on NVFP4 operands plus their NVFP4 "
+                         "quantization, projected to the full layer (quantize share %.0f%%)"
+                         % (100 * info["quant_s"] / sec),
+               "wall_s": wall}
+
+    if rank == 0:
+        line = {
+            "metric": "quantize+GEMM TFLOP/s & % of FP8/FP4 peak; ms/layer (CodonFM-5B shape)",
+            "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": {"nvfp4": "e2m1", "mxfp8": "e4m3", "fp8_current": "e4m3/e5m2", "fp8_delayed": "e4m3/e5m2",
+                      "bf16": "bf16"}[recipe],
+            "data": "synthetic",
+            "config": {"workload": f"CodonFM-5B layer, 12 GEMMs, {recipe} {'autocast' if autocast else 'pre-quantize'}"
+                                   f" (M={layer.M}, hidden {args.hidden_size}, intermediate {args.intermediate_size})",
+                       "global_batch": args.micro_batch_size * world, "seq_len": args.sequence_length,
+                       "parallelism": f"replicas x{world}", "l2": "inputs larger than L2 (working set > 4 GB)"},
+            "roofline": roof,
+            "quantize": {"ms_per_layer": quant_ms, "gemm_ms_per_layer": gemm_ms},
+            "recipes": recipes,
+            "gemms": {n: {kk: (round(v, 4) if isinstance(v, float) else v) for kk, v in r.items()}
+                      for n, r in table.items()},
+            "clocks": clk,
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+            "gpu_launches": layer.kernels_per_step(recipe, autocast) * args.steps,
+            "hbm_peak_gbs": hbm,
+        }
+        if args.output:
+            json.dump(line, open(args.output, "w"), indent=1)
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_setup(args)
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_lpq(args, rank, world, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

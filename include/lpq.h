@@ -1,0 +1,234 @@
+/*
+ * lpq — block-scaled low-precision quantize-then-GEMM for transformer linear
+ * layers on GB300 (sm_103a).  C ABI of liblpq.so.
+ *
+ * What the library computes is defined by these pages:
+ *   [FP8]   "Optimizing Transformer models for low-precision training"
+ *           (setupai.cc summary), "technical deep dive": E4M3 (1/4/3 bits,
+ *           forward activations and weights) and E5M2 (1/5/2, gradients);
+ *           per-tensor dynamic scaling from the amax; amax history.
+ *   [NVFP4] "Accelerate LLM training with NVFP4 on Blackwell" (setupai.cc
+ *           summary), "technical deep dive": E2M1 values (range about +-6), an
+ *           E4M3 scale per 16-value micro-block plus an FP32 tensor scale.
+ *   [TE]    "How to optimize Transformer-based models for low-precision
+ *           training" (developer.nvidia.cn): config -> 12 GEMM shapes
+ *           ("model configuration and training input", "autocast vs
+ *           pre-quantize"), Fprop/Dgrad/Wgrad benchmarked separately,
+ *           pre-quantize mode, the NVFP4 extra costs (random Hadamard
+ *           transform on Wgrad inputs, stochastic rounding of gradients, 2D
+ *           weight blocks, extra amax pass) and silent fallbacks to avoid
+ *           ("interpreting real-model results").
+ *   [NeMo]  "Faster training throughput in FP8 with NVIDIA NeMo", "advantages
+ *           and trade-offs": delayed, current, sub-channel (1x128 / 128x128)
+ *           and MXFP8 (32-value blocks, E8M0 power-of-two scales).
+ *
+ * Conventions for every entry point:
+ *   - Device pointers are owned by the caller; the library allocates no device
+ *     memory (TMEM inside kernels is allocated and released per launch).
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream) and the call returns without synchronising.
+ *   - Every call returns an lpq_status; nothing throws across the ABI.  A
+ *     non-OK status leaves a message readable with lpq_last_error() on the
+ *     calling thread.  A call that returns non-OK has enqueued nothing unless
+ *     the status is LPQ_ERR_CUDA.
+ *   - No call ever falls back to another format, precision or a CPU path
+ *     ([TE] warns of silent fallbacks): an unsupported combination is an error.
+ *   - Matrices are row-major and contiguous along their last dimension.
+ */
+#ifndef LPQ_H_
+#define LPQ_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *lpq_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+  LPQ_OK = 0,
+  LPQ_ERR_INVALID_ARG = 1, /* NULL pointer, bad enum or flag */
+  LPQ_ERR_SHAPE = 2,       /* a dimension is not a multiple of the block / tile rule */
+  LPQ_ERR_ALIGN = 3,       /* a pointer is not 16-byte aligned */
+  LPQ_ERR_UNSUPPORTED = 4, /* format / layout / operand pairing not provided */
+  LPQ_ERR_ARCH = 5,        /* current device is not compute capability 10.3 */
+  LPQ_ERR_CUDA = 6,        /* a CUDA runtime call failed */
+  LPQ_ERR_TIMEOUT = 7      /* a device-side wait gave up (see lpq_device_status) */
+} lpq_status;
+
+typedef enum {
+  LPQ_BF16 = 0,               /* unquantized bf16 (the speed-up baseline) */
+  LPQ_FP8_E4M3 = 1,           /* per-tensor scaled E4M3 [FP8] */
+  LPQ_FP8_E5M2 = 2,           /* per-tensor scaled E5M2 [FP8] */
+  LPQ_MXFP8 = 3,              /* E4M3 codes, one E8M0 scale per 32 values [NeMo] */
+  LPQ_NVFP4 = 4,              /* E2M1 codes, E4M3 scale per 16 + FP32 tensor scale [NVFP4] */
+  LPQ_NVFP4_2D = 5,           /* NVFP4 with one scale per 16x16 tile (weights) [TE] */
+  LPQ_FP8_BLOCK_1x128 = 6,    /* E4M3, FP32 scale per 1x128 block (activations) [NeMo] */
+  LPQ_FP8_BLOCK_128x128 = 7   /* E4M3, FP32 scale per 128x128 block (weights) [NeMo] */
+} lpq_format;
+
+typedef enum { LPQ_SCALING_CURRENT = 0, LPQ_SCALING_DELAYED = 1 } lpq_scaling;
+
+/* lpq_quantize flags */
+enum {
+  LPQ_ROWWISE = 1,     /* emit the row-wise copy [rows, cols] */
+  LPQ_COLWISE = 2,     /* emit the column-wise copy [cols, rows] (re-blocked along rows) */
+  LPQ_RHT_COLWISE = 4, /* NVFP4: 16-point random-sign Hadamard on the column-wise copy */
+  LPQ_STOCHASTIC = 8   /* NVFP4: stochastic rounding of the E2M1 codes (both copies) */
+};
+
+/* Scale-factor layouts of a copy. */
+enum {
+  LPQ_SF_PLAIN = 0, /* [rows, cols / block] row-major (FP8 block: FP32 [rows / br, cols / 128]) */
+  LPQ_SF_GEMM = 1   /* tensor-core layout read by lpq_gemm (see lpq_copy_bytes) */
+};
+
+/* One quantized copy of a matrix.  All pointers are device pointers.
+ *   codes        [rows, cols] bytes (FP8 formats), [rows, cols / 2] packed
+ *                E2M1 (NVFP4: low nibble = even column), or bf16 [rows, cols].
+ *   scales       block scales: u8 E8M0 (MXFP8), u8 E4M3 (NVFP4), FP32
+ *                scale_inv (FP8 block); NULL for per-tensor FP8 and bf16.
+ *   tensor_scale one FP32 dequantization factor: scale_inv for per-tensor
+ *                FP8, the FP32 tensor scale for NVFP4; NULL otherwise.
+ *   amax         one FP32: max |value| of this copy's input values (after the
+ *                Hadamard transform for an RHT copy).  Required for per-tensor
+ *                FP8 and NVFP4 (lpq_quantize writes it), optional otherwise.
+ *   rows, cols   dimensions of this copy (the column-wise copy of an
+ *                [R, C] tensor is [C, R]).
+ *   colwise      1 for a column-wise copy, 0 for a row-wise copy.        */
+typedef struct {
+  void *codes;
+  void *scales;
+  float *tensor_scale;
+  float *amax;
+  int64_t rows, cols;
+  int32_t fmt;       /* lpq_format */
+  int32_t sf_layout; /* LPQ_SF_PLAIN or LPQ_SF_GEMM */
+  int32_t colwise;
+  int32_t reserved;
+} lpq_qview;
+
+typedef struct {
+  lpq_qview row, col;
+} lpq_qtensor;
+
+/* Delayed-scaling state of one tensor role ([FP8] amax history; [NeMo]
+ * per-tensor delayed scaling).  Device pointers.  Initial state: history all
+ * 0, pos 0, scale 1, scale_inv 1.  The state is raw FP32/INT32 arrays, so a
+ * checkpoint is a copy of them. */
+typedef struct {
+  float *amax_history; /* [len] */
+  int32_t *pos;        /* next slot of the ring */
+  float *scale;        /* scale used by the next quantize */
+  float *scale_inv;
+  int32_t len;         /* 1..1024; the workloads use 16 */
+} lpq_delayed_state;
+
+/* Bytes of one copy's codes and scales for format `fmt`, a copy of `rows` x
+ * `cols` and scale layout `sf_layout`.  Host-only, needs no GPU.
+ * LPQ_SF_GEMM layout for MXFP8 / NVFP4: 128-row groups x KT atoms of 512
+ * bytes; atom (g, t) starts at (g * KT + t) * 512 and holds, for row
+ * r = 128 g + 32 j + i (i < 32, j < 4), its 4 scales of column-blocks
+ * 4t .. 4t+3 at bytes 16 i + 4 j + 0..3.  KT = ceil(cols / 128) for MXFP8 and
+ * 4 * ceil(cols / 256) for NVFP4; entries beyond the matrix read as 0.
+ * LPQ_SF_GEMM for FP8_BLOCK_1x128 is FP32 [cols / 128, rows] (rows fastest);
+ * for FP8_BLOCK_128x128 it equals the plain layout. */
+lpq_status lpq_copy_bytes(int32_t fmt, int64_t rows, int64_t cols, int32_t sf_layout,
+                          size_t *codes_bytes, size_t *scale_bytes);
+
+/* Quantizes x [rows, cols] bf16 (device) into the copies `flags` selects.
+ *   fmt            LPQ_FP8_E4M3/E5M2 (with `scaling`), LPQ_MXFP8, LPQ_NVFP4,
+ *                  LPQ_NVFP4_2D, LPQ_FP8_BLOCK_*, or LPQ_BF16 (row-wise =
+ *                  copy, column-wise = transpose).
+ *   scaling        per-tensor FP8 only.  CURRENT: scale = fmax / amax(x)
+ *                  from an extra amax pass.  DELAYED: scale = *state->scale
+ *                  from earlier steps; amax(x) is measured in the same pass
+ *                  and written to out->row.amax (or col.amax); the state is
+ *                  NOT advanced — call lpq_scale_update with that amax.
+ *   seed, counter_offset   stochastic rounding: Philox-4x32-10 key = seed,
+ *                  element j of a copy (row-major index + counter_offset)
+ *                  uses word j mod 4 of counter (j / 4, copy id, 0).
+ *                  counter_offset must be a multiple of 4.
+ *   rht_seed       the 16 Hadamard signs: bits of word 0 of
+ *                  Philox(key = (rht_seed, 0), counter = (0, 0, 2, 0)).
+ *   out            views to fill; out->row used if LPQ_ROWWISE, out->col if
+ *                  LPQ_COLWISE.  Each view's rows/cols/fmt must match.
+ * Shape rules: cols a multiple of the row-wise block (16 NVFP4, 32 MXFP8, 128
+ * FP8 block, 16 NVFP4_2D), rows a multiple of the column-wise block when
+ * LPQ_COLWISE is set (same numbers; 128x128 needs neither rows nor cols beyond
+ * cols % 128 == 0 and rows % 128 == 0 for its column copy), and every row of
+ * every output 16-byte aligned.  A 0 x n or n x 0 input is valid and enqueues
+ * nothing but the scalar outputs. */
+lpq_status lpq_quantize(const void *x, int64_t rows, int64_t cols, int32_t fmt, int32_t scaling,
+                        uint32_t flags, uint64_t seed, uint64_t counter_offset, uint32_t rht_seed,
+                        const lpq_delayed_state *state, lpq_qtensor *out, lpq_stream_t stream);
+
+/* Delayed-scaling update (one CTA): history[pos] = *amax; pos = (pos+1) % len;
+ * m = max(history); scale = fmax / m if m > 0 and finite (else unchanged);
+ * scale_inv = 1 / scale.  fmax is 448 (E4M3) or 57344 (E5M2). */
+lpq_status lpq_scale_update(const lpq_delayed_state *state, const float *amax, float fmax,
+                            lpq_stream_t stream);
+
+/* Which copies a GEMM of a linear layer reads ([TE]: Fprop, Dgrad and Wgrad
+ * are separate GEMMs).  X [M, K] activations, W [N, K] weights, dY [M, N]:
+ *   LPQ_FPROP  Y  = X W^T   : a = X row-wise,   b = W row-wise   -> C [M, N]
+ *   LPQ_DGRAD  dX = dY W    : a = dY row-wise,  b = W col-wise   -> C [M, K]
+ *   LPQ_WGRAD  dW = dY^T X  : a = dY col-wise,  b = X col-wise   -> C [N, K]
+ * The layout only states which copies are expected (checked against the
+ * views' `colwise` flags); the arithmetic is the same. */
+typedef enum { LPQ_FPROP = 0, LPQ_DGRAD = 1, LPQ_WGRAD = 2 } lpq_layout;
+
+/* C[m, n] = sum_k deq(a)[m, k] * deq(b)[n, k], FP32 accumulation on the
+ * tensor cores (tcgen05), output bf16 (c_is_fp32 = 0) or FP32, row-major with
+ * leading dimension n.  a is [m, k], b is [n, k], both contiguous along k.
+ * Legal pairings: BF16 x BF16; {E4M3, E5M2} x {E4M3, E5M2} (per-tensor,
+ * scale_inv product applied in the epilogue); MXFP8 x MXFP8; {NVFP4,
+ * NVFP4_2D} x {NVFP4, NVFP4_2D} (tensor scales in the epilogue); FP8 block
+ * (1x128 or 128x128) x FP8 block (FP32 block scales applied per 128-deep
+ * slice).  Block-scaled operands must use LPQ_SF_GEMM.  k must be a multiple
+ * of 32 (128 for FP8 block); m and n are arbitrary (>= 0).  Anything else
+ * returns LPQ_ERR_UNSUPPORTED or LPQ_ERR_SHAPE; nothing falls back. */
+lpq_status lpq_gemm(int32_t layout, const lpq_qview *a, const lpq_qview *b, void *c, int32_t c_is_fp32,
+                    int64_t m, int64_t n, int64_t k, lpq_stream_t stream);
+
+/* Transformer configuration ([TE] "model configuration and training input"). */
+typedef struct {
+  int64_t hidden, intermediate, heads, layers, micro_batch, seq;
+} lpq_transformer_cfg;
+
+typedef struct {
+  char name[24];   /* e.g. "qkv_fprop" */
+  int32_t layout;  /* lpq_layout */
+  int64_t m, k, n; /* C [m, n] = sum over k */
+} lpq_gemm_shape;
+
+/* The 12 GEMMs of one layer: M = micro_batch * seq; QKV (K = hidden,
+ * N = 3 hidden), attention out (hidden, hidden), MLP up (hidden,
+ * intermediate), MLP down (intermediate, hidden), each as Fprop (M, K, N),
+ * Dgrad (M, N, K) and Wgrad (N, M, K).  `heads` and `layers` do not change
+ * the linear shapes.  Host-only. */
+lpq_status lpq_layer_shapes(const lpq_transformer_cfg *cfg, lpq_gemm_shape out[12], int32_t *count);
+
+/* Text of the last non-OK status on this thread ("" if none). */
+const char *lpq_last_error(void);
+
+/* Synchronises `stream`, then reads and clears the device error word that
+ * kernels set when a bounded wait gives up (0 = none, else an lpq_status). */
+lpq_status lpq_device_status(lpq_stream_t stream, int32_t *code);
+
+/* Failure-detection check: launches one CTA whose bounded wait (the same
+ * helper the GEMM pipeline uses) waits on a barrier that nothing completes.
+ * After limit_ns (0 < limit_ns <= 1 s) the wait gives up and records
+ * LPQ_ERR_TIMEOUT in the device error word, which lpq_device_status then
+ * returns; the CUDA context stays usable.  No fault, trap or hang is involved. */
+lpq_status lpq_selftest_wait(uint64_t limit_ns, lpq_stream_t stream);
+
+/* Library version (major * 10000 + minor * 100 + patch). */
+int32_t lpq_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* LPQ_H_ */

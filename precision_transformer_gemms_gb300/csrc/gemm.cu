@@ -1,0 +1,388 @@
+// Tensor-core GEMMs of liblpq on sm_103a: C[m, n] = sum_k A[m, k] B[n, k]
+// with both operands contiguous along k ("TN"), as every Fprop, Dgrad and
+// Wgrad of a linear layer is posed ("How to optimize Transformer-based models
+// for low-precision training", autocast vs pre-quantize: the 12 GEMMs of a
+// layer, benchmarked separately per pass).
+//
+// One CTA computes a 128 x BN output tile.  Warp 0 (one lane) streams A/B
+// tiles into a shared-memory ring with TMA (128-byte swizzle) and the block
+// scale factors with bulk copies; warp 1 (one lane) moves scale factors into
+// TMEM (tcgen05.cp) and issues the tcgen05.mma instructions, accumulating in
+// FP32 in TMEM; all four warps then read the accumulator back with
+// tcgen05.ld, apply the per-tensor scale product and store bf16 or FP32.
+//
+// Kinds: kind::f16 (bf16 x bf16), kind::f8f6f4 (per-tensor E4M3/E5M2),
+// kind::mxf8f6f4.block_scale (MXFP8: E4M3 with an E8M0 scale per 32 values,
+// "Faster training throughput in FP8 with NVIDIA NeMo", MXFP8) and
+// kind::mxf4nvf4.block_scale (NVFP4: E2M1 with an E4M3 scale per 16 values and
+// an FP32 tensor scale, "Accelerate LLM training with NVFP4 on Blackwell").
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_bf16.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "lpq_device.cuh"
+
+namespace lpq {
+
+// Device error word: set when a bounded wait inside a kernel of this library
+// gives up; read and cleared by lpq_device_status.
+__device__ int g_device_error = 0;
+
+namespace {
+
+constexpr int kBM = 128;
+constexpr int kKBytes = 128;  // bytes of K per pipeline stage (one 128-byte swizzle row)
+
+template <int KIND, int BN>
+struct Cfg {
+  static constexpr int kSfAtoms = KIND == kKindNVF4 ? 4 : (KIND == kKindMXF8 ? 1 : 0);  // per 128 rows
+  static constexpr int kA = kBM * kKBytes;
+  static constexpr int kB = BN * kKBytes;
+  static constexpr int kSfa = kSfAtoms * 512;
+  static constexpr int kSfb = kSfAtoms * 512 * (BN / 128);
+  static constexpr int kStages = 4;
+  static constexpr int kStage = kA + kB + kSfa + kSfb;
+  static constexpr int kSmem = kStages * kStage + 1024 /*align slack*/ + 256 /*barriers*/;
+  static constexpr int kSfaCols = kSfAtoms * 4;
+  static constexpr int kSfbCols = kSfAtoms * 4 * (BN / 128);
+  static constexpr int kTmemCols = (BN + kSfaCols + kSfbCols) <= 256 ? 256 : 512;
+};
+
+struct GemmArgs {
+  const uint8_t* sfa;  // tensor-core scale layout of A (block-scaled kinds)
+  const uint8_t* sfb;
+  int64_t sfa_kt, sfb_kt;  // atoms per 128-row group
+  int64_t sfb_groups;      // 128-row groups of B
+  void* c;
+  int64_t M, N, K;
+  int c_fp32;
+  const float* alpha_a;  // per-tensor factors (may be NULL)
+  const float* alpha_b;
+  uint32_t idesc;
+  int num_k;  // k-tiles of kKBytes
+};
+
+template <int KIND, int BN>
+__global__ void __launch_bounds__(128, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const GemmArgs g) {
+  using CF = Cfg<KIND, BN>;
+  constexpr int S = CF::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = sA + S * CF::kA;
+  uint8_t* sSfa = sB + S * CF::kB;
+  uint8_t* sSfb = sSfa + S * CF::kSfa;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sSfb + S * CF::kSfb);
+  uint64_t* empty = full + S;
+  uint64_t* accbar = empty + S;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accbar + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t m0 = (int64_t)blockIdx.y * kBM, n0 = (int64_t)blockIdx.x * BN;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(accbar, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, CF::kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const uint32_t tmem_d = tmem_base;
+  const uint32_t tmem_sfa = tmem_base + BN;
+  const uint32_t tmem_sfb = tmem_sfa + CF::kSfaCols;
+
+  if (warp == 0 && lane == 0) {
+    // ------------------------------------------------------------ producer
+    const int elem_per_kt = KIND == kKindF16 ? kKBytes / 2 : kKBytes;  // TMA x unit: elements (bf16) or bytes
+    const int64_t ga = m0 / 128;
+    for (int kt = 0; kt < g.num_k; ++kt) {
+      const int s = kt % S;
+      const uint32_t ph = (uint32_t)(kt / S) & 1u;
+      if (!mbar_wait_bounded(&empty[s], ph ^ 1u, abort_flag, &g_device_error)) break;
+      mbar_arrive_expect_tx(&full[s], CF::kStage);
+      tma_load_2d(sA + s * CF::kA, &tmA, kt * elem_per_kt, (int32_t)m0, &full[s]);
+      tma_load_2d(sB + s * CF::kB, &tmB, kt * elem_per_kt, (int32_t)n0, &full[s]);
+      if constexpr (CF::kSfAtoms > 0) {
+        bulk_load(sSfa + s * CF::kSfa, g.sfa + (ga * g.sfa_kt + (int64_t)kt * CF::kSfAtoms) * 512, CF::kSfa,
+                  &full[s]);
+#pragma unroll
+        for (int i = 0; i < BN / 128; ++i) {
+          int64_t gb = n0 / 128 + i;
+          if (gb >= g.sfb_groups) gb = g.sfb_groups - 1;
+          bulk_load(sSfb + s * CF::kSfb + i * CF::kSfAtoms * 512,
+                    g.sfb + (gb * g.sfb_kt + (int64_t)kt * CF::kSfAtoms) * 512, CF::kSfAtoms * 512, &full[s]);
+        }
+      }
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ------------------------------------------------------------ MMA issuer
+    for (int kt = 0; kt < g.num_k; ++kt) {
+      const int s = kt % S;
+      const uint32_t ph = (uint32_t)(kt / S) & 1u;
+      if (!mbar_wait_bounded(&full[s], ph, abort_flag, &g_device_error)) break;
+      tc_fence_after();
+      const uint32_t a_base = smem_u32(sA + s * CF::kA);
+      const uint32_t b_base = smem_u32(sB + s * CF::kB);
+      if constexpr (KIND == kKindMXF8) {
+        tmem_cp_sf(tmem_sfa, smem_desc(smem_u32(sSfa + s * CF::kSfa), 0, 128, 0));
+#pragma unroll
+        for (int i = 0; i < BN / 128; ++i)
+          tmem_cp_sf(tmem_sfb + 4 * i, smem_desc(smem_u32(sSfb + s * CF::kSfb + i * 512), 0, 128, 0));
+      } else if constexpr (KIND == kKindNVF4) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          tmem_cp_sf(tmem_sfa + 4 * j, smem_desc(smem_u32(sSfa + s * CF::kSfa + j * 512), 0, 128, 0));
+#pragma unroll
+          for (int i = 0; i < BN / 128; ++i)
+            tmem_cp_sf(tmem_sfb + 4 * (BN / 128) * j + 4 * i,
+                       smem_desc(smem_u32(sSfb + s * CF::kSfb + (i * 4 + j) * 512), 0, 128, 0));
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint64_t ad = smem_desc(a_base + 32 * j, 16, 1024, 2);
+        const uint64_t bd = smem_desc(b_base + 32 * j, 16, 1024, 2);
+        const uint32_t acc = (kt > 0 || j > 0) ? 1u : 0u;
+        if constexpr (KIND == kKindF16 || KIND == kKindF8F6F4) {
+          mma_ss<KIND>(tmem_d, ad, bd, g.idesc, acc);
+        } else if constexpr (KIND == kKindMXF8) {
+          const uint32_t id = g.idesc | ((uint32_t)j << 4) | ((uint32_t)j << 29);
+          mma_bs<KIND>(tmem_d, ad, bd, id, tmem_sfa, tmem_sfb, acc);
+        } else {
+          mma_bs<KIND>(tmem_d, ad, bd, g.idesc, tmem_sfa + 4 * j, tmem_sfb + 4 * (BN / 128) * j, acc);
+        }
+      }
+      tc_commit(&empty[s]);
+    }
+    tc_commit(accbar);
+  }
+
+  // -------------------------------------------------------------- epilogue (all 4 warps)
+  __syncwarp();
+  const bool ok = mbar_wait_bounded(accbar, 0, abort_flag, &g_device_error);
+  __syncwarp();
+  tc_fence_after();
+  float alpha = 1.0f;
+  if (g.alpha_a) alpha = *g.alpha_a;
+  if (g.alpha_b) alpha = __fmul_rn(alpha, *g.alpha_b);
+  const int64_t row = m0 + warp * 32 + lane;
+  const bool vec_ok = g.c_fp32 ? (g.N % 4 == 0) : (g.N % 8 == 0);
+#pragma unroll 1
+  for (int cc = 0; cc < BN / 32; ++cc) {
+    uint32_t v[32];
+    tmem_ld32(tmem_d + ((uint32_t)(warp * 32) << 16) + (uint32_t)(cc * 32), v);
+    const int64_t col0 = n0 + cc * 32;
+    if (!ok || row >= g.M || col0 >= g.N) continue;
+    const bool full_run = vec_ok && col0 + 32 <= g.N;
+    if (g.c_fp32) {
+      float* out = static_cast<float*>(g.c) + row * g.N + col0;
+      if (full_run) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          reinterpret_cast<float4*>(out)[i] =
+              make_float4(__fmul_rn(__uint_as_float(v[4 * i]), alpha), __fmul_rn(__uint_as_float(v[4 * i + 1]), alpha),
+                          __fmul_rn(__uint_as_float(v[4 * i + 2]), alpha), __fmul_rn(__uint_as_float(v[4 * i + 3]), alpha));
+      } else {
+        for (int i = 0; i < 32 && col0 + i < g.N; ++i) out[i] = __fmul_rn(__uint_as_float(v[i]), alpha);
+      }
+    } else {
+      __nv_bfloat16* out = static_cast<__nv_bfloat16*>(g.c) + row * g.N + col0;
+      if (full_run) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          __nv_bfloat162 h = __floats2bfloat162_rn(__fmul_rn(__uint_as_float(v[2 * i]), alpha),
+                                                   __fmul_rn(__uint_as_float(v[2 * i + 1]), alpha));
+          pk[i] = *reinterpret_cast<uint32_t*>(&h);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          reinterpret_cast<uint4*>(out)[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+      } else {
+        for (int i = 0; i < 32 && col0 + i < g.N; ++i) out[i] = __float2bfloat16_rn(__fmul_rn(__uint_as_float(v[i]), alpha));
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, CF::kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------------ host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 2D map over a row-major [rows, inner] matrix whose rows are `row_bytes`
+// apart; box = box_inner x box_rows, 128-byte swizzle, zero fill outside.
+lpq_status make_map(CUtensorMap* map, const void* base, bool bf16, int64_t inner, int64_t rows, int64_t row_bytes,
+                    uint32_t box_inner, uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return set_error(LPQ_ERR_CUDA, "cuTensorMapEncodeTiled unavailable from the driver");
+  cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)(rows > 0 ? rows : 1)};
+  cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+  cuuint32_t box[2] = {box_inner, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
+                  const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return set_error(LPQ_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return LPQ_OK;
+}
+
+// Instruction descriptors (tcgen05): D format F32 in bits 4-5 (dense kinds),
+// A/B formats in 7-9 / 10-12, K-major A and B (bits 15, 16 clear), N >> 3 in
+// 17-22, M >> 4 in 24-28; block-scaled kinds put the scale type in bit 23
+// (1 = E8M0, 0 = E4M3) and the scale-factor selectors in 4-5 (B) and 29-30 (A).
+uint32_t idesc_dense(uint32_t afmt, uint32_t bfmt, int n) {
+  return (1u << 4) | (afmt << 7) | (bfmt << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
+}
+uint32_t idesc_block_scaled(uint32_t afmt, uint32_t bfmt, uint32_t e8m0, int n) {
+  return (afmt << 7) | (bfmt << 10) | ((uint32_t)(n >> 3) << 17) | (e8m0 << 23) | ((uint32_t)(kBM >> 4) << 24);
+}
+
+template <int KIND, int BN>
+lpq_status run(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& g, cudaStream_t s) {
+  using CF = Cfg<KIND, BN>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<KIND, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, CF::kSmem);
+    if (e != cudaSuccess) return cuda_check(e, "cudaFuncSetAttribute(gemm smem)");
+    attr_set = true;
+  }
+  dim3 grid((unsigned)((g.N + BN - 1) / BN), (unsigned)((g.M + kBM - 1) / kBM));
+  if (grid.y > 65535u) return set_error(LPQ_ERR_SHAPE, "m too large for one launch");
+  gemm_kernel<KIND, BN><<<grid, 128, CF::kSmem, s>>>(ta, tb, g);
+  return cuda_check(cudaGetLastError(), "gemm kernel launch");
+}
+
+}  // namespace
+
+lpq_status launch_gemm(const lpq_qview* a, const lpq_qview* b, void* c, int32_t c_is_fp32, int64_t m, int64_t n,
+                       int64_t k, cudaStream_t s) {
+  if (m == 0 || n == 0) return LPQ_OK;
+  const int32_t fa = a->fmt, fb = b->fmt;
+  GemmArgs g{};
+  g.c = c;
+  g.M = m;
+  g.N = n;
+  g.K = k;
+  g.c_fp32 = c_is_fp32;
+  if (k == 0) {
+    // Empty reduction: C = 0.
+    size_t bytes = (size_t)m * (size_t)n * (c_is_fp32 ? 4 : 2);
+    return cuda_check(cudaMemsetAsync(c, 0, bytes, s), "cudaMemsetAsync(C)");
+  }
+  CUtensorMap ta, tb;
+  lpq_status st;
+  constexpr int BN = 256;
+  if (fa == LPQ_BF16) {
+    g.num_k = (int)((k * 2 + kKBytes - 1) / kKBytes);
+    if ((st = make_map(&ta, a->codes, true, k, m, k * 2, 64, kBM)) != LPQ_OK) return st;
+    if ((st = make_map(&tb, b->codes, true, k, n, k * 2, 64, BN)) != LPQ_OK) return st;
+    g.idesc = idesc_dense(1, 1, BN);  // BF16 x BF16 -> F32
+    return run<kKindF16, BN>(ta, tb, g, s);
+  }
+  if (fa == LPQ_FP8_E4M3 || fa == LPQ_FP8_E5M2) {
+    g.num_k = (int)((k + kKBytes - 1) / kKBytes);
+    if ((st = make_map(&ta, a->codes, false, k, m, k, 128, kBM)) != LPQ_OK) return st;
+    if ((st = make_map(&tb, b->codes, false, k, n, k, 128, BN)) != LPQ_OK) return st;
+    g.idesc = idesc_dense(fa == LPQ_FP8_E5M2 ? 1 : 0, fb == LPQ_FP8_E5M2 ? 1 : 0, BN);
+    g.alpha_a = a->tensor_scale;
+    g.alpha_b = b->tensor_scale;
+    return run<kKindF8F6F4, BN>(ta, tb, g, s);
+  }
+  if (fa == LPQ_MXFP8) {
+    g.num_k = (int)((k + kKBytes - 1) / kKBytes);
+    if ((st = make_map(&ta, a->codes, false, k, m, k, 128, kBM)) != LPQ_OK) return st;
+    if ((st = make_map(&tb, b->codes, false, k, n, k, 128, BN)) != LPQ_OK) return st;
+    g.idesc = idesc_block_scaled(0, 0, 1, BN);  // E4M3 x E4M3, E8M0 scales
+    g.sfa = static_cast<const uint8_t*>(a->scales);
+    g.sfb = static_cast<const uint8_t*>(b->scales);
+    g.sfa_kt = sf_kt_atoms(LPQ_MXFP8, k);
+    g.sfb_kt = g.sfa_kt;
+    g.sfb_groups = sf_row_groups(n);
+    return run<kKindMXF8, BN>(ta, tb, g, s);
+  }
+  if (fa == LPQ_NVFP4 || fa == LPQ_NVFP4_2D) {
+    g.num_k = (int)((k / 2 + kKBytes - 1) / kKBytes);
+    if ((st = make_map(&ta, a->codes, false, k / 2, m, k / 2, 128, kBM)) != LPQ_OK) return st;
+    if ((st = make_map(&tb, b->codes, false, k / 2, n, k / 2, 128, BN)) != LPQ_OK) return st;
+    g.idesc = idesc_block_scaled(1, 1, 0, BN);  // E2M1 x E2M1, E4M3 scales
+    g.sfa = static_cast<const uint8_t*>(a->scales);
+    g.sfb = static_cast<const uint8_t*>(b->scales);
+    g.sfa_kt = sf_kt_atoms(LPQ_NVFP4, k);
+    g.sfb_kt = g.sfa_kt;
+    g.sfb_groups = sf_row_groups(n);
+    g.alpha_a = a->tensor_scale;
+    g.alpha_b = b->tensor_scale;
+    return run<kKindNVF4, BN>(ta, tb, g, s);
+  }
+  return set_error(LPQ_ERR_UNSUPPORTED, "no GEMM kernel for format %d", fa);
+}
+
+// One CTA waits with the bounded wait on a barrier that nothing completes;
+// used to check that a wait that runs out reports LPQ_ERR_TIMEOUT and leaves
+// the context usable.
+__global__ void selftest_wait_kernel(uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) mbar_wait_bounded(&bar, 0, &abort_flag, &g_device_error, limit_ns);
+}
+
+lpq_status launch_selftest_wait(uint64_t limit_ns, cudaStream_t s) {
+  selftest_wait_kernel<<<1, 32, 0, s>>>(limit_ns);
+  return cuda_check(cudaGetLastError(), "selftest kernel launch");
+}
+
+lpq_status read_and_clear_device_error(cudaStream_t s, int32_t* code) {
+  lpq_status st = cuda_check(cudaStreamSynchronize(s), "cudaStreamSynchronize");
+  if (st != LPQ_OK) return st;
+  int v = 0;
+  if ((st = cuda_check(cudaMemcpyFromSymbol(&v, g_device_error, sizeof(int)), "read device error word")) != LPQ_OK)
+    return st;
+  const int zero = 0;
+  if ((st = cuda_check(cudaMemcpyToSymbol(g_device_error, &zero, sizeof(int)), "clear device error word")) != LPQ_OK)
+    return st;
+  *code = v;
+  return LPQ_OK;
+}
+
+}  // namespace lpq

@@ -1,0 +1,335 @@
+// Device helpers for liblpq: format arithmetic (exactly one IEEE rounding per
+// float operation, no contraction), the counter-based generator, the 16-point
+// Hadamard butterfly, and thin inline-PTX wrappers for mbarrier, TMA and the
+// fifth-generation tensor core (tcgen05) on sm_103a.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "lpq_internal.h"
+
+namespace lpq {
+
+// ------------------------------------------------------------------ bf16 / fp32
+__device__ __forceinline__ float bf16_lo(uint32_t pair) { return __uint_as_float(pair << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t pair) { return __uint_as_float(pair & 0xFFFF0000u); }
+
+// 8 bf16 from a 16-byte vector into floats (exact).
+__device__ __forceinline__ void unpack8(const uint4& v, float f[8]) {
+  f[0] = bf16_lo(v.x); f[1] = bf16_hi(v.x);
+  f[2] = bf16_lo(v.y); f[3] = bf16_hi(v.y);
+  f[4] = bf16_lo(v.z); f[5] = bf16_hi(v.z);
+  f[6] = bf16_lo(v.w); f[7] = bf16_hi(v.w);
+}
+
+// max(|x|) that ignores NaN (fmaxf returns the non-NaN operand).
+__device__ __forceinline__ float absmax_acc(float m, float x) { return fmaxf(m, fabsf(x)); }
+
+__device__ __forceinline__ bool finite_pos(float a) { return a > 0.f && a <= 3.402823466e38f; }
+
+// ------------------------------------------------------------------ conversions
+// Two fp32 -> packed E4M3 / E5M2 bytes, round-to-nearest-even, saturating.
+// Result byte 0 encodes `lo`, byte 1 encodes `hi`.
+__device__ __forceinline__ uint16_t cvt_e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+__device__ __forceinline__ uint16_t cvt_e5m2x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+// Two fp32 -> packed E2M1 nibbles (low nibble encodes `lo`), RNE, saturating.
+__device__ __forceinline__ uint32_t cvt_e2m1x2(float lo, float hi) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 t;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\t"
+      "cvt.u32.u8 %0, t;\n\t}"
+      : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+template <bool kE5M2>
+__device__ __forceinline__ uint16_t cvt_fp8x2(float lo, float hi) {
+  if constexpr (kE5M2) return cvt_e5m2x2(lo, hi); else return cvt_e4m3x2(lo, hi);
+}
+
+// Value of an E4M3 code 0..0x7E as fp32 (exact: via the f16 conversion).
+__device__ __forceinline__ float e4m3_value(uint32_t code) {
+  uint32_t h2;
+  uint16_t in = (uint16_t)(code & 0xFF);
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(in));
+  return __half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFF)));
+}
+
+// 2^k as fp32 for k in [-127, 127]; 2^-127 is the subnormal 0x00400000.
+__device__ __forceinline__ float pow2_exact(int k) {
+  return k >= -126 ? __uint_as_float((uint32_t)(k + 127) << 23) : __uint_as_float(0x00400000u);
+}
+
+// MXFP8 block exponent: the smallest e with 448 * 2^e >= a (a >= 0), from the
+// exact decomposition a = m * 2^E: e = E - 8 + (m > 1.75), clamped to
+// [-127, 127]; a = 0 gives -127, a non-finite amax gives 127.
+__device__ __forceinline__ int mx_exponent(float a) {
+  if (a == 0.f) return -127;
+  uint32_t b = __float_as_uint(a);
+  uint32_t be = (b >> 23) & 0xFF, frac = b & 0x7FFFFF;
+  if (be == 0xFF) return 127;
+  int E;
+  if (be == 0) {  // subnormal: normalise the significand
+    int p = 31 - __clz(frac);
+    E = p - 149;
+    frac = (frac << (23 - p)) & 0x7FFFFF;
+  } else {
+    E = (int)be - 127;
+  }
+  int e = E - 8 + (frac > 0x600000u ? 1 : 0);
+  return e < -127 ? -127 : (e > 127 ? 127 : e);
+}
+
+// ------------------------------------------------------------------ Philox-4x32-10
+// Salmon et al., SC'11: per round the even words are multiplied by the two
+// multipliers, hi/lo halves mixed with the odd words and the round key; the
+// key is bumped by the Weyl constants between rounds.
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    if (r > 0) { k0 += 0x9E3779B9u; k1 += 0xBB67AE85u; }
+    uint32_t lo0 = 0xD2511F53u * c.x, hi0 = __umulhi(0xD2511F53u, c.x);
+    uint32_t lo1 = 0xCD9E8D57u * c.z, hi1 = __umulhi(0xCD9E8D57u, c.z);
+    c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+  }
+  return c;
+}
+
+// 4 random words for elements j = 4g .. 4g+3 of copy `copy_id`.
+__device__ __forceinline__ uint4 sr_words(uint64_t seed, uint64_t g, uint32_t copy_id) {
+  return philox4x32_10(make_uint4((uint32_t)g, (uint32_t)(g >> 32), copy_id, 0u), (uint32_t)seed,
+                       (uint32_t)(seed >> 32));
+}
+
+__device__ __forceinline__ uint32_t rht_signs(uint32_t rht_seed) {
+  return philox4x32_10(make_uint4(0u, 0u, 2u, 0u), rht_seed, 0u).x & 0xFFFFu;
+}
+
+// 16-point random-sign Hadamard: sign flip, butterfly stages h = 1, 2, 4, 8
+// ((t_i, t_{i+h}) -> (t_i + t_{i+h}, t_i - t_{i+h})), then * 1/4.
+__device__ __forceinline__ void rht16(float t[16], uint32_t signs) {
+#pragma unroll
+  for (int j = 0; j < 16; ++j)
+    if ((signs >> j) & 1u) t[j] = -t[j];
+#pragma unroll
+  for (int h = 1; h < 16; h <<= 1)
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      if ((i & h) == 0) {
+        float a = t[i], b = t[i + h];
+        t[i] = __fadd_rn(a, b);
+        t[i + h] = __fsub_rn(a, b);
+      }
+#pragma unroll
+  for (int j = 0; j < 16; ++j) t[j] = __fmul_rn(0.25f, t[j]);
+}
+
+// Stochastic E2M1 code of y with random word r: between adjacent magnitudes
+// lo <= |y| <= hi, round up iff float(r >> 8) < ((|y| - lo) / (hi - lo)) * 2^24.
+__device__ __forceinline__ uint32_t sr_e2m1(float y, uint32_t r) {
+  if (y != y) return 0x7u;
+  uint32_t s = (__float_as_uint(y) >> 31) << 3;
+  float a = fabsf(y);
+  if (a >= 6.0f) return s | 7u;
+  uint32_t lo;
+  float vlo, vhi;
+  if (a < 0.5f) { lo = 0; vlo = 0.f; vhi = 0.5f; }
+  else if (a < 1.0f) { lo = 1; vlo = 0.5f; vhi = 1.f; }
+  else if (a < 1.5f) { lo = 2; vlo = 1.f; vhi = 1.5f; }
+  else if (a < 2.0f) { lo = 3; vlo = 1.5f; vhi = 2.f; }
+  else if (a < 3.0f) { lo = 4; vlo = 2.f; vhi = 3.f; }
+  else if (a < 4.0f) { lo = 5; vlo = 3.f; vhi = 4.f; }
+  else { lo = 6; vlo = 4.f; vhi = 6.f; }
+  float frac = __fdiv_rn(__fsub_rn(a, vlo), __fsub_rn(vhi, vlo));
+  bool up = (float)(r >> 8) < __fmul_rn(frac, 16777216.0f);
+  return s | (up ? lo + 1 : lo);
+}
+
+// ------------------------------------------------------------------ warp helpers
+__device__ __forceinline__ float warp_max_xor(float v, int width_lanes) {
+  for (int o = 1; o < width_lanes; o <<= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+  return v;
+}
+
+// Non-negative floats order like their bit patterns.
+__device__ __forceinline__ void atomic_max_nonneg(float* addr, float v) {
+  atomicMax(reinterpret_cast<int*>(addr), __float_as_int(v));
+}
+
+// ------------------------------------------------------------------ GEMM scale layout
+// Byte offset of scale (row r, column-block kb) in the tensor-core layout:
+// 128-row groups of KT atoms of 512 bytes; inside an atom, row 32 j + i (i <
+// 32) keeps its 4 consecutive column-block scales at bytes 16 i + 4 j.
+__device__ __forceinline__ int64_t sf_gemm_offset(int64_t r, int64_t kb, int64_t kt_atoms) {
+  return ((r >> 7) * kt_atoms + (kb >> 2)) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4 + (kb & 3);
+}
+
+// ------------------------------------------------------------------ mbarrier / TMA / tcgen05
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ uint64_t global_timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Bounded wait for the phase of `parity` to complete.  Gives up after
+// `limit_ns` (or as soon as *abort is set by another thread of the CTA):
+// records LPQ_ERR_TIMEOUT in *err (first writer wins), sets *abort and
+// returns false.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort, int* err,
+                                                  uint64_t limit_ns = kWaitLimitNs) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (;;) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort) return false;
+    if (global_timer_ns() - t0 > limit_ns) {
+      atomicCAS(err, 0, (int)LPQ_ERR_TIMEOUT);
+      *abort = 1;
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int32_t x, int32_t y,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];"
+      ::"r"(smem_u32(dst)), "l"(map), "r"(smem_u32(bar)), "r"(x), "r"(y)
+      : "memory");
+}
+// Plain bulk copy global -> shared (16-byte aligned, size multiple of 16).
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
+}
+
+// tcgen05 ----------------------------------------------------------------------
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
+               "r"(ncols) : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// Arrive on `bar` once all earlier tcgen05 operations of this thread finish.
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   smem_u32(bar)) : "memory");
+}
+
+// Shared-memory matrix descriptor (tcgen05): start address >> 4 in bits 0-13,
+// leading byte offset >> 4 in 16-29, stride byte offset >> 4 in 32-45, the
+// fixed version 1 in 46-47, swizzle mode in 61-63 (2 = 128-byte swizzle,
+// 0 = none).
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo, uint32_t swizzle) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)((lbo & 0x3FFFFu) >> 4) << 16;
+  d |= (uint64_t)((sbo & 0x3FFFFu) >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)(swizzle & 7) << 61;
+  return d;
+}
+
+// D(tmem) (+)= A(smem) * B(smem)^T, kinds without block scales.
+template <int kKind>
+__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                       uint32_t accumulate) {
+  if constexpr (kKind == kKindF16) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate) : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate) : "memory");
+  }
+}
+
+// Block-scaled MMA with scale factors in TMEM.
+template <int kKind>
+__device__ __forceinline__ void mma_bs(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                       uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  if constexpr (kKind == kKindMXF8) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
+        ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
+        ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+  }
+}
+
+// Copy 32 rows x 16 bytes of scale factors from shared memory into 4 TMEM
+// columns, replicated into all four 32-lane quarters.
+__device__ __forceinline__ void tmem_cp_sf(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
+// Load 32 consecutive fp32 columns of this warp's 32 TMEM lanes.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+      "%14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+        "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]),
+        "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]),
+        "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+}  // namespace lpq

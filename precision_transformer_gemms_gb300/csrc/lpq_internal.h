@@ -1,0 +1,43 @@
+// Internal declarations shared by the translation units of liblpq.
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "lpq.h"
+
+namespace lpq {
+
+// Device-side bounded waits give up after this long (a healthy wait in these
+// kernels lasts microseconds).
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
+
+// Tensor-core instruction kinds used by the GEMM kernels.
+enum { kKindF16 = 0, kKindF8F6F4 = 1, kKindMXF8 = 2, kKindNVF4 = 3 };
+
+// Thread-local error text (capi.cu).
+lpq_status set_error(lpq_status st, const char* fmt, ...);
+lpq_status cuda_check(cudaError_t e, const char* what);
+
+// Scale-factor geometry of the tensor-core layout.
+inline int64_t sf_kt_atoms(int32_t fmt, int64_t cols) {
+  if (fmt == LPQ_MXFP8) return (cols + 127) / 128;
+  return ((cols + 255) / 256) * 4;  // NVFP4 / NVFP4_2D
+}
+inline int64_t sf_row_groups(int64_t rows) { return (rows + 127) / 128; }
+
+// Quantizer launchers (quantize.cu).  `x` bf16 [rows, cols]; views validated.
+lpq_status launch_quantize(const void* x, int64_t rows, int64_t cols, int32_t fmt, int32_t scaling,
+                           uint32_t flags, uint64_t seed, uint64_t counter_offset, uint32_t rht_seed,
+                           const lpq_delayed_state* state, lpq_qtensor* out, cudaStream_t stream);
+lpq_status launch_scale_update(const lpq_delayed_state* state, const float* amax, float fmax,
+                               cudaStream_t stream);
+
+// GEMM launcher (gemm.cu).  Operands validated.
+lpq_status launch_gemm(const lpq_qview* a, const lpq_qview* b, void* c, int32_t c_is_fp32, int64_t m,
+                       int64_t n, int64_t k, cudaStream_t stream);
+
+// Device error word (gemm.cu owns it).
+lpq_status read_and_clear_device_error(cudaStream_t stream, int32_t* code);
+lpq_status launch_selftest_wait(uint64_t limit_ns, cudaStream_t stream);
+
+}  // namespace lpq

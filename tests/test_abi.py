@@ -1,0 +1,97 @@
+"""CPU checks of the C ABI library: it loads, exports every entry point the
+header declares, its host-only helpers agree with the oracle and the pages,
+and argument validation returns the documented status codes without a GPU."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle as o
+from precision_transformer_gemms_gb300 import lpq
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "lpq.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(lpq_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_function():
+    names = declared_functions()
+    assert len(names) >= 9
+    L = lpq.lib()
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_layer_shapes_match_oracle():
+    got = lpq.layer_shapes(4096, 16384, 31, 512)
+    want = o.layer_shapes(4096, 16384, 31, 512)
+    assert [(n, m, k, nn) for n, _, m, k, nn in got] == want
+    assert [lay for _, lay, *_ in got] == [0, 1, 2] * 4
+
+
+def test_copy_bytes():
+    assert lpq.copy_bytes(lpq.NVFP4, 15872, 4096, lpq.SF_PLAIN) == (15872 * 2048, 15872 * 256)
+    # 4 bits per value + one byte per 16 values = 4.5 bits per value
+    cb, sb = lpq.copy_bytes(lpq.NVFP4, 1024, 4096, lpq.SF_PLAIN)
+    assert (cb + sb) * 8 / (1024 * 4096) == 4.5
+    assert lpq.copy_bytes(lpq.MXFP8, 256, 512, lpq.SF_GEMM) == (256 * 512, 2 * 4 * 512)
+    assert lpq.copy_bytes(lpq.NVFP4, 300, 544, lpq.SF_GEMM)[1] == 3 * (4 * 3) * 512
+    assert lpq.copy_bytes(lpq.FP8_BLOCK_1x128, 256, 512, lpq.SF_GEMM) == (256 * 512, 4 * 256 * 4)
+    assert lpq.copy_bytes(lpq.BF16, 3, 16, lpq.SF_PLAIN) == (96, 0)
+    with pytest.raises(lpq.LpqError) as e:
+        lpq.copy_bytes(lpq.MXFP8, 4, 48)
+    assert e.value.status == lpq.ERR_SHAPE
+
+
+def _quantize_raw(x_ptr, rows, cols, fmt, flags, scaling=0, ctr=0, out=None, state=None):
+    out = out or lpq.QTensorC()
+    return lpq.lib().lpq_quantize(x_ptr, rows, cols, fmt, scaling, flags, 0, ctr, 0, state, ctypes.byref(out), None)
+
+
+def test_quantize_validation_codes():
+    assert _quantize_raw(None, 4, 32, 99, lpq.ROWWISE) == lpq.ERR_INVALID_ARG
+    assert _quantize_raw(None, 4, 32, lpq.MXFP8, 0) == lpq.ERR_INVALID_ARG
+    assert _quantize_raw(None, 4, 32, lpq.MXFP8, lpq.ROWWISE | lpq.STOCHASTIC) == lpq.ERR_UNSUPPORTED
+    assert _quantize_raw(None, 4, 32, lpq.NVFP4, lpq.ROWWISE | lpq.RHT_COLWISE) == lpq.ERR_INVALID_ARG
+    assert _quantize_raw(None, 4, 32, lpq.NVFP4, lpq.ROWWISE, ctr=2) == lpq.ERR_INVALID_ARG
+    assert _quantize_raw(None, 4, 32, lpq.MXFP8, lpq.ROWWISE, scaling=1) == lpq.ERR_UNSUPPORTED
+    assert _quantize_raw(None, 4, 32, lpq.FP8_E4M3, lpq.ROWWISE, scaling=1) == lpq.ERR_INVALID_ARG  # no state
+    assert _quantize_raw(None, 4, 32, lpq.MXFP8, lpq.ROWWISE) == lpq.ERR_INVALID_ARG  # x NULL
+    assert _quantize_raw(ctypes.c_void_p(8), 4, 32, lpq.MXFP8, lpq.ROWWISE) == lpq.ERR_ALIGN
+    assert _quantize_raw(ctypes.c_void_p(16), 4, 40, lpq.MXFP8, lpq.ROWWISE) == lpq.ERR_SHAPE
+    assert _quantize_raw(ctypes.c_void_p(16), 40, 32, lpq.MXFP8, lpq.COLWISE) == lpq.ERR_SHAPE  # rows % 32
+    # a view that does not match the request
+    out = lpq.QTensorC()
+    out.row = lpq.QView(16, 16, 16, 16, 4, 64, lpq.MXFP8, lpq.SF_GEMM, 0, 0)
+    assert _quantize_raw(ctypes.c_void_p(16), 4, 32, lpq.MXFP8, lpq.ROWWISE, out=out) == lpq.ERR_SHAPE
+    assert "expected" in lpq.last_error()
+
+
+def test_gemm_validation_codes():
+    L = lpq.lib()
+
+    def view(fmt, rows, cols, colwise=0):
+        return lpq.QView(16, 16, 16, 16, rows, cols, fmt, lpq.SF_GEMM, colwise, 0)
+
+    a, b = view(lpq.MXFP8, 128, 256), view(lpq.NVFP4, 64, 256)
+    call = lambda lay, a, b, m, n, k, c=16: L.lpq_gemm(lay, ctypes.byref(a), ctypes.byref(b), c, 0, m, n, k, None)
+    assert call(0, a, b, 128, 64, 256) == lpq.ERR_UNSUPPORTED  # mixed formats never fall back
+    assert call(0, a, view(lpq.MXFP8, 64, 256), 128, 64, 128) == lpq.ERR_SHAPE  # k mismatch
+    assert call(1, a, view(lpq.MXFP8, 64, 256), 128, 64, 256) == lpq.ERR_INVALID_ARG  # dgrad wants b col-wise
+    assert call(7, a, a, 128, 128, 256) == lpq.ERR_INVALID_ARG
+    assert call(0, view(lpq.MXFP8, 128, 48), view(lpq.MXFP8, 64, 48), 128, 64, 48) == lpq.ERR_SHAPE
+    assert call(0, a, view(lpq.MXFP8, 64, 256), 128, 64, 256, c=8) == lpq.ERR_ALIGN
+
+
+def test_scale_update_and_selftest_validation():
+    L = lpq.lib()
+    st = lpq.DelayedStateC(None, None, None, None, 16)
+    assert L.lpq_scale_update(ctypes.byref(st), None, 448.0, None) == lpq.ERR_INVALID_ARG
+    assert L.lpq_selftest_wait(0, None) == lpq.ERR_INVALID_ARG
+    assert L.lpq_selftest_wait(5_000_000_000, None) == lpq.ERR_INVALID_ARG

@@ -1,0 +1,162 @@
+"""GPU parity of the tensor-core GEMMs: every checked output element must satisfy
+|C - C_ref| <= 1e-3 * sum_k |a b| against the oracle's FP64 GEMM of the
+dequantized operands (plus half a bf16 ulp of C for bf16 output)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as o
+from precision_transformer_gemms_gb300 import lpq
+from lpq_testutil import bf16_input, gemm_gate, oracle_operand
+
+pytestmark = pytest.mark.gpu
+
+# (M, K, N): tiny, the MXFP8 tiny case, ragged M/N/K tails, several tiles in every dimension
+SHAPES = [(4, 32, 16), (256, 512, 384), (300, 544, 200), (520, 1056, 776)]
+
+
+def quantize_pair(fmt_a, fmt_b, M, K, N, seed=0):
+    xa, _ = bf16_input((M, K), std=1.0, seed=seed, outlier_frac=0.001, outlier_scale=50)
+    xb, _ = bf16_input((N, K), std=0.02, seed=seed + 1)
+    if fmt_a == lpq.BF16:
+        return lpq.Copy.of_bf16(xa), lpq.Copy.of_bf16(xb)
+    qa = lpq.quantize(xa, fmt_a, lpq.ROWWISE)
+    qb = lpq.quantize(xb, fmt_b, lpq.ROWWISE)
+    return qa.row, qb.row
+
+
+def check(a, b, M, N, K, out_fp32, layout=lpq.FPROP):
+    c = lpq.gemm(layout, a, b, out_fp32=out_fp32)
+    torch.cuda.synchronize()
+    assert lpq.device_status() == 0
+    ref, bound = o.gemm(oracle_operand(a), oracle_operand(b), M, N, K)
+    nbad, worst = gemm_gate(c, ref, bound, not out_fp32)
+    assert nbad == 0, f"{nbad} elements outside the gate (worst {worst:.3g}x)"
+
+
+@pytest.mark.parametrize("out_fp32", [True, False])
+@pytest.mark.parametrize("shape", SHAPES)
+@pytest.mark.parametrize("fmts", [(lpq.BF16, lpq.BF16), (lpq.FP8_E4M3, lpq.FP8_E4M3), (lpq.FP8_E5M2, lpq.FP8_E4M3),
+                                  (lpq.MXFP8, lpq.MXFP8), (lpq.NVFP4, lpq.NVFP4), (lpq.NVFP4, lpq.NVFP4_2D)])
+def test_gemm_parity(fmts, shape, out_fp32):
+    M, K, N = shape
+    if fmts[1] == lpq.NVFP4_2D and N % 16:
+        pytest.skip("2D weight tiles need N % 16 == 0")
+    a, b = quantize_pair(*fmts, M, K, N)
+    check(a, b, M, N, K, out_fp32)
+
+
+def test_gemm_closed_form_all_ones():
+    """All-ones operands: every output is exactly K (MXFP8 scales are exact
+    powers of two, so the products are exact)."""
+    M, K, N = 256, 1024, 256
+    x = torch.ones((M, K), dtype=torch.bfloat16, device="cuda")
+    y = torch.ones((N, K), dtype=torch.bfloat16, device="cuda")
+    for fmt in (lpq.MXFP8, lpq.NVFP4, lpq.BF16):
+        if fmt == lpq.BF16:
+            a, b = lpq.Copy.of_bf16(x), lpq.Copy.of_bf16(y)
+        else:
+            a, b = lpq.quantize(x, fmt, lpq.ROWWISE).row, lpq.quantize(y, fmt, lpq.ROWWISE).row
+        c = lpq.gemm(lpq.FPROP, a, b, out_fp32=True)
+        torch.cuda.synchronize()
+        ref, _ = o.gemm(oracle_operand(a), oracle_operand(b), 1, 1, K, pairs=np.array([[0, 0]]))
+        assert float(ref[0]) == pytest.approx(K, rel=1e-6)
+        if fmt == lpq.NVFP4:  # the FP32 tensor scales 1/2688 are rounded: K up to a few ulps
+            assert torch.allclose(c, torch.full_like(c, float(ref[0])), rtol=1e-6, atol=0), fmt
+        else:
+            assert torch.all(c == float(ref[0])), (fmt, float(ref[0]), c.flatten()[:4])
+
+
+def test_gemm_single_nonzero_k():
+    M, K, N = 128, 256, 256
+    x = torch.zeros((M, K), dtype=torch.bfloat16, device="cuda")
+    y = torch.zeros((N, K), dtype=torch.bfloat16, device="cuda")
+    x[:, 77] = 3.0
+    y[:, 77] = -2.0
+    for fmt in (lpq.MXFP8, lpq.FP8_E4M3, lpq.NVFP4, lpq.BF16):
+        if fmt == lpq.BF16:
+            a, b = lpq.Copy.of_bf16(x), lpq.Copy.of_bf16(y)
+        else:
+            a, b = lpq.quantize(x, fmt, lpq.ROWWISE).row, lpq.quantize(y, fmt, lpq.ROWWISE).row
+        c = lpq.gemm(lpq.FPROP, a, b, out_fp32=True)
+        torch.cuda.synchronize()
+        ref, _ = o.gemm(oracle_operand(a), oracle_operand(b), 1, 1, K, pairs=np.array([[0, 0]]))
+        assert torch.allclose(c, torch.full_like(c, float(ref[0])), rtol=1e-6), fmt
+
+
+@pytest.mark.parametrize("fmt", [lpq.MXFP8, lpq.NVFP4, lpq.FP8_E4M3, lpq.BF16])
+def test_fprop_dgrad_wgrad_layouts(fmt):
+    """The three GEMMs of a linear layer on the copies each one reads."""
+    M, K, N = 256, 512, 384
+    X, _ = bf16_input((M, K), std=1.0, seed=20)
+    W, _ = bf16_input((N, K), std=0.02, seed=21)
+    dY, _ = bf16_input((M, N), std=1e-3, seed=22)
+    both = lpq.ROWWISE | lpq.COLWISE
+    if fmt == lpq.BF16:
+        qx, qw, qd = (lpq.quantize(t, fmt, both) for t in (X, W, dY))
+    elif fmt == lpq.NVFP4:
+        qx = lpq.quantize(X, fmt, both | lpq.RHT_COLWISE, rht_seed=9)
+        qw = lpq.quantize(W, lpq.NVFP4_2D, both)
+        qd = lpq.quantize(dY, fmt, both | lpq.RHT_COLWISE | lpq.STOCHASTIC, seed=3, rht_seed=9)
+    elif fmt == lpq.FP8_E4M3:
+        qx = lpq.quantize(X, fmt, both)
+        qw = lpq.quantize(W, fmt, both)
+        qd = lpq.quantize(dY, lpq.FP8_E5M2, both)
+    else:
+        qx, qw, qd = (lpq.quantize(t, fmt, both) for t in (X, W, dY))
+    check(qx.row, qw.row, M, N, K, True, lpq.FPROP)      # Y  [M, N]
+    check(qd.row, qw.col, M, K, N, True, lpq.DGRAD)      # dX [M, K]
+    check(qd.col, qx.col, N, K, M, True, lpq.WGRAD)      # dW [N, K]
+
+
+@pytest.mark.parametrize("fmt", [lpq.NVFP4, lpq.MXFP8])
+def test_full_size_sampled(fmt):
+    """QKV Fprop at the layer's size (15872 x 4096 x 12288): the first and last
+    128 x 128 output tiles and 4096 uniformly sampled elements."""
+    M, K, N = 15872, 4096, 12288
+    X, _ = bf16_input((M, K), std=1.0, seed=30)
+    W, _ = bf16_input((N, K), std=0.02, seed=31)
+    qx = lpq.quantize(X, fmt, lpq.ROWWISE)
+    qw = lpq.quantize(W, lpq.NVFP4_2D if fmt == lpq.NVFP4 else fmt, lpq.ROWWISE)
+    c = lpq.gemm(lpq.FPROP, qx.row, qw.row)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(0)
+    first = np.array([(m, n) for m in range(128) for n in range(128)])
+    last = np.array([(M - 128 + m, N - 128 + n) for m in range(128) for n in range(128)])
+    rand = np.stack([rng.integers(0, M, 4096), rng.integers(0, N, 4096)], 1)
+    pairs = np.concatenate([first, last, rand]).astype(np.int64)
+    ref, bound = o.gemm(oracle_operand(qx.row), oracle_operand(qw.row), M, N, K, pairs)
+    got = c[torch.from_numpy(pairs[:, 0]).cuda(), torch.from_numpy(pairs[:, 1]).cuda()]
+    nbad, worst = gemm_gate(got, ref, bound, True)
+    assert nbad == 0, f"{nbad} bad (worst {worst:.3g}x)"
+
+
+def test_empty_and_zero_k():
+    a = lpq.Copy(lpq.MXFP8, 0, 128, False)
+    b = lpq.Copy(lpq.MXFP8, 64, 128, False)
+    c = lpq.gemm(lpq.FPROP, a, b)
+    assert c.shape == (0, 64)
+    x = torch.empty((64, 0), dtype=torch.bfloat16, device="cuda")
+    c = lpq.gemm(lpq.FPROP, lpq.Copy.of_bf16(x), lpq.Copy.of_bf16(torch.empty((32, 0), dtype=torch.bfloat16,
+                                                                               device="cuda")), out_fp32=True)
+    torch.cuda.synchronize()
+    assert torch.all(c == 0)
+
+
+def test_no_fallback_on_mixed_formats():
+    x, _ = bf16_input((128, 128), seed=40)
+    a = lpq.quantize(x, lpq.MXFP8, lpq.ROWWISE).row
+    b = lpq.quantize(x, lpq.NVFP4, lpq.ROWWISE).row
+    with pytest.raises(lpq.LpqError) as e:
+        lpq.gemm(lpq.FPROP, a, b)
+    assert e.value.status == lpq.ERR_UNSUPPORTED
+
+
+def test_bounded_wait_reports_timeout_and_context_survives():
+    assert lpq.device_status() == 0
+    lpq.selftest_wait(20_000_000)  # 20 ms
+    assert lpq.device_status() == lpq.ERR_TIMEOUT
+    assert lpq.device_status() == 0  # read clears it
+    x, bits = bf16_input((64, 128), seed=41)
+    q = lpq.quantize(x, lpq.MXFP8, lpq.ROWWISE)
+    assert np.array_equal(q.row.codes_matrix().cpu().numpy(), o.mxfp8(bits, colwise=False)["row"])
