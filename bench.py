@@ -57,6 +57,8 @@ def parse():
     p.add_argument("--sequence_length", type=int, default=512)
     p.add_argument("--seed", type=int, default=0)
     p.add_argument("-o", "--output", default=None, help="write the per-GEMM table as JSON here")
+    p.add_argument("--mma-peaks", action="store_true",
+                   help="only measure the dense tcgen05 rates (shared-memory-resident operands) and exit")
     return p.parse_args()
 
 
@@ -527,8 +529,29 @@ def run_lpq(args, rank, world, local):
         print(json.dumps(line), flush=True)
 
 
+def run_mma_peaks(args):
+    """Dense tcgen05 rates per kind, operands resident in shared memory."""
+    import torch
+    from precision_transformer_gemms_gb300 import lpq
+    torch.cuda.set_device(0)
+    clocks = ClockSampler(0)
+    clocks.start()
+    out = {}
+    for kind in ("bf16", "fp8", "mxfp8", "nvfp4"):
+        iters = 40000 if kind == "nvfp4" else 20000
+        out[kind] = lpq.mma_peak(kind, iters=iters, with_scale_copies=False)
+        if kind in ("mxfp8", "nvfp4"):
+            out[kind + "_with_scale_copies"] = lpq.mma_peak(kind, iters=iters, with_scale_copies=True)
+    out["clocks"] = clocks.stop()
+    out["unit"] = "TFLOP/s"
+    print(json.dumps(out), flush=True)
+
+
 def main():
     args = parse()
+    if args.mma_peaks:
+        run_mma_peaks(args)
+        return
     rank, world, local = dist_setup(args)
     if args.impl == "reference":
         run_reference(args, rank, world)

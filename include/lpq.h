@@ -225,6 +225,15 @@ lpq_status lpq_device_status(lpq_stream_t stream, int32_t *code);
  * returns; the CUDA context stays usable.  No fault, trap or hang is involved. */
 lpq_status lpq_selftest_wait(uint64_t limit_ns, lpq_stream_t stream);
 
+/* Tensor-core rate measurement (the dense peaks the roofline divides by):
+ * one CTA per SM issues `iters` k-steps of four 128 x 256 tcgen05.mma on
+ * zero operands resident in shared memory; kind 0 = kind::f16 (bf16, K 16),
+ * 1 = kind::f8f6f4 (E4M3, K 32), 2 = MXFP8 block-scaled (K 32), 3 = NVFP4
+ * block-scaled (K 64).  with_scale_copies adds the per-step tcgen05.cp of the
+ * scale factors (kinds 2, 3).  FLOPs = SMs * iters * 4 * 2 * 128 * 256 * K;
+ * the caller times the launch with events on `stream`. */
+lpq_status lpq_mma_peak(int32_t kind, int32_t iters, int32_t with_scale_copies, lpq_stream_t stream);
+
 /* Library version (major * 10000 + minor * 100 + patch). */
 int32_t lpq_version(void);
 

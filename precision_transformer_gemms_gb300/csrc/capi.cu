@@ -269,4 +269,12 @@ lpq_status lpq_selftest_wait(uint64_t limit_ns, lpq_stream_t stream) {
   return launch_selftest_wait(limit_ns, reinterpret_cast<cudaStream_t>(stream));
 }
 
+lpq_status lpq_mma_peak(int32_t kind, int32_t iters, int32_t with_scale_copies, lpq_stream_t stream) {
+  if (kind < 0 || kind > 3) return set_error(LPQ_ERR_INVALID_ARG, "kind %d", kind);
+  if (iters < 1 || iters > (1 << 24)) return set_error(LPQ_ERR_INVALID_ARG, "iters %d", iters);
+  lpq_status st = check_arch();
+  if (st != LPQ_OK) return st;
+  return launch_mma_peak(kind, iters, with_scale_copies, reinterpret_cast<cudaStream_t>(stream));
+}
+
 }  // extern "C"

@@ -20,8 +20,10 @@
 #include <cuda_fp16.h>
 #include <cuda_bf16.h>
 #include <stdio.h>
+#include <stdlib.h>
 #include <string.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "lpq_device.cuh"
@@ -37,20 +39,26 @@ namespace {
 constexpr int kBM = 128;
 constexpr int kKBytes = 128;  // bytes of K per pipeline stage (one 128-byte swizzle row)
 
-template <int KIND, int BN>
+template <int KIND, int BN, int NACC>
 struct Cfg {
   static constexpr int kSfAtoms = KIND == kKindNVF4 ? 4 : (KIND == kKindMXF8 ? 1 : 0);  // per 128 rows
   static constexpr int kA = kBM * kKBytes;
   static constexpr int kB = BN * kKBytes;
   static constexpr int kSfa = kSfAtoms * 512;
   static constexpr int kSfb = kSfAtoms * 512 * (BN / 128);
-  static constexpr int kStages = 4;
   static constexpr int kStage = kA + kB + kSfa + kSfb;
-  static constexpr int kSmem = kStages * kStage + 1024 /*align slack*/ + 256 /*barriers*/;
+  static constexpr int kStages = (220 * 1024) / kStage > 8 ? 8 : (220 * 1024) / kStage;
+  static constexpr int kSmem = kStages * kStage + 1024 /*align slack*/ + 512 /*barriers*/;
   static constexpr int kSfaCols = kSfAtoms * 4;
   static constexpr int kSfbCols = kSfAtoms * 4 * (BN / 128);
-  static constexpr int kTmemCols = (BN + kSfaCols + kSfbCols) <= 256 ? 256 : 512;
+  static constexpr int kCols = NACC * BN + kSfaCols + kSfbCols;
+  static constexpr int kTmemCols = kCols <= 32 ? 32 : kCols <= 64 ? 64 : kCols <= 128 ? 128 : kCols <= 256 ? 256 : 512;
+  static_assert(kCols <= 512, "TMEM holds 512 columns");
+  static_assert(BN % 128 == 0 || kSfAtoms == 0, "scale atoms cover 128 rows");
 };
+
+constexpr int kGroupM = 16;  // tiles along M that share a band of B tiles (L2 reuse)
+constexpr int kThreadsGemm = 192;
 
 struct GemmArgs {
   const uint8_t* sfa;  // tensor-core scale layout of A (block-scaled kinds)
@@ -64,12 +72,30 @@ struct GemmArgs {
   const float* alpha_b;
   uint32_t idesc;
   int num_k;  // k-tiles of kKBytes
+  int tiles_m, tiles_n;
 };
 
-template <int KIND, int BN>
-__global__ void __launch_bounds__(128, 1)
+// Tile t of the persistent schedule -> (m tile, n tile): consecutive tiles
+// walk down a band of kGroupM m-tiles before moving to the next n-tile.
+__device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int& mt, int& nt) {
+  const int per_group = kGroupM * tiles_n;
+  const int group = t / per_group;
+  const int first_m = group * kGroupM;
+  const int gsize = min(kGroupM, tiles_m - first_m);
+  const int r = t - group * per_group;
+  mt = first_m + r % gsize;
+  nt = r / gsize;
+}
+
+// Persistent warp-specialized GEMM.  Warp 0: TMA producer; warp 1: TMEM
+// allocator and MMA issuer; warps 2..5: epilogue (warp w reads TMEM lanes
+// 32 * (w % 4) ..).  The shared-memory ring runs continuously across the
+// CTA's tiles; NACC accumulators in TMEM let the epilogue of one tile overlap
+// the main loop of the next.
+template <int KIND, int BN, int NACC>
+__global__ void __launch_bounds__(kThreadsGemm, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const GemmArgs g) {
-  using CF = Cfg<KIND, BN>;
+  using CF = Cfg<KIND, BN, NACC>;
   constexpr int S = CF::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -79,19 +105,23 @@ __global__ void __launch_bounds__(128, 1)
   uint8_t* sSfb = sSfa + S * CF::kSfa;
   uint64_t* full = reinterpret_cast<uint64_t*>(sSfb + S * CF::kSfb);
   uint64_t* empty = full + S;
-  uint64_t* accbar = empty + S;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accbar + 1);
+  uint64_t* acc_full = empty + S;
+  uint64_t* acc_empty = acc_full + NACC;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + NACC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t m0 = (int64_t)blockIdx.y * kBM, n0 = (int64_t)blockIdx.x * BN;
+  const int total = g.tiles_m * g.tiles_n;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    mbar_init(accbar, 1);
+    for (int a = 0; a < NACC; ++a) {
+      mbar_init(&acc_full[a], 1);
+      mbar_init(&acc_empty[a], 4);  // one arrive per epilogue warp
+    }
     *abort_flag = 0;
     fence_barrier_init();
     prefetch_tmap(&tmA);
@@ -102,119 +132,172 @@ __global__ void __launch_bounds__(128, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  const uint32_t tmem_d = tmem_base;
-  const uint32_t tmem_sfa = tmem_base + BN;
+  const uint32_t tmem_sfa = tmem_base + NACC * BN;
   const uint32_t tmem_sfb = tmem_sfa + CF::kSfaCols;
 
-  if (warp == 0 && lane == 0) {
-    // ------------------------------------------------------------ producer
-    const int elem_per_kt = KIND == kKindF16 ? kKBytes / 2 : kKBytes;  // TMA x unit: elements (bf16) or bytes
-    const int64_t ga = m0 / 128;
-    for (int kt = 0; kt < g.num_k; ++kt) {
-      const int s = kt % S;
-      const uint32_t ph = (uint32_t)(kt / S) & 1u;
-      if (!mbar_wait_bounded(&empty[s], ph ^ 1u, abort_flag, &g_device_error)) break;
-      mbar_arrive_expect_tx(&full[s], CF::kStage);
-      tma_load_2d(sA + s * CF::kA, &tmA, kt * elem_per_kt, (int32_t)m0, &full[s]);
-      tma_load_2d(sB + s * CF::kB, &tmB, kt * elem_per_kt, (int32_t)n0, &full[s]);
-      if constexpr (CF::kSfAtoms > 0) {
-        bulk_load(sSfa + s * CF::kSfa, g.sfa + (ga * g.sfa_kt + (int64_t)kt * CF::kSfAtoms) * 512, CF::kSfa,
-                  &full[s]);
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------------------------------------------------- producer
+      const int elem_per_kt = KIND == kKindF16 ? kKBytes / 2 : kKBytes;  // TMA x unit: elements (bf16) or bytes
+      uint32_t it = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        int mt, nt;
+        tile_coords(t, g.tiles_m, g.tiles_n, mt, nt);
+        const int32_t m0 = mt * kBM, n0 = nt * BN;
+        for (int kt = 0; kt < g.num_k; ++kt, ++it) {
+          const int s = it % S;
+          const uint32_t ph = (it / S) & 1u;
+          if (!(ok = mbar_wait_bounded(&empty[s], ph ^ 1u, abort_flag, &g_device_error))) break;
+          mbar_arrive_expect_tx(&full[s], CF::kStage);
+          tma_load_2d(sA + s * CF::kA, &tmA, kt * elem_per_kt, m0, &full[s]);
+          tma_load_2d(sB + s * CF::kB, &tmB, kt * elem_per_kt, n0, &full[s]);
+          if constexpr (CF::kSfAtoms > 0) {
+            bulk_load(sSfa + s * CF::kSfa, g.sfa + ((int64_t)mt * g.sfa_kt + (int64_t)kt * CF::kSfAtoms) * 512,
+                      CF::kSfa, &full[s]);
 #pragma unroll
-        for (int i = 0; i < BN / 128; ++i) {
-          int64_t gb = n0 / 128 + i;
-          if (gb >= g.sfb_groups) gb = g.sfb_groups - 1;
-          bulk_load(sSfb + s * CF::kSfb + i * CF::kSfAtoms * 512,
-                    g.sfb + (gb * g.sfb_kt + (int64_t)kt * CF::kSfAtoms) * 512, CF::kSfAtoms * 512, &full[s]);
+            for (int i = 0; i < BN / 128; ++i) {
+              int64_t gb = (int64_t)n0 / 128 + i;
+              if (gb >= g.sfb_groups) gb = g.sfb_groups - 1;
+              bulk_load(sSfb + s * CF::kSfb + i * CF::kSfAtoms * 512,
+                        g.sfb + (gb * g.sfb_kt + (int64_t)kt * CF::kSfAtoms) * 512, CF::kSfAtoms * 512, &full[s]);
+            }
+          }
         }
       }
     }
-  } else if (warp == 1 && lane == 0) {
-    // ------------------------------------------------------------ MMA issuer
-    for (int kt = 0; kt < g.num_k; ++kt) {
-      const int s = kt % S;
-      const uint32_t ph = (uint32_t)(kt / S) & 1u;
-      if (!mbar_wait_bounded(&full[s], ph, abort_flag, &g_device_error)) break;
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------------------------------------------------- MMA issuer
+      uint32_t it = 0, lt = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++lt) {
+        const uint32_t a = lt % NACC, aph = (lt / NACC) & 1u;
+        if (!(ok = mbar_wait_bounded(&acc_empty[a], aph ^ 1u, abort_flag, &g_device_error))) break;
+        tc_fence_after();
+        const uint32_t tmem_d = tmem_base + a * BN;
+        for (int kt = 0; kt < g.num_k; ++kt, ++it) {
+          const int s = it % S;
+          const uint32_t ph = (it / S) & 1u;
+          if (!(ok = mbar_wait_bounded(&full[s], ph, abort_flag, &g_device_error))) break;
+          tc_fence_after();
+          const uint32_t a_base = smem_u32(sA + s * CF::kA);
+          const uint32_t b_base = smem_u32(sB + s * CF::kB);
+          if constexpr (KIND == kKindMXF8) {
+            tmem_cp_sf(tmem_sfa, smem_desc(smem_u32(sSfa + s * CF::kSfa), 0, 128, 0));
+#pragma unroll
+            for (int i = 0; i < BN / 128; ++i)
+              tmem_cp_sf(tmem_sfb + 4 * i, smem_desc(smem_u32(sSfb + s * CF::kSfb + i * 512), 0, 128, 0));
+          } else if constexpr (KIND == kKindNVF4) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              tmem_cp_sf(tmem_sfa + 4 * j, smem_desc(smem_u32(sSfa + s * CF::kSfa + j * 512), 0, 128, 0));
+#pragma unroll
+              for (int i = 0; i < BN / 128; ++i)
+                tmem_cp_sf(tmem_sfb + 4 * (BN / 128) * j + 4 * i,
+                           smem_desc(smem_u32(sSfb + s * CF::kSfb + (i * 4 + j) * 512), 0, 128, 0));
+            }
+          }
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint64_t ad = smem_desc(a_base + 32 * j, 16, 1024, 2);
+            const uint64_t bd = smem_desc(b_base + 32 * j, 16, 1024, 2);
+            const uint32_t acc = (kt > 0 || j > 0) ? 1u : 0u;
+            if constexpr (KIND == kKindF16 || KIND == kKindF8F6F4) {
+              mma_ss<KIND>(tmem_d, ad, bd, g.idesc, acc);
+            } else if constexpr (KIND == kKindMXF8) {
+              const uint32_t id = g.idesc | ((uint32_t)j << 4) | ((uint32_t)j << 29);
+              mma_bs<KIND>(tmem_d, ad, bd, id, tmem_sfa, tmem_sfb, acc);
+            } else {
+              mma_bs<KIND>(tmem_d, ad, bd, g.idesc, tmem_sfa + 4 * j, tmem_sfb + 4 * (BN / 128) * j, acc);
+            }
+          }
+          tc_commit(&empty[s]);
+        }
+        if (ok) tc_commit(&acc_full[a]);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;  // TMEM lane quarter of this warp
+    float alpha = 1.0f;
+    if (g.alpha_a) alpha = *g.alpha_a;
+    if (g.alpha_b) alpha = __fmul_rn(alpha, *g.alpha_b);
+    const bool vec_ok = g.c_fp32 ? (g.N % 4 == 0) : (g.N % 8 == 0);
+    uint32_t lt = 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x, ++lt) {
+      int mt, nt;
+      tile_coords(t, g.tiles_m, g.tiles_n, mt, nt);
+      const uint32_t a = lt % NACC, aph = (lt / NACC) & 1u;
+      if (!mbar_wait_bounded(&acc_full[a], aph, abort_flag, &g_device_error)) break;
+      __syncwarp();
       tc_fence_after();
-      const uint32_t a_base = smem_u32(sA + s * CF::kA);
-      const uint32_t b_base = smem_u32(sB + s * CF::kB);
-      if constexpr (KIND == kKindMXF8) {
-        tmem_cp_sf(tmem_sfa, smem_desc(smem_u32(sSfa + s * CF::kSfa), 0, 128, 0));
-#pragma unroll
-        for (int i = 0; i < BN / 128; ++i)
-          tmem_cp_sf(tmem_sfb + 4 * i, smem_desc(smem_u32(sSfb + s * CF::kSfb + i * 512), 0, 128, 0));
-      } else if constexpr (KIND == kKindNVF4) {
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          tmem_cp_sf(tmem_sfa + 4 * j, smem_desc(smem_u32(sSfa + s * CF::kSfa + j * 512), 0, 128, 0));
-#pragma unroll
-          for (int i = 0; i < BN / 128; ++i)
-            tmem_cp_sf(tmem_sfb + 4 * (BN / 128) * j + 4 * i,
-                       smem_desc(smem_u32(sSfb + s * CF::kSfb + (i * 4 + j) * 512), 0, 128, 0));
-        }
-      }
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const uint64_t ad = smem_desc(a_base + 32 * j, 16, 1024, 2);
-        const uint64_t bd = smem_desc(b_base + 32 * j, 16, 1024, 2);
-        const uint32_t acc = (kt > 0 || j > 0) ? 1u : 0u;
-        if constexpr (KIND == kKindF16 || KIND == kKindF8F6F4) {
-          mma_ss<KIND>(tmem_d, ad, bd, g.idesc, acc);
-        } else if constexpr (KIND == kKindMXF8) {
-          const uint32_t id = g.idesc | ((uint32_t)j << 4) | ((uint32_t)j << 29);
-          mma_bs<KIND>(tmem_d, ad, bd, id, tmem_sfa, tmem_sfb, acc);
-        } else {
-          mma_bs<KIND>(tmem_d, ad, bd, g.idesc, tmem_sfa + 4 * j, tmem_sfb + 4 * (BN / 128) * j, acc);
-        }
-      }
-      tc_commit(&empty[s]);
-    }
-    tc_commit(accbar);
-  }
-
-  // -------------------------------------------------------------- epilogue (all 4 warps)
-  __syncwarp();
-  const bool ok = mbar_wait_bounded(accbar, 0, abort_flag, &g_device_error);
-  __syncwarp();
-  tc_fence_after();
-  float alpha = 1.0f;
-  if (g.alpha_a) alpha = *g.alpha_a;
-  if (g.alpha_b) alpha = __fmul_rn(alpha, *g.alpha_b);
-  const int64_t row = m0 + warp * 32 + lane;
-  const bool vec_ok = g.c_fp32 ? (g.N % 4 == 0) : (g.N % 8 == 0);
+      const int64_t row = (int64_t)mt * kBM + q * 32 + lane;
+      const uint32_t tbase = tmem_base + a * BN + ((uint32_t)(q * 32) << 16);
+      if (!g.c_fp32) {
+        // bf16 output, 128 columns at a time: drain TMEM into registers as
+        // packed bf16 pairs and store them; TMEM goes back to the MMA warp as
+        // soon as the last group is in registers, before its stores.
+        __nv_bfloat16* out_row = static_cast<__nv_bfloat16*>(g.c) + row * g.N + (int64_t)nt * BN;
+        const int64_t ncols = g.N - (int64_t)nt * BN;
 #pragma unroll 1
-  for (int cc = 0; cc < BN / 32; ++cc) {
-    uint32_t v[32];
-    tmem_ld32(tmem_d + ((uint32_t)(warp * 32) << 16) + (uint32_t)(cc * 32), v);
-    const int64_t col0 = n0 + cc * 32;
-    if (!ok || row >= g.M || col0 >= g.N) continue;
-    const bool full_run = vec_ok && col0 + 32 <= g.N;
-    if (g.c_fp32) {
-      float* out = static_cast<float*>(g.c) + row * g.N + col0;
-      if (full_run) {
+        for (int grp = 0; grp < BN / 128; ++grp) {
+          uint32_t pk[64];
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-          reinterpret_cast<float4*>(out)[i] =
-              make_float4(__fmul_rn(__uint_as_float(v[4 * i]), alpha), __fmul_rn(__uint_as_float(v[4 * i + 1]), alpha),
-                          __fmul_rn(__uint_as_float(v[4 * i + 2]), alpha), __fmul_rn(__uint_as_float(v[4 * i + 3]), alpha));
-      } else {
-        for (int i = 0; i < 32 && col0 + i < g.N; ++i) out[i] = __fmul_rn(__uint_as_float(v[i]), alpha);
-      }
-    } else {
-      __nv_bfloat16* out = static_cast<__nv_bfloat16*>(g.c) + row * g.N + col0;
-      if (full_run) {
-        uint32_t pk[16];
+          for (int cc = 0; cc < 4; ++cc) {
+            uint32_t v[32];
+            tmem_ld32(tbase + (uint32_t)(grp * 128 + cc * 32), v);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          __nv_bfloat162 h = __floats2bfloat162_rn(__fmul_rn(__uint_as_float(v[2 * i]), alpha),
-                                                   __fmul_rn(__uint_as_float(v[2 * i + 1]), alpha));
-          pk[i] = *reinterpret_cast<uint32_t*>(&h);
+            for (int i = 0; i < 16; ++i) {
+              __nv_bfloat162 h = __floats2bfloat162_rn(__fmul_rn(__uint_as_float(v[2 * i]), alpha),
+                                                       __fmul_rn(__uint_as_float(v[2 * i + 1]), alpha));
+              pk[cc * 16 + i] = *reinterpret_cast<uint32_t*>(&h);
+            }
+          }
+          if (grp == BN / 128 - 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_empty[a]);
+          }
+          if (row < g.M) {
+            __nv_bfloat16* out = out_row + grp * 128;
+            const int64_t nc = ncols - grp * 128;
+            if (vec_ok && nc >= 128) {
+#pragma unroll
+              for (int i = 0; i < 16; ++i)
+                reinterpret_cast<uint4*>(out)[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+            } else {
+#pragma unroll
+              for (int i = 0; i < 64; ++i) {
+                if (2 * i < nc) out[2 * i] = __ushort_as_bfloat16((unsigned short)(pk[i] & 0xFFFFu));
+                if (2 * i + 1 < nc) out[2 * i + 1] = __ushort_as_bfloat16((unsigned short)(pk[i] >> 16));
+              }
+            }
+          }
         }
+        continue;
+      }
+#pragma unroll 1
+      for (int cc = 0; cc < BN / 32; ++cc) {
+        uint32_t v[32];
+        tmem_ld32(tbase + (uint32_t)(cc * 32), v);
+        if (cc == BN / 32 - 1) {  // accumulator fully read: hand it back to the MMA warp
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&acc_empty[a]);
+        }
+        const int64_t col0 = (int64_t)nt * BN + cc * 32;
+        if (row >= g.M || col0 >= g.N) continue;
+        float* out = static_cast<float*>(g.c) + row * g.N + col0;
+        if (vec_ok && col0 + 32 <= g.N) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-          reinterpret_cast<uint4*>(out)[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
-      } else {
-        for (int i = 0; i < 32 && col0 + i < g.N; ++i) out[i] = __float2bfloat16_rn(__fmul_rn(__uint_as_float(v[i]), alpha));
+          for (int i = 0; i < 8; ++i)
+            reinterpret_cast<float4*>(out)[i] = make_float4(
+                __fmul_rn(__uint_as_float(v[4 * i]), alpha), __fmul_rn(__uint_as_float(v[4 * i + 1]), alpha),
+                __fmul_rn(__uint_as_float(v[4 * i + 2]), alpha), __fmul_rn(__uint_as_float(v[4 * i + 3]), alpha));
+        } else {
+          for (int i = 0; i < 32 && col0 + i < g.N; ++i) out[i] = __fmul_rn(__uint_as_float(v[i]), alpha);
+        }
       }
     }
   }
@@ -272,19 +355,42 @@ uint32_t idesc_block_scaled(uint32_t afmt, uint32_t bfmt, uint32_t e8m0, int n) 
   return (afmt << 7) | (bfmt << 10) | ((uint32_t)(n >> 3) << 17) | (e8m0 << 23) | ((uint32_t)(kBM >> 4) << 24);
 }
 
-template <int KIND, int BN>
-lpq_status run(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& g, cudaStream_t s) {
-  using CF = Cfg<KIND, BN>;
+int g_sms = 0;
+
+template <int KIND, int BN, int NACC>
+lpq_status run(const CUtensorMap& ta, const CUtensorMap& tb, GemmArgs g, cudaStream_t s) {
+  using CF = Cfg<KIND, BN, NACC>;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<KIND, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, CF::kSmem);
+    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<KIND, BN, NACC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         CF::kSmem);
     if (e != cudaSuccess) return cuda_check(e, "cudaFuncSetAttribute(gemm smem)");
     attr_set = true;
   }
-  dim3 grid((unsigned)((g.N + BN - 1) / BN), (unsigned)((g.M + kBM - 1) / kBM));
-  if (grid.y > 65535u) return set_error(LPQ_ERR_SHAPE, "m too large for one launch");
-  gemm_kernel<KIND, BN><<<grid, 128, CF::kSmem, s>>>(ta, tb, g);
+  if (g_sms == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&g_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (g_sms <= 0) g_sms = 148;
+  }
+  const int64_t tm = (g.M + kBM - 1) / kBM, tn = (g.N + BN - 1) / BN;
+  if (tm * tn > (int64_t)1 << 30) return set_error(LPQ_ERR_SHAPE, "too many output tiles");
+  g.tiles_m = (int)tm;
+  g.tiles_n = (int)tn;
+  const int grid = (int)std::min<int64_t>(tm * tn, g_sms);
+  gemm_kernel<KIND, BN, NACC><<<grid, kThreadsGemm, CF::kSmem, s>>>(ta, tb, g);
   return cuda_check(cudaGetLastError(), "gemm kernel launch");
+}
+
+// Output-tile width of the block-scaled GEMMs: 256 (one TMEM accumulator) or
+// 128 (two accumulators, epilogue overlapped); LPQ_GEMM_BN overrides.
+int lpq_gemm_config_bn() {
+  static int bn = -1;
+  if (bn < 0) {
+    const char* e = getenv("LPQ_GEMM_BN");
+    bn = (e && atoi(e) == 128) ? 128 : 256;
+  }
+  return bn;
 }
 
 }  // namespace
@@ -307,12 +413,13 @@ lpq_status launch_gemm(const lpq_qview* a, const lpq_qview* b, void* c, int32_t 
   CUtensorMap ta, tb;
   lpq_status st;
   constexpr int BN = 256;
+  const int nv_bn = lpq_gemm_config_bn();
   if (fa == LPQ_BF16) {
     g.num_k = (int)((k * 2 + kKBytes - 1) / kKBytes);
     if ((st = make_map(&ta, a->codes, true, k, m, k * 2, 64, kBM)) != LPQ_OK) return st;
     if ((st = make_map(&tb, b->codes, true, k, n, k * 2, 64, BN)) != LPQ_OK) return st;
     g.idesc = idesc_dense(1, 1, BN);  // BF16 x BF16 -> F32
-    return run<kKindF16, BN>(ta, tb, g, s);
+    return run<kKindF16, BN, 2>(ta, tb, g, s);
   }
   if (fa == LPQ_FP8_E4M3 || fa == LPQ_FP8_E5M2) {
     g.num_k = (int)((k + kKBytes - 1) / kKBytes);
@@ -321,7 +428,7 @@ lpq_status launch_gemm(const lpq_qview* a, const lpq_qview* b, void* c, int32_t 
     g.idesc = idesc_dense(fa == LPQ_FP8_E5M2 ? 1 : 0, fb == LPQ_FP8_E5M2 ? 1 : 0, BN);
     g.alpha_a = a->tensor_scale;
     g.alpha_b = b->tensor_scale;
-    return run<kKindF8F6F4, BN>(ta, tb, g, s);
+    return run<kKindF8F6F4, BN, 2>(ta, tb, g, s);
   }
   if (fa == LPQ_MXFP8) {
     g.num_k = (int)((k + kKBytes - 1) / kKBytes);
@@ -333,7 +440,12 @@ lpq_status launch_gemm(const lpq_qview* a, const lpq_qview* b, void* c, int32_t 
     g.sfa_kt = sf_kt_atoms(LPQ_MXFP8, k);
     g.sfb_kt = g.sfa_kt;
     g.sfb_groups = sf_row_groups(n);
-    return run<kKindMXF8, BN>(ta, tb, g, s);
+    if (nv_bn == 128) {
+      if ((st = make_map(&tb, b->codes, false, k, n, k, 128, 128)) != LPQ_OK) return st;
+      g.idesc = idesc_block_scaled(0, 0, 1, 128);
+      return run<kKindMXF8, 128, 2>(ta, tb, g, s);
+    }
+    return run<kKindMXF8, BN, 1>(ta, tb, g, s);
   }
   if (fa == LPQ_NVFP4 || fa == LPQ_NVFP4_2D) {
     g.num_k = (int)((k / 2 + kKBytes - 1) / kKBytes);
@@ -347,9 +459,111 @@ lpq_status launch_gemm(const lpq_qview* a, const lpq_qview* b, void* c, int32_t 
     g.sfb_groups = sf_row_groups(n);
     g.alpha_a = a->tensor_scale;
     g.alpha_b = b->tensor_scale;
-    return run<kKindNVF4, BN>(ta, tb, g, s);
+    if (nv_bn == 128) {
+      if ((st = make_map(&tb, b->codes, false, k / 2, n, k / 2, 128, 128)) != LPQ_OK) return st;
+      g.idesc = idesc_block_scaled(1, 1, 0, 128);
+      return run<kKindNVF4, 128, 2>(ta, tb, g, s);
+    }
+    return run<kKindNVF4, BN, 1>(ta, tb, g, s);
   }
   return set_error(LPQ_ERR_UNSUPPORTED, "no GEMM kernel for format %d", fa);
+}
+
+// Tensor-core rate measurement: every CTA issues `iters` k-steps of four
+// 128 x 256 MMAs on operand tiles resident in shared memory (no global
+// traffic), optionally with the per-step scale-factor copies of the
+// block-scaled kinds.  Operands are zero; the FLOP count is what is timed.
+template <int KIND>
+__global__ void __launch_bounds__(128, 1) mma_peak_kernel(int iters, int with_sf, uint32_t idesc) {
+  constexpr int BN = 256;
+  using CF = Cfg<KIND, BN, 1>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = sA + CF::kA;
+  uint8_t* sSf = sB + CF::kB;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sSf + CF::kSfa + CF::kSfb);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 1);
+  int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+  const int warp = threadIdx.x >> 5;
+  for (int i = threadIdx.x; i < (CF::kA + CF::kB + CF::kSfa + CF::kSfb) / 16; i += blockDim.x)
+    reinterpret_cast<uint4*>(smem)[i] = make_uint4(0, 0, 0, 0);
+  if (threadIdx.x == 0) {
+    mbar_init(bar, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  if (warp == 1) tmem_alloc(tmem_slot, CF::kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+  const uint32_t tsfa = tbase + BN, tsfb = tsfa + CF::kSfaCols;
+  if (threadIdx.x == 0) {
+    const uint32_t a_base = smem_u32(sA), b_base = smem_u32(sB);
+    for (int it = 0; it < iters; ++it) {
+      if (KIND == kKindMXF8 && with_sf) {
+        tmem_cp_sf(tsfa, smem_desc(smem_u32(sSf), 0, 128, 0));
+        tmem_cp_sf(tsfb, smem_desc(smem_u32(sSf + 512), 0, 128, 0));
+        tmem_cp_sf(tsfb + 4, smem_desc(smem_u32(sSf + 1024), 0, 128, 0));
+      } else if (KIND == kKindNVF4 && with_sf) {
+        for (int j = 0; j < 4; ++j) {
+          tmem_cp_sf(tsfa + 4 * j, smem_desc(smem_u32(sSf + j * 512), 0, 128, 0));
+          tmem_cp_sf(tsfb + 8 * j, smem_desc(smem_u32(sSf + 2048 + j * 512), 0, 128, 0));
+          tmem_cp_sf(tsfb + 8 * j + 4, smem_desc(smem_u32(sSf + 4096 + j * 512), 0, 128, 0));
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint64_t ad = smem_desc(a_base + 32 * j, 16, 1024, 2);
+        const uint64_t bd = smem_desc(b_base + 32 * j, 16, 1024, 2);
+        const uint32_t acc = (it > 0 || j > 0) ? 1u : 0u;
+        if constexpr (KIND == kKindF16 || KIND == kKindF8F6F4) {
+          mma_ss<KIND>(tbase, ad, bd, idesc, acc);
+        } else if constexpr (KIND == kKindMXF8) {
+          mma_bs<KIND>(tbase, ad, bd, idesc | ((uint32_t)j << 4) | ((uint32_t)j << 29), tsfa, tsfb, acc);
+        } else {
+          mma_bs<KIND>(tbase, ad, bd, idesc, tsfa + 4 * j, tsfb + 8 * j, acc);
+        }
+      }
+    }
+    tc_commit(bar);
+    mbar_wait_bounded(bar, 0, abort_flag, &g_device_error);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tbase, CF::kTmemCols);
+  }
+}
+
+template <int KIND>
+lpq_status run_peak(int iters, int with_sf, uint32_t idesc, cudaStream_t s) {
+  using CF = Cfg<KIND, 256, 1>;
+  const int smem = CF::kA + CF::kB + CF::kSfa + CF::kSfb + 1024 + 256;
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(mma_peak_kernel<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return cuda_check(e, "cudaFuncSetAttribute(peak)");
+    attr = true;
+  }
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  mma_peak_kernel<KIND><<<sms, 128, smem, s>>>(iters, with_sf, idesc);
+  return cuda_check(cudaGetLastError(), "peak kernel launch");
+}
+
+lpq_status launch_mma_peak(int32_t kind, int32_t iters, int32_t with_sf, cudaStream_t s) {
+  switch (kind) {
+    case kKindF16: return run_peak<kKindF16>(iters, 0, idesc_dense(1, 1, 256), s);
+    case kKindF8F6F4: return run_peak<kKindF8F6F4>(iters, 0, idesc_dense(0, 0, 256), s);
+    case kKindMXF8: return run_peak<kKindMXF8>(iters, with_sf, idesc_block_scaled(0, 0, 1, 256), s);
+    case kKindNVF4: return run_peak<kKindNVF4>(iters, with_sf, idesc_block_scaled(1, 1, 0, 256), s);
+  }
+  return set_error(LPQ_ERR_INVALID_ARG, "kind %d", kind);
 }
 
 // One CTA waits with the bounded wait on a barrier that nothing completes;

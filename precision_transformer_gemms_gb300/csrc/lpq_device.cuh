@@ -96,12 +96,41 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1
 #pragma unroll
   for (int r = 0; r < 10; ++r) {
     if (r > 0) { k0 += 0x9E3779B9u; k1 += 0xBB67AE85u; }
-    uint32_t lo0 = 0xD2511F53u * c.x, hi0 = __umulhi(0xD2511F53u, c.x);
-    uint32_t lo1 = 0xCD9E8D57u * c.z, hi1 = __umulhi(0xCD9E8D57u, c.z);
-    c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+    const uint64_t p0 = (uint64_t)0xD2511F53u * c.x;  // one wide multiply gives both halves
+    const uint64_t p1 = (uint64_t)0xCD9E8D57u * c.z;
+    c = make_uint4((uint32_t)(p1 >> 32) ^ c.y ^ k0, (uint32_t)p1, (uint32_t)(p0 >> 32) ^ c.w ^ k1, (uint32_t)p0);
   }
   return c;
 }
+
+// Philox-4x32-10 with the ten round keys precomputed (the key schedule only
+// depends on the seed, so a thread that draws many words computes it once).
+struct PhiloxKeys {
+  uint32_t k0[10], k1[10];
+  __device__ __forceinline__ explicit PhiloxKeys(uint64_t seed) {
+    uint32_t a = (uint32_t)seed, b = (uint32_t)(seed >> 32);
+#pragma unroll
+    for (int r = 0; r < 10; ++r) {
+      k0[r] = a;
+      k1[r] = b;
+      a += 0x9E3779B9u;
+      b += 0xBB67AE85u;
+    }
+  }
+  __device__ __forceinline__ uint4 operator()(uint4 c) const {
+#pragma unroll
+    for (int r = 0; r < 10; ++r) {
+      const uint64_t p0 = (uint64_t)0xD2511F53u * c.x;
+      const uint64_t p1 = (uint64_t)0xCD9E8D57u * c.z;
+      c = make_uint4((uint32_t)(p1 >> 32) ^ c.y ^ k0[r], (uint32_t)p1, (uint32_t)(p0 >> 32) ^ c.w ^ k1[r], (uint32_t)p0);
+    }
+    return c;
+  }
+  // 4 random words for elements j = 4g .. 4g+3 of copy `copy_id`.
+  __device__ __forceinline__ uint4 words(uint64_t g, uint32_t copy_id) const {
+    return (*this)(make_uint4((uint32_t)g, (uint32_t)(g >> 32), copy_id, 0u));
+  }
+};
 
 // 4 random words for elements j = 4g .. 4g+3 of copy `copy_id`.
 __device__ __forceinline__ uint4 sr_words(uint64_t seed, uint64_t g, uint32_t copy_id) {
@@ -134,23 +163,21 @@ __device__ __forceinline__ void rht16(float t[16], uint32_t signs) {
 
 // Stochastic E2M1 code of y with random word r: between adjacent magnitudes
 // lo <= |y| <= hi, round up iff float(r >> 8) < ((|y| - lo) / (hi - lo)) * 2^24.
+// hi - lo is 0.5, 1 or 2, so the quotient times 2^24 is the exact product
+// (|y| - lo) * 2^24 / (hi - lo) (Sterbenz subtraction, power-of-two scaling).
 __device__ __forceinline__ uint32_t sr_e2m1(float y, uint32_t r) {
-  if (y != y) return 0x7u;
-  uint32_t s = (__float_as_uint(y) >> 31) << 3;
-  float a = fabsf(y);
-  if (a >= 6.0f) return s | 7u;
-  uint32_t lo;
-  float vlo, vhi;
-  if (a < 0.5f) { lo = 0; vlo = 0.f; vhi = 0.5f; }
-  else if (a < 1.0f) { lo = 1; vlo = 0.5f; vhi = 1.f; }
-  else if (a < 1.5f) { lo = 2; vlo = 1.f; vhi = 1.5f; }
-  else if (a < 2.0f) { lo = 3; vlo = 1.5f; vhi = 2.f; }
-  else if (a < 3.0f) { lo = 4; vlo = 2.f; vhi = 3.f; }
-  else if (a < 4.0f) { lo = 5; vlo = 3.f; vhi = 4.f; }
-  else { lo = 6; vlo = 4.f; vhi = 6.f; }
-  float frac = __fdiv_rn(__fsub_rn(a, vlo), __fsub_rn(vhi, vlo));
-  bool up = (float)(r >> 8) < __fmul_rn(frac, 16777216.0f);
-  return s | (up ? lo + 1 : lo);
+  const uint32_t s = (__float_as_uint(y) >> 31) << 3;
+  const float a = fabsf(y);
+  // lower neighbour `lo` (code and value) and 2^24 / (hi - lo) on each grid segment
+  const bool seg0 = a < 2.0f, seg1 = a < 4.0f;
+  const float t = seg0 ? __fmul_rn(a, 2.0f) : a;                  // exact
+  const uint32_t q = (uint32_t)__float2int_rz(t);                  // 0..3 (seg0), 2..3 (seg1)
+  const uint32_t lo = seg0 ? q : (seg1 ? q + 2u : 6u);
+  const float vlo = seg0 ? __fmul_rn((float)q, 0.5f) : (seg1 ? (float)q : 4.0f);
+  const float scale = seg0 ? 33554432.0f : (seg1 ? 16777216.0f : 8388608.0f);
+  const bool up = (float)(r >> 8) < __fmul_rn(__fsub_rn(a, vlo), scale);
+  const uint32_t code = (a >= 6.0f || a != a) ? 7u : (up ? lo + 1u : lo);
+  return (a != a) ? 7u : (s | code);
 }
 
 // ------------------------------------------------------------------ warp helpers

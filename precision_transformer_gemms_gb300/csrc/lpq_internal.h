@@ -39,5 +39,6 @@ lpq_status launch_gemm(const lpq_qview* a, const lpq_qview* b, void* c, int32_t 
 // Device error word (gemm.cu owns it).
 lpq_status read_and_clear_device_error(cudaStream_t stream, int32_t* code);
 lpq_status launch_selftest_wait(uint64_t limit_ns, cudaStream_t stream);
+lpq_status launch_mma_peak(int32_t kind, int32_t iters, int32_t with_sf, cudaStream_t stream);
 
 }  // namespace lpq

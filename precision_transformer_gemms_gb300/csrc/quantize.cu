@@ -137,6 +137,8 @@ __global__ void __launch_bounds__(kThreads) quant_tile_kernel(const QParams p) {
 
   const int t = threadIdx.x;
   const int64_t r0 = (int64_t)blockIdx.y * TR, c0 = (int64_t)blockIdx.x * kTC;
+  // The shared tile feeds the column-wise copy and the 2D / 128x128 scales.
+  const bool kNeedTile = p.col_codes != nullptr || KIND == QK_NV2D || KIND == QK_BLK128;
   const int64_t R = p.R, C = p.C;
   constexpr float kFmax = kE5M2 ? 57344.0f : 448.0f;
 
@@ -166,6 +168,7 @@ __global__ void __launch_bounds__(kThreads) quant_tile_kernel(const QParams p) {
     }
     if (KIND == QK_NV && p.rht) signs = rht_signs(p.rht_seed);
   }
+  const PhiloxKeys keys(p.seed);
 
   // ---------------------------------------------------------------- load (+ row-wise copy)
   const int lr = t >> 4;        // row within a 16-row slab
@@ -179,7 +182,7 @@ __global__ void __launch_bounds__(kThreads) quant_tile_kernel(const QParams p) {
     const bool ok = col_ok && r < R;
     uint4 v = make_uint4(0u, 0u, 0u, 0u);
     if (ok) v = ld_stream(p.x + r * C + c0 + lc);
-    *reinterpret_cast<uint4*>(&tile[rl][lc]) = v;
+    if (kNeedTile) *reinterpret_cast<uint4*>(&tile[rl][lc]) = v;
     float f[8];
     unpack8(v, f);
     if constexpr (KIND == QK_BLK128 || KIND == QK_FP8) {
@@ -217,8 +220,8 @@ __global__ void __launch_bounds__(kThreads) quant_tile_kernel(const QParams p) {
       uint4 w0 = make_uint4(0, 0, 0, 0), w1 = w0;
       if (p.sr) {
         const uint64_t g = (p.ctr_off + (uint64_t)(r * C + c0 + lc)) >> 2;
-        w0 = sr_words(p.seed, g, 0u);
-        w1 = sr_words(p.seed, g + 1, 0u);
+        w0 = keys.words(g, 0u);
+        w1 = keys.words(g + 1, 0u);
       }
       const uint32_t q = nv_codes8(f, fb, p.sr, w0, w1);
       if (ok) {
@@ -258,6 +261,7 @@ __global__ void __launch_bounds__(kThreads) quant_tile_kernel(const QParams p) {
       }
     }
   }
+  if (!kNeedTile) return;
   __syncthreads();
 
   // ---------------------------------------------------------------- 2D / 128x128 tiles
@@ -447,7 +451,7 @@ __global__ void __launch_bounds__(kThreads) quant_tile_kernel(const QParams p) {
       if (p.sr) {
         const uint64_t g = (p.ctr_off + (uint64_t)(c * R + rr)) >> 2;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) w[j] = sr_words(p.seed, g + j, 1u);
+        for (int j = 0; j < 4; ++j) w[j] = keys.words(g + j, 1u);
       }
       const uint32_t a = nv_codes8(f, fb, p.sr, w[0], w[1]);
       const uint32_t b = nv_codes8(f + 8, fb, p.sr, w[2], w[3]);

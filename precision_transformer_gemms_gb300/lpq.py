@@ -83,9 +83,10 @@ def lib():
         L.lpq_last_error.restype = ctypes.c_char_p
         L.lpq_device_status.argtypes = [P, ctypes.POINTER(I32)]
         L.lpq_selftest_wait.argtypes = [U64, P]
+        L.lpq_mma_peak.argtypes = [I32, I32, I32, P]
         L.lpq_version.restype = I32
         for name in ("lpq_copy_bytes", "lpq_quantize", "lpq_scale_update", "lpq_gemm", "lpq_layer_shapes",
-                     "lpq_device_status", "lpq_selftest_wait"):
+                     "lpq_device_status", "lpq_selftest_wait", "lpq_mma_peak"):
             getattr(L, name).restype = I32
         _lib = L
     return _lib
@@ -232,3 +233,21 @@ def device_status(stream=None):
 
 def selftest_wait(limit_ns, stream=None):
     _check(lib().lpq_selftest_wait(int(limit_ns), _stream(stream)))
+
+
+MMA_KINDS = {"bf16": 0, "fp8": 1, "mxfp8": 2, "nvfp4": 3}
+MMA_K = {0: 16, 1: 32, 2: 32, 3: 64}
+
+
+def mma_peak(kind, iters=20000, with_scale_copies=True, stream=None):
+    """Dense tcgen05 rate in TFLOP/s for `kind` (see lpq_mma_peak)."""
+    k = MMA_KINDS[kind] if isinstance(kind, str) else kind
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    _check(lib().lpq_mma_peak(k, 64, int(with_scale_copies), _stream(stream)))  # warm-up
+    e0.record()
+    _check(lib().lpq_mma_peak(k, iters, int(with_scale_copies), _stream(stream)))
+    e1.record()
+    torch.cuda.synchronize()
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    flops = sms * iters * 4 * 2 * 128 * 256 * MMA_K[k]
+    return flops / (e0.elapsed_time(e1) * 1e-3) / 1e12
