@@ -206,7 +206,6 @@ lpq_status lpq_gemm(int32_t layout, const lpq_qview* a, const lpq_qview* b, void
                        (fa == LPQ_MXFP8 && fb == LPQ_MXFP8) || (is_nvfp4(fa) && is_nvfp4(fb)) ||
                        (is_block(fa) && is_block(fb));
   if (!pair_ok) return set_error(LPQ_ERR_UNSUPPORTED, "no GEMM for the pairing %d x %d (no fallback)", fa, fb);
-  if (is_block(fa)) return set_error(LPQ_ERR_UNSUPPORTED, "sub-channel FP8 GEMM not built into this library yet");
   const int64_t kmul = is_block(fa) ? 128 : 32;
   if (k % kmul) return set_error(LPQ_ERR_SHAPE, "k %lld not a multiple of %lld", (long long)k, (long long)kmul);
   if (m > 0 && n > 0) {
@@ -220,6 +219,12 @@ lpq_status lpq_gemm(int32_t layout, const lpq_qview* a, const lpq_qview* b, void
           if (v->sf_layout != LPQ_SF_GEMM)
             return set_error(LPQ_ERR_INVALID_ARG, "block-scaled operands need LPQ_SF_GEMM scales");
           if (!v->scales || !aligned16(v->scales)) return set_error(LPQ_ERR_ALIGN, "operand scales NULL/unaligned");
+        }
+        if (is_block(v->fmt)) {
+          if (v->sf_layout != LPQ_SF_GEMM)
+            return set_error(LPQ_ERR_INVALID_ARG, "sub-channel operands need LPQ_SF_GEMM factors");
+          if (!v->scales || (reinterpret_cast<uintptr_t>(v->scales) & 3u))
+            return set_error(LPQ_ERR_ALIGN, "operand factors NULL/unaligned");
         }
         if ((is_fp8_pertensor(v->fmt) || is_nvfp4(v->fmt)) && !v->tensor_scale)
           return set_error(LPQ_ERR_INVALID_ARG, "operand tensor_scale NULL");

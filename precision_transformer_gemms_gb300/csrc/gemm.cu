@@ -382,6 +382,224 @@ lpq_status run(const CUtensorMap& ta, const CUtensorMap& tb, GemmArgs g, cudaStr
   return cuda_check(cudaGetLastError(), "gemm kernel launch");
 }
 
+// Sub-channel FP8 GEMM ("Faster training throughput in FP8 with NVIDIA NeMo",
+// sub-channel scaling: 1x128 activation and 128x128 weight blocks with FP32
+// factors).  Every 128-deep K slice is one pipeline stage: the MMA warp
+// computes the slice's partial product sum_{k in slice} qa * qb with
+// kind::f8f6f4 into one of two TMEM buffers; the epilogue warps read it and
+// accumulate partial * sa[m, slice] * sb[n, slice] in FP32 registers (the
+// tensor cores have no FP32 block scales), while the next slice runs.
+struct BlockArgs {
+  const float* sa;  // A factors: 1x128 -> [K/128][M]; 128x128 -> [ceil(M/128)][K/128]
+  const float* sb;  // B factors, same convention with N
+  int a_rows, b_rows;  // block rows: 1 or 128
+  void* c;
+  int64_t M, N, K;
+  int c_fp32;
+  uint32_t idesc;
+  int num_k;
+  int tiles_m, tiles_n;
+};
+
+constexpr int kBlkBN = 128;
+constexpr int kBlkStages = 6;
+constexpr int kBlkStage = kBM * kKBytes + kBlkBN * kKBytes;
+constexpr int kBlkSmem = kBlkStages * kBlkStage + 1024 + 512 + kBlkBN * 4;
+
+__global__ void __launch_bounds__(kThreadsGemm, 1)
+    block_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                      const BlockArgs g) {
+  constexpr int S = kBlkStages, BN = kBlkBN;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = sA + S * kBM * kKBytes;
+  float* s_sb = reinterpret_cast<float*>(sB + S * BN * kKBytes);  // per-slice B factors (1x128 B)
+  uint64_t* full = reinterpret_cast<uint64_t*>(s_sb + BN);
+  uint64_t* empty = full + S;
+  uint64_t* acc_full = empty + S;   // [2]
+  uint64_t* acc_empty = acc_full + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int total = g.tiles_m * g.tiles_n;
+  const int64_t KB = g.K / 128;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&acc_full[a], 1);
+      mbar_init(&acc_empty[a], 4);
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, 256);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      uint32_t it = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        int mt, nt;
+        tile_coords(t, g.tiles_m, g.tiles_n, mt, nt);
+        for (int kt = 0; kt < g.num_k; ++kt, ++it) {
+          const int s = it % S;
+          const uint32_t ph = (it / S) & 1u;
+          if (!(ok = mbar_wait_bounded(&empty[s], ph ^ 1u, abort_flag, &g_device_error))) break;
+          mbar_arrive_expect_tx(&full[s], kBlkStage);
+          tma_load_2d(sA + s * kBM * kKBytes, &tmA, kt * kKBytes, mt * kBM, &full[s]);
+          tma_load_2d(sB + s * BN * kKBytes, &tmB, kt * kKBytes, nt * BN, &full[s]);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      uint32_t it = 0, slice = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        for (int kt = 0; kt < g.num_k; ++kt, ++it, ++slice) {
+          const uint32_t a = slice & 1u, aph = (slice >> 1) & 1u;
+          if (!(ok = mbar_wait_bounded(&acc_empty[a], aph ^ 1u, abort_flag, &g_device_error))) break;
+          const int s = it % S;
+          const uint32_t ph = (it / S) & 1u;
+          if (!(ok = mbar_wait_bounded(&full[s], ph, abort_flag, &g_device_error))) break;
+          tc_fence_after();
+          const uint32_t a_base = smem_u32(sA + s * kBM * kKBytes);
+          const uint32_t b_base = smem_u32(sB + s * BN * kKBytes);
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            mma_ss<kKindF8F6F4>(tmem_base + a * BN, smem_desc(a_base + 32 * j, 16, 1024, 2),
+                                smem_desc(b_base + 32 * j, 16, 1024, 2), g.idesc, j > 0 ? 1u : 0u);
+          tc_commit(&empty[s]);
+          tc_commit(&acc_full[a]);
+        }
+      }
+    }
+  } else {
+    const int q = warp & 3;
+    const int et = threadIdx.x - 64;  // 0..127 across the epilogue warps
+    const bool vec_ok = g.c_fp32 ? (g.N % 4 == 0) : (g.N % 8 == 0);
+    uint32_t slice = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+      int mt, nt;
+      tile_coords(t, g.tiles_m, g.tiles_n, mt, nt);
+      const int64_t row = (int64_t)mt * kBM + q * 32 + lane;
+      const int64_t n0 = (int64_t)nt * BN;
+      float acc[BN];
+#pragma unroll
+      for (int i = 0; i < BN; ++i) acc[i] = 0.f;
+      for (int kt = 0; kt < g.num_k; ++kt, ++slice) {
+        const uint32_t a = slice & 1u, aph = (slice >> 1) & 1u;
+        // this slice's factors: A per row (or per 128-row block), B per column (or block)
+        float fa;
+        if (g.a_rows == 1) fa = row < g.M ? g.sa[(int64_t)kt * g.M + row] : 0.f;
+        else fa = g.sa[(int64_t)mt * KB + kt];
+        if (g.b_rows == 1) {
+          asm volatile("bar.sync 1, 128;" ::: "memory");
+          const int64_t n = n0 + et;
+          s_sb[et] = n < g.N ? g.sb[(int64_t)kt * g.N + n] : 0.f;
+          asm volatile("bar.sync 1, 128;" ::: "memory");
+        }
+        const float fb_blk = g.b_rows == 1 ? 0.f : g.sb[(n0 / 128) * KB + kt];
+        if (!(ok = mbar_wait_bounded(&acc_full[a], aph, abort_flag, &g_device_error))) break;
+        __syncwarp();
+        tc_fence_after();
+        const uint32_t tb = tmem_base + a * BN + ((uint32_t)(q * 32) << 16);
+#pragma unroll
+        for (int cc = 0; cc < BN / 32; ++cc) {
+          uint32_t v[32];
+          tmem_ld32(tb + (uint32_t)(cc * 32), v);
+          if (cc == BN / 32 - 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_empty[a]);
+          }
+          if (g.b_rows == 1) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              acc[cc * 32 + i] = __fadd_rn(acc[cc * 32 + i],
+                                           __fmul_rn(__uint_as_float(v[i]), __fmul_rn(fa, s_sb[cc * 32 + i])));
+          } else {
+            const float f = __fmul_rn(fa, fb_blk);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) acc[cc * 32 + i] = __fadd_rn(acc[cc * 32 + i], __fmul_rn(__uint_as_float(v[i]), f));
+          }
+        }
+      }
+      if (!ok || row >= g.M) continue;
+      const int64_t ncols = g.N - n0;
+      if (g.c_fp32) {
+        float* out = static_cast<float*>(g.c) + row * g.N + n0;
+        if (vec_ok && ncols >= BN) {
+#pragma unroll
+          for (int i = 0; i < BN / 4; ++i)
+            reinterpret_cast<float4*>(out)[i] = make_float4(acc[4 * i], acc[4 * i + 1], acc[4 * i + 2], acc[4 * i + 3]);
+        } else {
+#pragma unroll
+          for (int i = 0; i < BN; ++i)
+            if (i < ncols) out[i] = acc[i];
+        }
+      } else {
+        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(g.c) + row * g.N + n0;
+        if (vec_ok && ncols >= BN) {
+#pragma unroll
+          for (int i = 0; i < BN / 8; ++i) {
+            uint32_t w[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              __nv_bfloat162 h = __floats2bfloat162_rn(acc[8 * i + 2 * j], acc[8 * i + 2 * j + 1]);
+              w[j] = *reinterpret_cast<uint32_t*>(&h);
+            }
+            reinterpret_cast<uint4*>(out)[i] = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < BN; ++i)
+            if (i < ncols) out[i] = __float2bfloat16_rn(acc[i]);
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, 256);
+  }
+}
+
+lpq_status run_block_gemm(const CUtensorMap& ta, const CUtensorMap& tb, BlockArgs g, cudaStream_t s) {
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(block_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kBlkSmem);
+    if (e != cudaSuccess) return cuda_check(e, "cudaFuncSetAttribute(block gemm)");
+    attr = true;
+  }
+  if (g_sms == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&g_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (g_sms <= 0) g_sms = 148;
+  }
+  const int64_t tm = (g.M + kBM - 1) / kBM, tn = (g.N + kBlkBN - 1) / kBlkBN;
+  g.tiles_m = (int)tm;
+  g.tiles_n = (int)tn;
+  const int grid = (int)std::min<int64_t>(tm * tn, g_sms);
+  block_gemm_kernel<<<grid, kThreadsGemm, kBlkSmem, s>>>(ta, tb, g);
+  return cuda_check(cudaGetLastError(), "block gemm launch");
+}
+
 // Output-tile width of the block-scaled GEMMs: 256 (one TMEM accumulator) or
 // 128 (two accumulators, epilogue overlapped); LPQ_GEMM_BN overrides.
 int lpq_gemm_config_bn() {
@@ -465,6 +683,23 @@ lpq_status launch_gemm(const lpq_qview* a, const lpq_qview* b, void* c, int32_t 
       return run<kKindNVF4, 128, 2>(ta, tb, g, s);
     }
     return run<kKindNVF4, BN, 1>(ta, tb, g, s);
+  }
+  if (fa == LPQ_FP8_BLOCK_1x128 || fa == LPQ_FP8_BLOCK_128x128) {
+    BlockArgs bg{};
+    bg.c = c;
+    bg.M = m;
+    bg.N = n;
+    bg.K = k;
+    bg.c_fp32 = c_is_fp32;
+    bg.num_k = (int)(k / 128);
+    bg.sa = static_cast<const float*>(a->scales);
+    bg.sb = static_cast<const float*>(b->scales);
+    bg.a_rows = fa == LPQ_FP8_BLOCK_1x128 ? 1 : 128;
+    bg.b_rows = fb == LPQ_FP8_BLOCK_1x128 ? 1 : 128;
+    if ((st = make_map(&ta, a->codes, false, k, m, k, 128, kBM)) != LPQ_OK) return st;
+    if ((st = make_map(&tb, b->codes, false, k, n, k, 128, kBlkBN)) != LPQ_OK) return st;
+    bg.idesc = idesc_dense(0, 0, kBlkBN);
+    return run_block_gemm(ta, tb, bg, s);
   }
   return set_error(LPQ_ERR_UNSUPPORTED, "no GEMM kernel for format %d", fa);
 }

@@ -46,6 +46,21 @@ def test_gemm_parity(fmts, shape, out_fp32):
     check(a, b, M, N, K, out_fp32)
 
 
+BLOCK_SHAPES = [(4, 128, 16), (256, 512, 384), (300, 640, 200), (520, 1024, 776)]
+
+
+@pytest.mark.parametrize("out_fp32", [True, False])
+@pytest.mark.parametrize("shape", BLOCK_SHAPES)
+@pytest.mark.parametrize("fmts", [(lpq.FP8_BLOCK_1x128, lpq.FP8_BLOCK_128x128),
+                                  (lpq.FP8_BLOCK_1x128, lpq.FP8_BLOCK_1x128)])
+def test_subchannel_gemm_parity(fmts, shape, out_fp32):
+    """Sub-channel FP8: per 128-deep slice the tensor-core partial is scaled by
+    the FP32 block factors and accumulated in FP32."""
+    M, K, N = shape
+    a, b = quantize_pair(*fmts, M, K, N, seed=7)
+    check(a, b, M, N, K, out_fp32)
+
+
 def test_gemm_closed_form_all_ones():
     """All-ones operands: every output is exactly K (MXFP8 scales are exact
     powers of two, so the products are exact)."""
@@ -84,7 +99,7 @@ def test_gemm_single_nonzero_k():
         assert torch.allclose(c, torch.full_like(c, float(ref[0])), rtol=1e-6), fmt
 
 
-@pytest.mark.parametrize("fmt", [lpq.MXFP8, lpq.NVFP4, lpq.FP8_E4M3, lpq.BF16])
+@pytest.mark.parametrize("fmt", [lpq.MXFP8, lpq.NVFP4, lpq.FP8_E4M3, lpq.BF16, lpq.FP8_BLOCK_1x128])
 def test_fprop_dgrad_wgrad_layouts(fmt):
     """The three GEMMs of a linear layer on the copies each one reads."""
     M, K, N = 256, 512, 384
@@ -98,6 +113,10 @@ def test_fprop_dgrad_wgrad_layouts(fmt):
         qx = lpq.quantize(X, fmt, both | lpq.RHT_COLWISE, rht_seed=9)
         qw = lpq.quantize(W, lpq.NVFP4_2D, both)
         qd = lpq.quantize(dY, fmt, both | lpq.RHT_COLWISE | lpq.STOCHASTIC, seed=3, rht_seed=9)
+    elif fmt == lpq.FP8_BLOCK_1x128:
+        qx = lpq.quantize(X, fmt, both)
+        qw = lpq.quantize(W, lpq.FP8_BLOCK_128x128, both)
+        qd = lpq.quantize(dY, fmt, both)
     elif fmt == lpq.FP8_E4M3:
         qx = lpq.quantize(X, fmt, both)
         qw = lpq.quantize(W, fmt, both)
