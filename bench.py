@@ -57,6 +57,9 @@ def parse():
     p.add_argument("--sequence_length", type=int, default=512)
     p.add_argument("--seed", type=int, default=0)
     p.add_argument("-o", "--output", default=None, help="write the per-GEMM table as JSON here")
+    p.add_argument("--workload", choices=["layer", "ksweep", "drift"], default="layer",
+                   help="layer: the contract line; ksweep / drift: the K-sweep and the FP8 drift runs")
+    p.add_argument("--verify", action="store_true", help="drift: compare every step with the oracle")
     p.add_argument("--mma-peaks", action="store_true",
                    help="only measure the dense tcgen05 rates (shared-memory-resident operands) and exit")
     return p.parse_args()
@@ -317,6 +320,30 @@ def summarize_events(layer, events, steps):
     return table
 
 
+def profiled_traffic(kernel_file, recipe):
+    """DRAM bytes per launch of the GEMM kernel from the committed ncu summary
+    (profiles/gemm_<recipe>_layer_traffic.md), or None when the kernel source
+    changed after the counters were taken (its sha256 is recorded there)."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", f"gemm_{recipe}_layer_traffic.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    vals = {}
+    for line in text.splitlines():
+        if ":" in line and line.strip().startswith("- "):
+            k, v = line.strip()[2:].split(":", 1)
+            vals[k.strip()] = v.strip().strip("`")
+    src = hashlib.sha256(open(kernel_file, "rb").read()).hexdigest()
+    if vals.get("kernel_source_sha256") != src:
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
 def measured_peaks():
     try:
         return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
@@ -427,9 +454,14 @@ def run_lpq(args, rank, world, local):
     else:
         peak = 1700.0 * ratio
         peak_src = f"of fallback: 1.7 PFLOP/s bf16 sustained x {ratio}"
+    algo_bytes = 0
+    for name, lay, m, k, n in layer.shapes:
+        per = {"nvfp4": 0.5 + 1 / 16, "mxfp8": 1 + 1 / 32, "fp8_current": 1, "fp8_delayed": 1, "bf16": 2}[recipe]
+        algo_bytes += (m * k + n * k) * per + m * n * 2
+    traffic = profiled_traffic(os.path.join(ROOT, "precision_transformer_gemms_gb300", "csrc", "gemm.cu"), recipe)
     roof = {"bound": "tensor", "achieved": gemm_achieved, "peak": peak, "unit": "TFLOP/s",
-            "frac": gemm_achieved / peak, "traffic": None, "kernel": f"gemm_kernel ({recipe})",
-            "peak_source": peak_src}
+            "frac": gemm_achieved / peak, "traffic": traffic, "kernel": f"gemm_kernel ({recipe})",
+            "peak_source": peak_src, "algorithmic_bytes_per_launch": algo_bytes / len(layer.shapes)}
     hbm = peaks["hbm_gbs"] if peaks else 6800.0
 
     # recipe sweep (fewer steps each)
@@ -541,16 +573,138 @@ def run_mma_peaks(args):
         iters = 40000 if kind == "nvfp4" else 20000
         out[kind] = lpq.mma_peak(kind, iters=iters, with_scale_copies=False)
         if kind in ("mxfp8", "nvfp4"):
-            out[kind + "_with_scale_copies"] = lpq.mma_peak(kind, iters=iters, with_scale_copies=True)
+            out[kind + "_with_scale_copies"] = lpq.mma_peak(kind, iters=iters, with_scale_copies=1)
+        if kind == "nvfp4":
+            out[kind + "_scale_copies_two_regions"] = lpq.mma_peak(kind, iters=iters, with_scale_copies=2)
+            out[kind + "_scale_copies_interleaved"] = lpq.mma_peak(kind, iters=iters, with_scale_copies=3)
     out["clocks"] = clocks.stop()
     out["unit"] = "TFLOP/s"
     print(json.dumps(out), flush=True)
+
+
+def _event_ms(fn, reps):
+    import torch
+    for _ in range(2):
+        fn()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        fn()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / reps
+
+
+def run_ksweep(args):
+    """Scaling-granularity K-sweep: 8192 x K x 8192 GEMMs (inputs ~N(0,1), 0.1%
+    entries x100) under per-tensor FP8, MXFP8, sub-channel FP8 (1x128 act,
+    128x128 weight), NVFP4 (1D act, 2D weight) and bf16; pre-quantize (GEMM
+    only) and autocast (quantize both operands + GEMM) times and speed-ups vs
+    the bf16 tcgen05 GEMM of the same shape."""
+    import torch
+    from precision_transformer_gemms_gb300 import lpq, synth
+    torch.cuda.set_device(0)
+    M = N = 8192
+    fmts = {"fp8_current": (lpq.FP8_E4M3, lpq.FP8_E4M3), "mxfp8": (lpq.MXFP8, lpq.MXFP8),
+            "fp8_subchannel": (lpq.FP8_BLOCK_1x128, lpq.FP8_BLOCK_128x128), "nvfp4": (lpq.NVFP4, lpq.NVFP4_2D)}
+    out = {}
+    for K in (1024, 2048, 4096, 8192, 16384):
+        A = synth.bf16_normal((M, K), 1.0, 50, "cuda", 0.001, 100.0)
+        B = synth.bf16_normal((N, K), 1.0, 51, "cuda", 0.001, 100.0)
+        C = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        ca, cb = lpq.Copy.of_bf16(A), lpq.Copy.of_bf16(B)
+        flops = 2 * M * N * K
+        row = {"bf16_ms": _event_ms(lambda: lpq.gemm(lpq.FPROP, ca, cb, c=C), 10)}
+        for name, (fa, fb) in fmts.items():
+            qa, qb = lpq.alloc(fa, M, K, lpq.ROWWISE), lpq.alloc(fb, N, K, lpq.ROWWISE)
+
+            def quant():
+                lpq.quantize(A, fa, lpq.ROWWISE, out=qa)
+                lpq.quantize(B, fb, lpq.ROWWISE, out=qb)
+
+            quant()
+            g = _event_ms(lambda: lpq.gemm(lpq.FPROP, qa.row, qb.row, c=C), 10)
+            ac = _event_ms(lambda: (quant(), lpq.gemm(lpq.FPROP, qa.row, qb.row, c=C)), 10)
+            row[name] = {"prequant_ms": g, "autocast_ms": ac, "prequant_tflops": flops / g / 1e9,
+                         "prequant_speedup_vs_bf16": row["bf16_ms"] / g, "autocast_speedup_vs_bf16": row["bf16_ms"] / ac}
+            del qa, qb
+        row["bf16_tflops"] = flops / row["bf16_ms"] / 1e9
+        out[K] = row
+        del A, B, C
+        torch.cuda.empty_cache()
+    print(json.dumps({"workload": "K-sweep 8192 x K x 8192", "unit": "ms / TFLOP/s", "results": out}), flush=True)
+
+
+def run_drift(args):
+    """Per-tensor FP8 current vs delayed scaling on the attention-output GEMMs
+    (M = 15872, 4096 x 4096 weight) over 20 steps whose activation std drifts
+    1 -> 4 (gradients std 1e-3); Fprop + Dgrad + Wgrad each step, autocast.
+    Reports per step the ms, the amax and the scale in use; with --verify
+    every step's codes are compared with the oracle."""
+    import numpy as np
+    import torch
+    from precision_transformer_gemms_gb300 import lpq, synth
+    torch.cuda.set_device(0)
+    M, K, N = args.micro_batch_size * args.sequence_length, args.hidden_size, args.hidden_size
+    W = synth.bf16_normal((N, K), synth.WEIGHT_STD, 1, "cuda")
+    both = lpq.ROWWISE | lpq.COLWISE
+    res = {}
+    for scaling in ("current", "delayed"):
+        sc = lpq.SCALING_DELAYED if scaling == "delayed" else lpq.SCALING_CURRENT
+        st = {r: lpq.DelayedState(16) for r in ("X", "W", "dY")}
+        bufs = {"X": lpq.alloc(lpq.FP8_E4M3, M, K, both), "W": lpq.alloc(lpq.FP8_E4M3, N, K, both),
+                "dY": lpq.alloc(lpq.FP8_E5M2, M, N, both)}
+        outs = [torch.empty((M, N), dtype=torch.bfloat16, device="cuda"),
+                torch.empty((M, K), dtype=torch.bfloat16, device="cuda"),
+                torch.empty((N, K), dtype=torch.bfloat16, device="cuda")]
+        steps, ref_state = [], None
+        if args.verify:
+            import oracle as o
+            ref_state = o.DelayedState(16)
+        for t in range(20):
+            X = synth.bf16_normal((M, K), synth.drift_std(t), 10 * t, "cuda")
+            dY = synth.bf16_normal((M, N), synth.GRAD_STD, 10 * t + 2, "cuda")
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for role, x, fmt in (("X", X, lpq.FP8_E4M3), ("W", W, lpq.FP8_E4M3), ("dY", dY, lpq.FP8_E5M2)):
+                lpq.quantize(x, fmt, both, scaling=sc, state=st[role] if sc else None, out=bufs[role])
+                if sc:
+                    lpq.scale_update(st[role], bufs[role].row.amax, lpq.FMAX[fmt])
+            lpq.gemm(lpq.FPROP, bufs["X"].row, bufs["W"].row, c=outs[0])
+            lpq.gemm(lpq.DGRAD, bufs["dY"].row, bufs["W"].col, c=outs[1])
+            lpq.gemm(lpq.WGRAD, bufs["dY"].col, bufs["X"].col, c=outs[2])
+            e1.record()
+            torch.cuda.synchronize()
+            rec = {"ms": e0.elapsed_time(e1), "x_amax": float(bufs["X"].row.amax.item()),
+                   "x_scale_inv": float(bufs["X"].row.tensor_scale.item())}
+            if args.verify:
+                import oracle as o
+                bits = synth.host_bits(X)
+                scale = None if sc == lpq.SCALING_CURRENT else float(ref_state.scale[0])
+                ref = o.fp8_pertensor(bits, o.E4M3, scale=scale)
+                rec["bit_exact"] = bool(np.array_equal(bufs["X"].row.codes_matrix().cpu().numpy(), ref["row"]) and
+                                        np.array_equal(bufs["X"].col.codes_matrix().cpu().numpy(), ref["col"]))
+                rec["saturated"] = ref["saturated"]
+                if scale is not None:
+                    ref_state.update(ref["amax"], 448.0)
+            steps.append(rec)
+        res[scaling] = {"steps": steps, "mean_ms": statistics.mean(s["ms"] for s in steps[2:])}
+        del bufs, outs
+        torch.cuda.empty_cache()
+    print(json.dumps({"workload": f"FP8 drift, attention-out M={M} K=N={K}, 20 steps", "results": res}), flush=True)
 
 
 def main():
     args = parse()
     if args.mma_peaks:
         run_mma_peaks(args)
+        return
+    if args.workload == "ksweep":
+        run_ksweep(args)
+        return
+    if args.workload == "drift":
+        run_drift(args)
         return
     rank, world, local = dist_setup(args)
     if args.impl == "reference":

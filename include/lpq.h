@@ -230,7 +230,9 @@ lpq_status lpq_selftest_wait(uint64_t limit_ns, lpq_stream_t stream);
  * zero operands resident in shared memory; kind 0 = kind::f16 (bf16, K 16),
  * 1 = kind::f8f6f4 (E4M3, K 32), 2 = MXFP8 block-scaled (K 32), 3 = NVFP4
  * block-scaled (K 64).  with_scale_copies adds the per-step tcgen05.cp of the
- * scale factors (kinds 2, 3).  FLOPs = SMs * iters * 4 * 2 * 128 * 256 * K;
+ * scale factors (kinds 2, 3): 1 = all of a step's copies before its MMAs,
+ * 2 = the same into two alternating TMEM regions, 3 = each MMA's copies
+ * right before it (NVFP4).  FLOPs = SMs * iters * 4 * 2 * 128 * 256 * K;
  * the caller times the launch with events on `stream`. */
 lpq_status lpq_mma_peak(int32_t kind, int32_t iters, int32_t with_scale_copies, lpq_stream_t stream);
 

@@ -734,15 +734,18 @@ __global__ void __launch_bounds__(128, 1) mma_peak_kernel(int iters, int with_sf
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
-  const uint32_t tsfa = tbase + BN, tsfb = tsfa + CF::kSfaCols;
+  // with_sf: 0 none, 1 all copies of a step before its MMAs, 2 the same into
+  // two alternating TMEM regions, 3 each MMA's copies right before it
+  const uint32_t region = CF::kSfaCols + CF::kSfbCols;
   if (threadIdx.x == 0) {
     const uint32_t a_base = smem_u32(sA), b_base = smem_u32(sB);
     for (int it = 0; it < iters; ++it) {
+      const uint32_t tsfa = tbase + BN + (with_sf == 2 ? (it & 1) * region : 0), tsfb = tsfa + CF::kSfaCols;
       if (KIND == kKindMXF8 && with_sf) {
         tmem_cp_sf(tsfa, smem_desc(smem_u32(sSf), 0, 128, 0));
         tmem_cp_sf(tsfb, smem_desc(smem_u32(sSf + 512), 0, 128, 0));
         tmem_cp_sf(tsfb + 4, smem_desc(smem_u32(sSf + 1024), 0, 128, 0));
-      } else if (KIND == kKindNVF4 && with_sf) {
+      } else if (KIND == kKindNVF4 && (with_sf == 1 || with_sf == 2)) {
         for (int j = 0; j < 4; ++j) {
           tmem_cp_sf(tsfa + 4 * j, smem_desc(smem_u32(sSf + j * 512), 0, 128, 0));
           tmem_cp_sf(tsfb + 8 * j, smem_desc(smem_u32(sSf + 2048 + j * 512), 0, 128, 0));
@@ -759,6 +762,11 @@ __global__ void __launch_bounds__(128, 1) mma_peak_kernel(int iters, int with_sf
         } else if constexpr (KIND == kKindMXF8) {
           mma_bs<KIND>(tbase, ad, bd, idesc | ((uint32_t)j << 4) | ((uint32_t)j << 29), tsfa, tsfb, acc);
         } else {
+          if (with_sf == 3) {
+            tmem_cp_sf(tsfa + 4 * j, smem_desc(smem_u32(sSf + j * 512), 0, 128, 0));
+            tmem_cp_sf(tsfb + 8 * j, smem_desc(smem_u32(sSf + 2048 + j * 512), 0, 128, 0));
+            tmem_cp_sf(tsfb + 8 * j + 4, smem_desc(smem_u32(sSf + 4096 + j * 512), 0, 128, 0));
+          }
           mma_bs<KIND>(tbase, ad, bd, idesc, tsfa + 4 * j, tsfb + 8 * j, acc);
         }
       }

@@ -175,13 +175,19 @@ __global__ void __launch_bounds__(kThreads) quant_tile_kernel(const QParams p) {
   const int lc = (t & 15) * 8;  // first of this thread's 8 columns
   const bool col_ok = c0 + lc < C;
   float local_amax = 0.f;
+  // all of this thread's 16-byte loads first, so they are in flight together
+  uint4 vbuf[TR / 16];
+#pragma unroll
+  for (int it = 0; it < TR / 16; ++it) {
+    const int64_t r = r0 + it * 16 + lr;
+    vbuf[it] = (col_ok && r < R) ? ld_stream(p.x + r * C + c0 + lc) : make_uint4(0u, 0u, 0u, 0u);
+  }
 #pragma unroll
   for (int it = 0; it < TR / 16; ++it) {
     const int rl = it * 16 + lr;
     const int64_t r = r0 + rl;
     const bool ok = col_ok && r < R;
-    uint4 v = make_uint4(0u, 0u, 0u, 0u);
-    if (ok) v = ld_stream(p.x + r * C + c0 + lc);
+    const uint4 v = vbuf[it];
     if (kNeedTile) *reinterpret_cast<uint4*>(&tile[rl][lc]) = v;
     float f[8];
     unpack8(v, f);
