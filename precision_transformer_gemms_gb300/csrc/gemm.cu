@@ -169,50 +169,50 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       // ---------------------------------------------------------- MMA issuer
-      uint32_t it = 0, lt = 0;
+      // Descriptors are precomputed: only the low word (start address >> 4)
+      // changes between stages and K steps.  Each MMA's scale-factor copies
+      // are issued right before it, so they overlap the previous MMA.
+      const uint32_t kHiSw = (uint32_t)(smem_desc(0, 16, 1024, 2) >> 32);
+      const uint32_t kLoSw = (uint32_t)smem_desc(0, 16, 1024, 2);
+      const uint32_t kHiSf = (uint32_t)(smem_desc(0, 0, 128, 0) >> 32);
+      const uint32_t a0 = kLoSw | (smem_u32(sA) >> 4), b0 = kLoSw | (smem_u32(sB) >> 4);
+      const uint32_t fa0 = smem_u32(sSfa) >> 4, fb0 = smem_u32(sSfb) >> 4;
+      uint32_t s = 0, ph = 0, lt = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++lt) {
         const uint32_t a = lt % NACC, aph = (lt / NACC) & 1u;
         if (!(ok = mbar_wait_bounded(&acc_empty[a], aph ^ 1u, abort_flag, &g_device_error))) break;
         tc_fence_after();
         const uint32_t tmem_d = tmem_base + a * BN;
-        for (int kt = 0; kt < g.num_k; ++kt, ++it) {
-          const int s = it % S;
-          const uint32_t ph = (it / S) & 1u;
+        for (int kt = 0; kt < g.num_k; ++kt) {
           if (!(ok = mbar_wait_bounded(&full[s], ph, abort_flag, &g_device_error))) break;
           tc_fence_after();
-          const uint32_t a_base = smem_u32(sA + s * CF::kA);
-          const uint32_t b_base = smem_u32(sB + s * CF::kB);
+          const uint32_t alo = a0 + s * (CF::kA >> 4), blo = b0 + s * (CF::kB >> 4);
+          const uint32_t falo = fa0 + s * (CF::kSfa >> 4), fblo = fb0 + s * (CF::kSfb >> 4);
           if constexpr (KIND == kKindMXF8) {
-            tmem_cp_sf(tmem_sfa, smem_desc(smem_u32(sSfa + s * CF::kSfa), 0, 128, 0));
+            tmem_cp_sf(tmem_sfa, ((uint64_t)kHiSf << 32) | falo);
 #pragma unroll
-            for (int i = 0; i < BN / 128; ++i)
-              tmem_cp_sf(tmem_sfb + 4 * i, smem_desc(smem_u32(sSfb + s * CF::kSfb + i * 512), 0, 128, 0));
-          } else if constexpr (KIND == kKindNVF4) {
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              tmem_cp_sf(tmem_sfa + 4 * j, smem_desc(smem_u32(sSfa + s * CF::kSfa + j * 512), 0, 128, 0));
-#pragma unroll
-              for (int i = 0; i < BN / 128; ++i)
-                tmem_cp_sf(tmem_sfb + 4 * (BN / 128) * j + 4 * i,
-                           smem_desc(smem_u32(sSfb + s * CF::kSfb + (i * 4 + j) * 512), 0, 128, 0));
-            }
+            for (int i = 0; i < BN / 128; ++i) tmem_cp_sf(tmem_sfb + 4 * i, ((uint64_t)kHiSf << 32) | (fblo + i * 32));
           }
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
-            const uint64_t ad = smem_desc(a_base + 32 * j, 16, 1024, 2);
-            const uint64_t bd = smem_desc(b_base + 32 * j, 16, 1024, 2);
+            const uint64_t ad = ((uint64_t)kHiSw << 32) | (alo + 2 * j);
+            const uint64_t bd = ((uint64_t)kHiSw << 32) | (blo + 2 * j);
             const uint32_t acc = (kt > 0 || j > 0) ? 1u : 0u;
             if constexpr (KIND == kKindF16 || KIND == kKindF8F6F4) {
               mma_ss<KIND>(tmem_d, ad, bd, g.idesc, acc);
             } else if constexpr (KIND == kKindMXF8) {
-              const uint32_t id = g.idesc | ((uint32_t)j << 4) | ((uint32_t)j << 29);
-              mma_bs<KIND>(tmem_d, ad, bd, id, tmem_sfa, tmem_sfb, acc);
+              mma_bs<KIND>(tmem_d, ad, bd, g.idesc | ((uint32_t)j << 4) | ((uint32_t)j << 29), tmem_sfa, tmem_sfb, acc);
             } else {
+              tmem_cp_sf(tmem_sfa + 4 * j, ((uint64_t)kHiSf << 32) | (falo + j * 32));
+#pragma unroll
+              for (int i = 0; i < BN / 128; ++i)
+                tmem_cp_sf(tmem_sfb + 4 * (BN / 128) * j + 4 * i, ((uint64_t)kHiSf << 32) | (fblo + (i * 4 + j) * 32));
               mma_bs<KIND>(tmem_d, ad, bd, g.idesc, tmem_sfa + 4 * j, tmem_sfb + 4 * (BN / 128) * j, acc);
             }
           }
           tc_commit(&empty[s]);
+          if (++s == (uint32_t)S) { s = 0; ph ^= 1u; }
         }
         if (ok) tc_commit(&acc_full[a]);
       }
@@ -405,11 +405,13 @@ constexpr int kBlkBN = 128;
 constexpr int kBlkStages = 6;
 constexpr int kBlkStage = kBM * kKBytes + kBlkBN * kKBytes;
 constexpr int kBlkSmem = kBlkStages * kBlkStage + 1024 + 512 + kBlkBN * 4;
+constexpr int kBlkEpiWarps = 8;  // two per TMEM lane quarter, 64 columns each
+constexpr int kBlkThreads = 64 + 32 * kBlkEpiWarps;
 
-__global__ void __launch_bounds__(kThreadsGemm, 1)
+__global__ void __launch_bounds__(kBlkThreads, 1)
     block_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                       const BlockArgs g) {
-  constexpr int S = kBlkStages, BN = kBlkBN;
+  constexpr int S = kBlkStages, BN = kBlkBN, HALF = BN / 2;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
@@ -432,7 +434,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&acc_full[a], 1);
-      mbar_init(&acc_empty[a], 4);
+      mbar_init(&acc_empty[a], kBlkEpiWarps);
     }
     *abort_flag = 0;
     fence_barrier_init();
@@ -464,30 +466,33 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      uint32_t it = 0, slice = 0;
+      const uint32_t kHiSw = (uint32_t)(smem_desc(0, 16, 1024, 2) >> 32);
+      const uint32_t a0 = (uint32_t)smem_desc(smem_u32(sA), 16, 1024, 2);
+      const uint32_t b0 = (uint32_t)smem_desc(smem_u32(sB), 16, 1024, 2);
+      uint32_t s = 0, ph = 0, slice = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-        for (int kt = 0; kt < g.num_k; ++kt, ++it, ++slice) {
+        for (int kt = 0; kt < g.num_k; ++kt, ++slice) {
           const uint32_t a = slice & 1u, aph = (slice >> 1) & 1u;
           if (!(ok = mbar_wait_bounded(&acc_empty[a], aph ^ 1u, abort_flag, &g_device_error))) break;
-          const int s = it % S;
-          const uint32_t ph = (it / S) & 1u;
           if (!(ok = mbar_wait_bounded(&full[s], ph, abort_flag, &g_device_error))) break;
           tc_fence_after();
-          const uint32_t a_base = smem_u32(sA + s * kBM * kKBytes);
-          const uint32_t b_base = smem_u32(sB + s * BN * kKBytes);
+          const uint32_t alo = a0 + s * (kBM * kKBytes >> 4), blo = b0 + s * (BN * kKBytes >> 4);
 #pragma unroll
           for (int j = 0; j < 4; ++j)
-            mma_ss<kKindF8F6F4>(tmem_base + a * BN, smem_desc(a_base + 32 * j, 16, 1024, 2),
-                                smem_desc(b_base + 32 * j, 16, 1024, 2), g.idesc, j > 0 ? 1u : 0u);
+            mma_ss<kKindF8F6F4>(tmem_base + a * BN, ((uint64_t)kHiSw << 32) | (alo + 2 * j),
+                                ((uint64_t)kHiSw << 32) | (blo + 2 * j), g.idesc, j > 0 ? 1u : 0u);
           tc_commit(&empty[s]);
           tc_commit(&acc_full[a]);
+          if (++s == (uint32_t)S) { s = 0; ph ^= 1u; }
         }
       }
     }
   } else {
-    const int q = warp & 3;
-    const int et = threadIdx.x - 64;  // 0..127 across the epilogue warps
+    const int ew = warp - 2;          // 0..7
+    const int q = warp & 3;           // TMEM lane quarter
+    const int half = ew >> 2;         // column half of the tile
+    const int et = threadIdx.x - 64;  // 0..255
     const bool vec_ok = g.c_fp32 ? (g.N % 4 == 0) : (g.N % 8 == 0);
     uint32_t slice = 0;
     bool ok = true;
@@ -496,9 +501,9 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
       tile_coords(t, g.tiles_m, g.tiles_n, mt, nt);
       const int64_t row = (int64_t)mt * kBM + q * 32 + lane;
       const int64_t n0 = (int64_t)nt * BN;
-      float acc[BN];
+      float acc[HALF];
 #pragma unroll
-      for (int i = 0; i < BN; ++i) acc[i] = 0.f;
+      for (int i = 0; i < HALF; ++i) acc[i] = 0.f;
       for (int kt = 0; kt < g.num_k; ++kt, ++slice) {
         const uint32_t a = slice & 1u, aph = (slice >> 1) & 1u;
         // this slice's factors: A per row (or per 128-row block), B per column (or block)
@@ -506,21 +511,23 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
         if (g.a_rows == 1) fa = row < g.M ? g.sa[(int64_t)kt * g.M + row] : 0.f;
         else fa = g.sa[(int64_t)mt * KB + kt];
         if (g.b_rows == 1) {
-          asm volatile("bar.sync 1, 128;" ::: "memory");
-          const int64_t n = n0 + et;
-          s_sb[et] = n < g.N ? g.sb[(int64_t)kt * g.N + n] : 0.f;
-          asm volatile("bar.sync 1, 128;" ::: "memory");
+          asm volatile("bar.sync 1, %0;" ::"n"(32 * kBlkEpiWarps) : "memory");
+          if (et < BN) {
+            const int64_t n = n0 + et;
+            s_sb[et] = n < g.N ? g.sb[(int64_t)kt * g.N + n] : 0.f;
+          }
+          asm volatile("bar.sync 1, %0;" ::"n"(32 * kBlkEpiWarps) : "memory");
         }
         const float fb_blk = g.b_rows == 1 ? 0.f : g.sb[(n0 / 128) * KB + kt];
         if (!(ok = mbar_wait_bounded(&acc_full[a], aph, abort_flag, &g_device_error))) break;
         __syncwarp();
         tc_fence_after();
-        const uint32_t tb = tmem_base + a * BN + ((uint32_t)(q * 32) << 16);
+        const uint32_t tb = tmem_base + a * BN + half * HALF + ((uint32_t)(q * 32) << 16);
 #pragma unroll
-        for (int cc = 0; cc < BN / 32; ++cc) {
+        for (int cc = 0; cc < 2; ++cc) {
           uint32_t v[32];
-          tmem_ld32(tb + (uint32_t)(cc * 32), v);
-          if (cc == BN / 32 - 1) {
+          tmem_ld32(tb + 32 * cc, v);
+          if (cc == 1) {  // slice fully read: the MMA warp may reuse this buffer
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&acc_empty[a]);
@@ -528,33 +535,34 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
           if (g.b_rows == 1) {
 #pragma unroll
             for (int i = 0; i < 32; ++i)
-              acc[cc * 32 + i] = __fadd_rn(acc[cc * 32 + i],
-                                           __fmul_rn(__uint_as_float(v[i]), __fmul_rn(fa, s_sb[cc * 32 + i])));
+              acc[32 * cc + i] = fmaf(__uint_as_float(v[i]), fa * s_sb[half * HALF + 32 * cc + i], acc[32 * cc + i]);
           } else {
-            const float f = __fmul_rn(fa, fb_blk);
+            const float f = fa * fb_blk;
 #pragma unroll
-            for (int i = 0; i < 32; ++i) acc[cc * 32 + i] = __fadd_rn(acc[cc * 32 + i], __fmul_rn(__uint_as_float(v[i]), f));
+            for (int i = 0; i < 32; ++i) acc[32 * cc + i] = fmaf(__uint_as_float(v[i]), f, acc[32 * cc + i]);
           }
         }
       }
       if (!ok || row >= g.M) continue;
-      const int64_t ncols = g.N - n0;
+      const int64_t c0 = n0 + half * HALF;
+      const int64_t ncols = g.N - c0;
+      if (ncols <= 0) continue;
       if (g.c_fp32) {
-        float* out = static_cast<float*>(g.c) + row * g.N + n0;
-        if (vec_ok && ncols >= BN) {
+        float* out = static_cast<float*>(g.c) + row * g.N + c0;
+        if (vec_ok && ncols >= HALF) {
 #pragma unroll
-          for (int i = 0; i < BN / 4; ++i)
+          for (int i = 0; i < HALF / 4; ++i)
             reinterpret_cast<float4*>(out)[i] = make_float4(acc[4 * i], acc[4 * i + 1], acc[4 * i + 2], acc[4 * i + 3]);
         } else {
 #pragma unroll
-          for (int i = 0; i < BN; ++i)
+          for (int i = 0; i < HALF; ++i)
             if (i < ncols) out[i] = acc[i];
         }
       } else {
-        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(g.c) + row * g.N + n0;
-        if (vec_ok && ncols >= BN) {
+        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(g.c) + row * g.N + c0;
+        if (vec_ok && ncols >= HALF) {
 #pragma unroll
-          for (int i = 0; i < BN / 8; ++i) {
+          for (int i = 0; i < HALF / 8; ++i) {
             uint32_t w[4];
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
@@ -565,7 +573,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
           }
         } else {
 #pragma unroll
-          for (int i = 0; i < BN; ++i)
+          for (int i = 0; i < HALF; ++i)
             if (i < ncols) out[i] = __float2bfloat16_rn(acc[i]);
         }
       }
@@ -596,7 +604,7 @@ lpq_status run_block_gemm(const CUtensorMap& ta, const CUtensorMap& tb, BlockArg
   g.tiles_m = (int)tm;
   g.tiles_n = (int)tn;
   const int grid = (int)std::min<int64_t>(tm * tn, g_sms);
-  block_gemm_kernel<<<grid, kThreadsGemm, kBlkSmem, s>>>(ta, tb, g);
+  block_gemm_kernel<<<grid, kBlkThreads, kBlkSmem, s>>>(ta, tb, g);
   return cuda_check(cudaGetLastError(), "block gemm launch");
 }
 
@@ -738,34 +746,38 @@ __global__ void __launch_bounds__(128, 1) mma_peak_kernel(int iters, int with_sf
   // two alternating TMEM regions, 3 each MMA's copies right before it
   const uint32_t region = CF::kSfaCols + CF::kSfbCols;
   if (threadIdx.x == 0) {
-    const uint32_t a_base = smem_u32(sA), b_base = smem_u32(sB);
+    const uint32_t kHiSw = (uint32_t)(smem_desc(0, 16, 1024, 2) >> 32);
+    const uint32_t kHiSf = (uint32_t)(smem_desc(0, 0, 128, 0) >> 32);
+    const uint32_t alo = (uint32_t)smem_desc(smem_u32(sA), 16, 1024, 2), blo = (uint32_t)smem_desc(smem_u32(sB), 16, 1024, 2);
+    const uint32_t flo = smem_u32(sSf) >> 4;
+    const bool cps_first = with_sf == 1 || with_sf == 2, cps_inter = with_sf == 3;
     for (int it = 0; it < iters; ++it) {
       const uint32_t tsfa = tbase + BN + (with_sf == 2 ? (it & 1) * region : 0), tsfb = tsfa + CF::kSfaCols;
       if (KIND == kKindMXF8 && with_sf) {
-        tmem_cp_sf(tsfa, smem_desc(smem_u32(sSf), 0, 128, 0));
-        tmem_cp_sf(tsfb, smem_desc(smem_u32(sSf + 512), 0, 128, 0));
-        tmem_cp_sf(tsfb + 4, smem_desc(smem_u32(sSf + 1024), 0, 128, 0));
-      } else if (KIND == kKindNVF4 && (with_sf == 1 || with_sf == 2)) {
+        tmem_cp_sf(tsfa, ((uint64_t)kHiSf << 32) | flo);
+        tmem_cp_sf(tsfb, ((uint64_t)kHiSf << 32) | (flo + 32));
+        tmem_cp_sf(tsfb + 4, ((uint64_t)kHiSf << 32) | (flo + 64));
+      } else if (KIND == kKindNVF4 && cps_first) {
         for (int j = 0; j < 4; ++j) {
-          tmem_cp_sf(tsfa + 4 * j, smem_desc(smem_u32(sSf + j * 512), 0, 128, 0));
-          tmem_cp_sf(tsfb + 8 * j, smem_desc(smem_u32(sSf + 2048 + j * 512), 0, 128, 0));
-          tmem_cp_sf(tsfb + 8 * j + 4, smem_desc(smem_u32(sSf + 4096 + j * 512), 0, 128, 0));
+          tmem_cp_sf(tsfa + 4 * j, ((uint64_t)kHiSf << 32) | (flo + j * 32));
+          tmem_cp_sf(tsfb + 8 * j, ((uint64_t)kHiSf << 32) | (flo + 128 + j * 32));
+          tmem_cp_sf(tsfb + 8 * j + 4, ((uint64_t)kHiSf << 32) | (flo + 256 + j * 32));
         }
       }
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const uint64_t ad = smem_desc(a_base + 32 * j, 16, 1024, 2);
-        const uint64_t bd = smem_desc(b_base + 32 * j, 16, 1024, 2);
+        const uint64_t ad = ((uint64_t)kHiSw << 32) | (alo + 2 * j);
+        const uint64_t bd = ((uint64_t)kHiSw << 32) | (blo + 2 * j);
         const uint32_t acc = (it > 0 || j > 0) ? 1u : 0u;
         if constexpr (KIND == kKindF16 || KIND == kKindF8F6F4) {
           mma_ss<KIND>(tbase, ad, bd, idesc, acc);
         } else if constexpr (KIND == kKindMXF8) {
           mma_bs<KIND>(tbase, ad, bd, idesc | ((uint32_t)j << 4) | ((uint32_t)j << 29), tsfa, tsfb, acc);
         } else {
-          if (with_sf == 3) {
-            tmem_cp_sf(tsfa + 4 * j, smem_desc(smem_u32(sSf + j * 512), 0, 128, 0));
-            tmem_cp_sf(tsfb + 8 * j, smem_desc(smem_u32(sSf + 2048 + j * 512), 0, 128, 0));
-            tmem_cp_sf(tsfb + 8 * j + 4, smem_desc(smem_u32(sSf + 4096 + j * 512), 0, 128, 0));
+          if (cps_inter) {
+            tmem_cp_sf(tsfa + 4 * j, ((uint64_t)kHiSf << 32) | (flo + j * 32));
+            tmem_cp_sf(tsfb + 8 * j, ((uint64_t)kHiSf << 32) | (flo + 128 + j * 32));
+            tmem_cp_sf(tsfb + 8 * j + 4, ((uint64_t)kHiSf << 32) | (flo + 256 + j * 32));
           }
           mma_bs<KIND>(tbase, ad, bd, idesc, tsfa + 4 * j, tsfb + 8 * j, acc);
         }

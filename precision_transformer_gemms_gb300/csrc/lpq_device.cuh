@@ -165,10 +165,11 @@ __device__ __forceinline__ void rht16(float t[16], uint32_t signs) {
 // lo <= |y| <= hi, round up iff float(r >> 8) < ((|y| - lo) / (hi - lo)) * 2^24.
 // hi - lo is 0.5, 1 or 2, so the quotient times 2^24 is the exact product
 // (|y| - lo) * 2^24 / (hi - lo) (Sterbenz subtraction, power-of-two scaling).
+// Written with selects rather than branches: lanes of a warp fall on
+// different grid segments.
 __device__ __forceinline__ uint32_t sr_e2m1(float y, uint32_t r) {
   const uint32_t s = (__float_as_uint(y) >> 31) << 3;
   const float a = fabsf(y);
-  // lower neighbour `lo` (code and value) and 2^24 / (hi - lo) on each grid segment
   const bool seg0 = a < 2.0f, seg1 = a < 4.0f;
   const float t = seg0 ? __fmul_rn(a, 2.0f) : a;                  // exact
   const uint32_t q = (uint32_t)__float2int_rz(t);                  // 0..3 (seg0), 2..3 (seg1)
