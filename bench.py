@@ -266,6 +266,28 @@ class Layer:
                 e1.record()
                 events.append((name, "gemm", e0, e1))
 
+    def fused_step(self, recipe, step_idx=0):
+        """One layer with each tensor quantized once into both copies (one
+        lpq_quantize per tensor and linear), then the linear's three GEMMs."""
+        L = self.lpq
+        for lin in self.linears:
+            for role in ("X", "W", "dY"):
+                fmt, extra, scaling = self.qcfg(recipe, role)
+                flags = L.ROWWISE | L.COLWISE | extra
+                if recipe == "nvfp4" and role in ("X", "dY"):
+                    flags |= L.RHT_COLWISE
+                qt = L.QTensor(self.buf(recipe, lin, role, False), self.buf(recipe, lin, role, True))
+                st = self.state(lin, role) if scaling == L.SCALING_DELAYED else None
+                L.quantize(self.inp[lin][role], fmt, flags, scaling=scaling, seed=step_idx * 64, rht_seed=1234,
+                           state=st, out=qt)
+                if st is not None:
+                    L.scale_update(st, qt.row.amax, L.FMAX[fmt])
+            for name, lay, lin2 in self.gemm_list():
+                if lin2 != lin:
+                    continue
+                (ra, ca), (rb, cb) = self.PASS[lay]
+                L.gemm(lay, self.buf(recipe, lin, ra, ca), self.buf(recipe, lin, rb, cb), c=self.out[name])
+
     def kernels_per_step(self, recipe, autocast):
         """Kernels of liblpq launched by one step (memsets are not kernels of ours)."""
         n = 12  # GEMMs
@@ -479,6 +501,19 @@ def run_lpq(args, rank, world, local):
                 ms, _ = time_steps(layer, r, ac, k, 2, world)
                 res[f"{mode}_ms_per_layer"] = ms
                 res[f"{mode}_tflops"] = layer.flops / (ms * 1e-3) / 1e12
+            if r != "bf16":
+                import torch
+                for w in range(2):
+                    layer.fused_step(r, w)
+                torch.cuda.synchronize()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                for s_ in range(k):
+                    layer.fused_step(r, 10 + s_)
+                e1.record()
+                torch.cuda.synchronize()
+                res["fused_ms_per_layer"] = e0.elapsed_time(e1) / k
+                res["fused_tflops"] = layer.flops / (res["fused_ms_per_layer"] * 1e-3) / 1e12
             recipes[r] = res
             # free this recipe's buffers before the next one
             for key in [k_ for k_ in layer.bufs if k_[0] == r and r != recipe]:
@@ -486,8 +521,9 @@ def run_lpq(args, rank, world, local):
             torch.cuda.empty_cache()
         if "bf16" in recipes:
             for r, res in recipes.items():
-                for mode in ("autocast", "prequant"):
-                    res[f"{mode}_speedup_vs_bf16"] = recipes["bf16"]["prequant_ms_per_layer"] / res[f"{mode}_ms_per_layer"]
+                for mode in ("autocast", "prequant", "fused"):
+                    if f"{mode}_ms_per_layer" in res:
+                        res[f"{mode}_speedup_vs_bf16"] = recipes["bf16"]["prequant_ms_per_layer"] / res[f"{mode}_ms_per_layer"]
 
     # e2e: pinned host inputs -> device, step, outputs -> host, every step
     e2e = None

@@ -58,7 +58,8 @@ struct Cfg {
 };
 
 constexpr int kGroupM = 16;  // tiles along M that share a band of B tiles (L2 reuse)
-constexpr int kThreadsGemm = 192;
+constexpr int kEpiWarps = 8;  // two per TMEM lane quarter, each owning half of the tile's columns
+constexpr int kThreadsGemm = 64 + 32 * kEpiWarps;
 
 struct GemmArgs {
   const uint8_t* sfa;  // tensor-core scale layout of A (block-scaled kinds)
@@ -120,7 +121,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
     }
     for (int a = 0; a < NACC; ++a) {
       mbar_init(&acc_full[a], 1);
-      mbar_init(&acc_empty[a], 4);  // one arrive per epilogue warp
+      mbar_init(&acc_empty[a], kEpiWarps);  // one arrive per epilogue warp
     }
     *abort_flag = 0;
     fence_barrier_init();
@@ -219,7 +220,10 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    const int q = warp & 3;  // TMEM lane quarter of this warp
+    // Warp w reads TMEM lanes 32 * (w % 4) .. of columns [half * BN/2, +BN/2).
+    constexpr int HALF = BN / 2;
+    const int q = warp & 3;
+    const int half = (warp - 2) >> 2;
     float alpha = 1.0f;
     if (g.alpha_a) alpha = *g.alpha_a;
     if (g.alpha_b) alpha = __fmul_rn(alpha, *g.alpha_b);
@@ -233,60 +237,53 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
       __syncwarp();
       tc_fence_after();
       const int64_t row = (int64_t)mt * kBM + q * 32 + lane;
-      const uint32_t tbase = tmem_base + a * BN + ((uint32_t)(q * 32) << 16);
+      const int64_t c0 = (int64_t)nt * BN + half * HALF;
+      const int64_t ncols = g.N - c0;
+      const uint32_t tbase = tmem_base + a * BN + half * HALF + ((uint32_t)(q * 32) << 16);
       if (!g.c_fp32) {
-        // bf16 output, 128 columns at a time: drain TMEM into registers as
-        // packed bf16 pairs and store them; TMEM goes back to the MMA warp as
-        // soon as the last group is in registers, before its stores.
-        __nv_bfloat16* out_row = static_cast<__nv_bfloat16*>(g.c) + row * g.N + (int64_t)nt * BN;
-        const int64_t ncols = g.N - (int64_t)nt * BN;
-#pragma unroll 1
-        for (int grp = 0; grp < BN / 128; ++grp) {
-          uint32_t pk[64];
+        // bf16: the warp's whole column range into registers as packed pairs,
+        // TMEM handed back, then the stores.
+        uint32_t pk[HALF / 2];
 #pragma unroll
-          for (int cc = 0; cc < 4; ++cc) {
-            uint32_t v[32];
-            tmem_ld32(tbase + (uint32_t)(grp * 128 + cc * 32), v);
+        for (int cc = 0; cc < HALF / 32; ++cc) {
+          uint32_t v[32];
+          tmem_ld32(tbase + (uint32_t)(cc * 32), v);
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              __nv_bfloat162 h = __floats2bfloat162_rn(__fmul_rn(__uint_as_float(v[2 * i]), alpha),
-                                                       __fmul_rn(__uint_as_float(v[2 * i + 1]), alpha));
-              pk[cc * 16 + i] = *reinterpret_cast<uint32_t*>(&h);
-            }
+          for (int i = 0; i < 16; ++i) {
+            __nv_bfloat162 h = __floats2bfloat162_rn(__fmul_rn(__uint_as_float(v[2 * i]), alpha),
+                                                     __fmul_rn(__uint_as_float(v[2 * i + 1]), alpha));
+            pk[cc * 16 + i] = *reinterpret_cast<uint32_t*>(&h);
           }
-          if (grp == BN / 128 - 1) {
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&acc_empty[a]);
-          }
-          if (row < g.M) {
-            __nv_bfloat16* out = out_row + grp * 128;
-            const int64_t nc = ncols - grp * 128;
-            if (vec_ok && nc >= 128) {
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acc_empty[a]);
+        if (row < g.M && ncols > 0) {
+          __nv_bfloat16* out = static_cast<__nv_bfloat16*>(g.c) + row * g.N + c0;
+          if (vec_ok && ncols >= HALF) {
 #pragma unroll
-              for (int i = 0; i < 16; ++i)
-                reinterpret_cast<uint4*>(out)[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
-            } else {
+            for (int i = 0; i < HALF / 8; ++i)
+              reinterpret_cast<uint4*>(out)[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+          } else {
 #pragma unroll
-              for (int i = 0; i < 64; ++i) {
-                if (2 * i < nc) out[2 * i] = __ushort_as_bfloat16((unsigned short)(pk[i] & 0xFFFFu));
-                if (2 * i + 1 < nc) out[2 * i + 1] = __ushort_as_bfloat16((unsigned short)(pk[i] >> 16));
-              }
+            for (int i = 0; i < HALF / 2; ++i) {
+              if (2 * i < ncols) out[2 * i] = __ushort_as_bfloat16((unsigned short)(pk[i] & 0xFFFFu));
+              if (2 * i + 1 < ncols) out[2 * i + 1] = __ushort_as_bfloat16((unsigned short)(pk[i] >> 16));
             }
           }
         }
         continue;
       }
 #pragma unroll 1
-      for (int cc = 0; cc < BN / 32; ++cc) {
+      for (int cc = 0; cc < HALF / 32; ++cc) {
         uint32_t v[32];
         tmem_ld32(tbase + (uint32_t)(cc * 32), v);
-        if (cc == BN / 32 - 1) {  // accumulator fully read: hand it back to the MMA warp
+        if (cc == HALF / 32 - 1) {  // accumulator columns fully read: hand them back
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&acc_empty[a]);
         }
-        const int64_t col0 = (int64_t)nt * BN + cc * 32;
+        const int64_t col0 = c0 + cc * 32;
         if (row >= g.M || col0 >= g.N) continue;
         float* out = static_cast<float*>(g.c) + row * g.N + col0;
         if (vec_ok && col0 + 32 <= g.N) {
@@ -716,8 +713,9 @@ lpq_status launch_gemm(const lpq_qview* a, const lpq_qview* b, void* c, int32_t 
 // 128 x 256 MMAs on operand tiles resident in shared memory (no global
 // traffic), optionally with the per-step scale-factor copies of the
 // block-scaled kinds.  Operands are zero; the FLOP count is what is timed.
-template <int KIND>
-__global__ void __launch_bounds__(128, 1) mma_peak_kernel(int iters, int with_sf, uint32_t idesc) {
+template <int KIND, int MODE>
+__global__ void __launch_bounds__(128, 1) mma_peak_kernel(int iters, uint32_t idesc) {
+  constexpr int with_sf = MODE;
   constexpr int BN = 256;
   using CF = Cfg<KIND, BN, 1>;
   extern __shared__ uint8_t smem_raw[];
@@ -750,14 +748,14 @@ __global__ void __launch_bounds__(128, 1) mma_peak_kernel(int iters, int with_sf
     const uint32_t kHiSf = (uint32_t)(smem_desc(0, 0, 128, 0) >> 32);
     const uint32_t alo = (uint32_t)smem_desc(smem_u32(sA), 16, 1024, 2), blo = (uint32_t)smem_desc(smem_u32(sB), 16, 1024, 2);
     const uint32_t flo = smem_u32(sSf) >> 4;
-    const bool cps_first = with_sf == 1 || with_sf == 2, cps_inter = with_sf == 3;
+    constexpr bool cps_first = with_sf == 1 || with_sf == 2, cps_inter = with_sf == 3;
     for (int it = 0; it < iters; ++it) {
       const uint32_t tsfa = tbase + BN + (with_sf == 2 ? (it & 1) * region : 0), tsfb = tsfa + CF::kSfaCols;
-      if (KIND == kKindMXF8 && with_sf) {
+      if constexpr (KIND == kKindMXF8 && with_sf) {
         tmem_cp_sf(tsfa, ((uint64_t)kHiSf << 32) | flo);
         tmem_cp_sf(tsfb, ((uint64_t)kHiSf << 32) | (flo + 32));
         tmem_cp_sf(tsfb + 4, ((uint64_t)kHiSf << 32) | (flo + 64));
-      } else if (KIND == kKindNVF4 && cps_first) {
+      } else if constexpr (KIND == kKindNVF4 && cps_first) {
         for (int j = 0; j < 4; ++j) {
           tmem_cp_sf(tsfa + 4 * j, ((uint64_t)kHiSf << 32) | (flo + j * 32));
           tmem_cp_sf(tsfb + 8 * j, ((uint64_t)kHiSf << 32) | (flo + 128 + j * 32));
@@ -774,7 +772,7 @@ __global__ void __launch_bounds__(128, 1) mma_peak_kernel(int iters, int with_sf
         } else if constexpr (KIND == kKindMXF8) {
           mma_bs<KIND>(tbase, ad, bd, idesc | ((uint32_t)j << 4) | ((uint32_t)j << 29), tsfa, tsfb, acc);
         } else {
-          if (cps_inter) {
+          if constexpr (cps_inter) {
             tmem_cp_sf(tsfa + 4 * j, ((uint64_t)kHiSf << 32) | (flo + j * 32));
             tmem_cp_sf(tsfb + 8 * j, ((uint64_t)kHiSf << 32) | (flo + 128 + j * 32));
             tmem_cp_sf(tsfb + 8 * j + 4, ((uint64_t)kHiSf << 32) | (flo + 256 + j * 32));
@@ -794,29 +792,36 @@ __global__ void __launch_bounds__(128, 1) mma_peak_kernel(int iters, int with_sf
   }
 }
 
-template <int KIND>
-lpq_status run_peak(int iters, int with_sf, uint32_t idesc, cudaStream_t s) {
+template <int KIND, int MODE>
+lpq_status run_peak(int iters, uint32_t idesc, cudaStream_t s) {
   using CF = Cfg<KIND, 256, 1>;
   const int smem = CF::kA + CF::kB + CF::kSfa + CF::kSfb + 1024 + 256;
   static bool attr = false;
   if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(mma_peak_kernel<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e = cudaFuncSetAttribute(mma_peak_kernel<KIND, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return cuda_check(e, "cudaFuncSetAttribute(peak)");
     attr = true;
   }
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  mma_peak_kernel<KIND><<<sms, 128, smem, s>>>(iters, with_sf, idesc);
+  mma_peak_kernel<KIND, MODE><<<sms, 128, smem, s>>>(iters, idesc);
   return cuda_check(cudaGetLastError(), "peak kernel launch");
 }
 
 lpq_status launch_mma_peak(int32_t kind, int32_t iters, int32_t with_sf, cudaStream_t s) {
+  const uint32_t mx = idesc_block_scaled(0, 0, 1, 256), nv = idesc_block_scaled(1, 1, 0, 256);
   switch (kind) {
-    case kKindF16: return run_peak<kKindF16>(iters, 0, idesc_dense(1, 1, 256), s);
-    case kKindF8F6F4: return run_peak<kKindF8F6F4>(iters, 0, idesc_dense(0, 0, 256), s);
-    case kKindMXF8: return run_peak<kKindMXF8>(iters, with_sf, idesc_block_scaled(0, 0, 1, 256), s);
-    case kKindNVF4: return run_peak<kKindNVF4>(iters, with_sf, idesc_block_scaled(1, 1, 0, 256), s);
+    case kKindF16: return run_peak<kKindF16, 0>(iters, idesc_dense(1, 1, 256), s);
+    case kKindF8F6F4: return run_peak<kKindF8F6F4, 0>(iters, idesc_dense(0, 0, 256), s);
+    case kKindMXF8: return with_sf ? run_peak<kKindMXF8, 1>(iters, mx, s) : run_peak<kKindMXF8, 0>(iters, mx, s);
+    case kKindNVF4:
+      switch (with_sf) {
+        case 0: return run_peak<kKindNVF4, 0>(iters, nv, s);
+        case 1: return run_peak<kKindNVF4, 1>(iters, nv, s);
+        case 2: return run_peak<kKindNVF4, 2>(iters, nv, s);
+        default: return run_peak<kKindNVF4, 3>(iters, nv, s);
+      }
   }
   return set_error(LPQ_ERR_INVALID_ARG, "kind %d", kind);
 }
