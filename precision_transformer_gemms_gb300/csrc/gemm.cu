@@ -379,6 +379,333 @@ lpq_status run(const CUtensorMap& ta, const CUtensorMap& tb, GemmArgs g, cudaStr
   return cuda_check(cudaGetLastError(), "gemm kernel launch");
 }
 
+// CTA-pair GEMM (cta_group::2).  A cluster of two CTAs on two SMs computes a
+// 256 x 256 output tile: each CTA loads its own 128 rows of A and its own 128
+// rows of B (each SM streams half the B bytes of the single-CTA kernel), the
+// even CTA issues the pair MMAs, and each CTA's TMEM holds the accumulator
+// rows of its half.  Every load is a TMA tile load that signals the even
+// CTA's full barrier; MMA completion is multicast to both CTAs.  For the
+// block-scaled kinds each CTA also loads the scale atoms of its A rows and of
+// all 256 B rows of the tile (each CTA's accumulator spans every column, so
+// each TMEM needs every column's scales; kSfbFull = false, each CTA holding
+// only its own 128 B rows, does not match the pair MMA), which the pair
+// copies (tcgen05.cp.cta_group::2) move into each CTA's TMEM.
+constexpr int kPairBN = 256;
+
+template <int KIND, bool kSfbFull>
+struct PairCfg {
+  static constexpr int kSfAtoms = KIND == kKindNVF4 ? 4 : (KIND == kKindMXF8 ? 1 : 0);
+  static constexpr int kA = kBM * kKBytes;
+  static constexpr int kB = (kPairBN / 2) * kKBytes;
+  static constexpr int kSfbGroups = kSfbFull ? 2 : 1;
+  static constexpr int kSfa = kSfAtoms * 512;
+  static constexpr int kSfb = kSfAtoms * 512 * kSfbGroups;
+  static constexpr int kStage = kA + kB + kSfa + kSfb;
+  static constexpr int kStages = (220 * 1024) / kStage > 8 ? 8 : (220 * 1024) / kStage;
+  static constexpr int kSmem = kStages * kStage + 1024 + 512;
+  static constexpr int kNacc = kSfAtoms == 0 ? 2 : 1;
+  static constexpr int kSfaCols = kSfAtoms * 4;
+  static constexpr int kSfbCols = kSfAtoms * 4 * kSfbGroups;
+};
+
+template <int KIND>
+__device__ __forceinline__ void mma_pair_bs(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t sfa, uint32_t sfb, uint32_t accumulate) {
+  if constexpr (KIND == kKindMXF8) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
+        ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate) : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
+        ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate) : "memory");
+  }
+}
+__device__ __forceinline__ void tmem_cp_sf_pair(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
+template <int KIND, bool kSfbFull>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm, 1)
+    gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                     const __grid_constant__ CUtensorMap tmSfa, const __grid_constant__ CUtensorMap tmSfb,
+                     const GemmArgs g) {
+  using PC = PairCfg<KIND, kSfbFull>;
+  constexpr int S = PC::kStages, NACC = PC::kNacc;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = sA + S * PC::kA;
+  uint8_t* sSfa = sB + S * PC::kB;
+  uint8_t* sSfb = sSfa + S * PC::kSfa;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sSfb + S * PC::kSfb);
+  uint64_t* empty = full + S;
+  uint64_t* acc_full = empty + S;
+  uint64_t* acc_empty = acc_full + NACC;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + NACC);
+  uint32_t* peer_base = tmem_slot + 1;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 2);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+  const int total = g.tiles_m * g.tiles_n;  // tiles_m counts 256-row pair tiles
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < NACC; ++a) {
+      mbar_init(&acc_full[a], 1);
+      mbar_init(&acc_empty[a], 2 * kEpiWarps);  // the epilogue warps of both CTAs
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+  }
+  if (warp == 1) tmem_alloc_pair(tmem_slot, 512);
+  tc_fence_before();
+  cluster_sync_all();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  // Both CTAs must see the same TMEM address; otherwise stop cleanly.
+  if (threadIdx.x == 0) st_shared_remote_u32(mapa_shared(smem_u32(peer_base), rank ^ 1u), tmem_base);
+  cluster_sync_all();
+  if (*peer_base != tmem_base) {
+    if (threadIdx.x == 0) atomicCAS(&g_device_error, 0, (int)LPQ_ERR_UNSUPPORTED);
+    *abort_flag = 1;
+  }
+  const bool run = *abort_flag == 0;
+  const uint32_t full_leader = mapa_shared(smem_u32(full), 0);
+  const uint32_t acc_empty_leader = mapa_shared(smem_u32(acc_empty), 0);
+  const uint32_t tmem_sfa = tmem_base + NACC * kPairBN;
+  const uint32_t tmem_sfb = tmem_sfa + PC::kSfaCols;
+
+  if (run && warp == 0) {
+    if (lane == 0) {
+      const int elem_per_kt = KIND == kKindF16 ? kKBytes / 2 : kKBytes;
+      uint32_t s = 0, ph = 0;
+      bool ok = true;
+      for (int t = pair; t < total && ok; t += npairs) {
+        int mt, nt;
+        tile_coords(t, g.tiles_m, g.tiles_n, mt, nt);
+        const int32_t arow = mt * 256 + (int32_t)rank * 128, brow = nt * kPairBN + (int32_t)rank * 128;
+        for (int kt = 0; kt < g.num_k; ++kt) {
+          if (!(ok = mbar_wait_bounded(&empty[s], ph ^ 1u, abort_flag, &g_device_error))) break;
+          if (leader) mbar_arrive_expect_tx(&full[s], 2 * PC::kStage);
+          const uint32_t fb = full_leader + 8 * s;
+          tma_load_2d_pair(sA + s * PC::kA, &tmA, kt * elem_per_kt, arow, fb);
+          tma_load_2d_pair(sB + s * PC::kB, &tmB, kt * elem_per_kt, brow, fb);
+          if constexpr (PC::kSfAtoms > 0) {
+            // scale atoms: rows of a 2D map are 512-byte atoms (128 x u32)
+            const int32_t ga = mt * 2 + (int32_t)rank;
+            tma_load_2d_pair(sSfa + s * PC::kSfa, &tmSfa, 0, (int32_t)(ga * g.sfa_kt + kt * PC::kSfAtoms), fb);
+#pragma unroll
+            for (int i = 0; i < PC::kSfbGroups; ++i) {
+              int64_t gb = kSfbFull ? (int64_t)nt * 2 + i : (int64_t)nt * 2 + rank;
+              if (gb >= g.sfb_groups) gb = g.sfb_groups - 1;
+              tma_load_2d_pair(sSfb + s * PC::kSfb + i * PC::kSfAtoms * 512, &tmSfb, 0,
+                               (int32_t)(gb * g.sfb_kt + kt * PC::kSfAtoms), fb);
+            }
+          }
+          if (++s == (uint32_t)S) { s = 0; ph ^= 1u; }
+        }
+      }
+    }
+  } else if (run && warp == 1) {
+    if (lane == 0 && leader) {
+      const uint32_t kHiSw = (uint32_t)(smem_desc(0, 16, 1024, 2) >> 32);
+      const uint32_t kHiSf = (uint32_t)(smem_desc(0, 0, 128, 0) >> 32);
+      const uint32_t a0 = (uint32_t)smem_desc(smem_u32(sA), 16, 1024, 2);
+      const uint32_t b0 = (uint32_t)smem_desc(smem_u32(sB), 16, 1024, 2);
+      const uint32_t fa0 = smem_u32(sSfa) >> 4, fb0 = smem_u32(sSfb) >> 4;
+      uint32_t s = 0, ph = 0, lt = 0;
+      bool ok = true;
+      for (int t = pair; t < total && ok; t += npairs, ++lt) {
+        const uint32_t a = lt % NACC, aph = (lt / NACC) & 1u;
+        if (!(ok = mbar_wait_bounded(&acc_empty[a], aph ^ 1u, abort_flag, &g_device_error))) break;
+        tc_fence_after();
+        const uint32_t tmem_d = tmem_base + a * kPairBN;
+        for (int kt = 0; kt < g.num_k; ++kt) {
+          if (!(ok = mbar_wait_bounded(&full[s], ph, abort_flag, &g_device_error))) break;
+          tc_fence_after();
+          const uint32_t alo = a0 + s * (PC::kA >> 4), blo = b0 + s * (PC::kB >> 4);
+          const uint32_t falo = fa0 + s * (PC::kSfa >> 4), fblo = fb0 + s * (PC::kSfb >> 4);
+          if constexpr (KIND == kKindMXF8) {
+            tmem_cp_sf_pair(tmem_sfa, ((uint64_t)kHiSf << 32) | falo);
+#pragma unroll
+            for (int i = 0; i < PC::kSfbGroups; ++i)
+              tmem_cp_sf_pair(tmem_sfb + 4 * i, ((uint64_t)kHiSf << 32) | (fblo + i * 32));
+          }
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint64_t ad = ((uint64_t)kHiSw << 32) | (alo + 2 * j);
+            const uint64_t bd = ((uint64_t)kHiSw << 32) | (blo + 2 * j);
+            const uint32_t acc = (kt > 0 || j > 0) ? 1u : 0u;
+            if constexpr (KIND == kKindF16 || KIND == kKindF8F6F4) {
+              mma_pair<KIND>(tmem_d, ad, bd, g.idesc, acc);
+            } else if constexpr (KIND == kKindMXF8) {
+              mma_pair_bs<KIND>(tmem_d, ad, bd, g.idesc | ((uint32_t)j << 4) | ((uint32_t)j << 29), tmem_sfa, tmem_sfb,
+                                acc);
+            } else {
+              tmem_cp_sf_pair(tmem_sfa + 4 * j, ((uint64_t)kHiSf << 32) | (falo + j * 32));
+#pragma unroll
+              for (int i = 0; i < PC::kSfbGroups; ++i)
+                tmem_cp_sf_pair(tmem_sfb + 4 * PC::kSfbGroups * j + 4 * i,
+                                ((uint64_t)kHiSf << 32) | (fblo + (i * 4 + j) * 32));
+              mma_pair_bs<KIND>(tmem_d, ad, bd, g.idesc, tmem_sfa + 4 * j, tmem_sfb + 4 * PC::kSfbGroups * j, acc);
+            }
+          }
+          tc_commit_pair(&empty[s], 0x3);
+          if (++s == (uint32_t)S) { s = 0; ph ^= 1u; }
+        }
+        if (ok) tc_commit_pair(&acc_full[a], 0x3);
+      }
+    }
+  } else if (run && warp >= 2) {
+    constexpr int HALF = kPairBN / 2;
+    const int q = warp & 3;
+    const int half = (warp - 2) >> 2;
+    float alpha = 1.0f;
+    if (g.alpha_a) alpha = *g.alpha_a;
+    if (g.alpha_b) alpha = __fmul_rn(alpha, *g.alpha_b);
+    const bool vec_ok = g.c_fp32 ? (g.N % 4 == 0) : (g.N % 8 == 0);
+    uint32_t lt = 0;
+    for (int t = pair; t < total; t += npairs, ++lt) {
+      int mt, nt;
+      tile_coords(t, g.tiles_m, g.tiles_n, mt, nt);
+      const uint32_t a = lt % NACC, aph = (lt / NACC) & 1u;
+      if (!mbar_wait_bounded(&acc_full[a], aph, abort_flag, &g_device_error)) break;
+      __syncwarp();
+      tc_fence_after();
+      const int64_t row = (int64_t)mt * 256 + rank * 128 + q * 32 + lane;
+      const int64_t c0 = (int64_t)nt * kPairBN + half * HALF;
+      const int64_t ncols = g.N - c0;
+      const uint32_t tbase = tmem_base + a * kPairBN + half * HALF + ((uint32_t)(q * 32) << 16);
+      if (!g.c_fp32) {
+        uint32_t pk[HALF / 2];
+#pragma unroll
+        for (int cc = 0; cc < HALF / 32; ++cc) {
+          uint32_t v[32];
+          tmem_ld32(tbase + (uint32_t)(cc * 32), v);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            __nv_bfloat162 h = __floats2bfloat162_rn(__fmul_rn(__uint_as_float(v[2 * i]), alpha),
+                                                     __fmul_rn(__uint_as_float(v[2 * i + 1]), alpha));
+            pk[cc * 16 + i] = *reinterpret_cast<uint32_t*>(&h);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if (leader) mbar_arrive(&acc_empty[a]); else mbar_arrive_remote(acc_empty_leader + 8 * a);
+        }
+        if (row < g.M && ncols > 0) {
+          __nv_bfloat16* out = static_cast<__nv_bfloat16*>(g.c) + row * g.N + c0;
+          if (vec_ok && ncols >= HALF) {
+#pragma unroll
+            for (int i = 0; i < HALF / 8; ++i)
+              reinterpret_cast<uint4*>(out)[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+          } else {
+#pragma unroll
+            for (int i = 0; i < HALF / 2; ++i) {
+              if (2 * i < ncols) out[2 * i] = __ushort_as_bfloat16((unsigned short)(pk[i] & 0xFFFFu));
+              if (2 * i + 1 < ncols) out[2 * i + 1] = __ushort_as_bfloat16((unsigned short)(pk[i] >> 16));
+            }
+          }
+        }
+        continue;
+      }
+#pragma unroll 1
+      for (int cc = 0; cc < HALF / 32; ++cc) {
+        uint32_t v[32];
+        tmem_ld32(tbase + (uint32_t)(cc * 32), v);
+        if (cc == HALF / 32 - 1) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) {
+            if (leader) mbar_arrive(&acc_empty[a]); else mbar_arrive_remote(acc_empty_leader + 8 * a);
+          }
+        }
+        const int64_t col0 = c0 + cc * 32;
+        if (row >= g.M || col0 >= g.N) continue;
+        float* out = static_cast<float*>(g.c) + row * g.N + col0;
+        if (vec_ok && col0 + 32 <= g.N) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            reinterpret_cast<float4*>(out)[i] = make_float4(
+                __fmul_rn(__uint_as_float(v[4 * i]), alpha), __fmul_rn(__uint_as_float(v[4 * i + 1]), alpha),
+                __fmul_rn(__uint_as_float(v[4 * i + 2]), alpha), __fmul_rn(__uint_as_float(v[4 * i + 3]), alpha));
+        } else {
+          for (int i = 0; i < 32 && col0 + i < g.N; ++i) out[i] = __fmul_rn(__uint_as_float(v[i]), alpha);
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  cluster_sync_all();  // no CTA leaves while its peer may still signal its barriers
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, 512);
+  }
+}
+
+// 2D map over a scale array in the tensor-core layout: rows are 512-byte
+// atoms (128 x u32), a box is `atoms` consecutive atoms.
+lpq_status make_sf_map(CUtensorMap* map, const void* base, int64_t total_atoms, uint32_t atoms) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return set_error(LPQ_ERR_CUDA, "cuTensorMapEncodeTiled unavailable from the driver");
+  cuuint64_t dims[2] = {128, (cuuint64_t)(total_atoms > 0 ? total_atoms : 1)};
+  cuuint64_t strides[1] = {512};
+  cuuint32_t box[2] = {128, atoms};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return set_error(LPQ_ERR_CUDA, "cuTensorMapEncodeTiled (scales) failed (%d)", (int)r);
+  return LPQ_OK;
+}
+
+template <int KIND, bool kSfbFull>
+lpq_status run_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tsa, const CUtensorMap& tsb,
+                    GemmArgs g, cudaStream_t s) {
+  using PC = PairCfg<KIND, kSfbFull>;
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_pair_kernel<KIND, kSfbFull>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         PC::kSmem);
+    if (e != cudaSuccess) return cuda_check(e, "cudaFuncSetAttribute(pair gemm)");
+    attr = true;
+  }
+  if (g_sms == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&g_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (g_sms <= 0) g_sms = 148;
+  }
+  const int64_t tm = (g.M + 255) / 256, tn = (g.N + kPairBN - 1) / kPairBN;
+  g.tiles_m = (int)tm;
+  g.tiles_n = (int)tn;
+  const int pairs = (int)std::min<int64_t>(tm * tn, g_sms / 2);
+  gemm_pair_kernel<KIND, kSfbFull><<<2 * pairs, kThreadsGemm, PC::kSmem, s>>>(ta, tb, tsa, tsb, g);
+  return cuda_check(cudaGetLastError(), "pair gemm launch");
+}
+
+// Kernel path per GEMM: the CTA-pair kernel (256 x 256 tiles) for bf16, FP8
+// and MXFP8, the single-CTA kernel for NVFP4 (its scale-factor copies leave
+// nothing to gain from pairs).  LPQ_GEMM_PAIR=0 forces single CTAs, =1 pairs
+// for every kind; read on every call so both paths can be exercised.
+bool use_pair(int kind) {
+  const char* e = getenv("LPQ_GEMM_PAIR");
+  if (e && e[0] == '0') return false;
+  if (e && e[0] == '1') return true;
+  return kind != kKindNVF4;
+}
 // Sub-channel FP8 GEMM ("Faster training throughput in FP8 with NVIDIA NeMo",
 // sub-channel scaling: 1x128 activation and 128x128 weight blocks with FP32
 // factors).  Every 128-deep K slice is one pipeline stage: the MMA warp
@@ -642,6 +969,12 @@ lpq_status launch_gemm(const lpq_qview* a, const lpq_qview* b, void* c, int32_t 
     if ((st = make_map(&ta, a->codes, true, k, m, k * 2, 64, kBM)) != LPQ_OK) return st;
     if ((st = make_map(&tb, b->codes, true, k, n, k * 2, 64, BN)) != LPQ_OK) return st;
     g.idesc = idesc_dense(1, 1, BN);  // BF16 x BF16 -> F32
+    if (use_pair(kKindF16) && m >= 256) {
+      if ((st = make_map(&ta, a->codes, true, k, m, k * 2, 64, kBM)) != LPQ_OK) return st;
+      if ((st = make_map(&tb, b->codes, true, k, n, k * 2, 64, kPairBN / 2)) != LPQ_OK) return st;
+      g.idesc = idesc_dense(1, 1, kPairBN) & ~(31u << 24) | (16u << 24);  // M = 256
+      return run_pair<kKindF16, true>(ta, tb, ta, tb, g, s);
+    }
     return run<kKindF16, BN, 2>(ta, tb, g, s);
   }
   if (fa == LPQ_FP8_E4M3 || fa == LPQ_FP8_E5M2) {
@@ -651,6 +984,11 @@ lpq_status launch_gemm(const lpq_qview* a, const lpq_qview* b, void* c, int32_t 
     g.idesc = idesc_dense(fa == LPQ_FP8_E5M2 ? 1 : 0, fb == LPQ_FP8_E5M2 ? 1 : 0, BN);
     g.alpha_a = a->tensor_scale;
     g.alpha_b = b->tensor_scale;
+    if (use_pair(kKindF8F6F4) && m >= 256) {
+      if ((st = make_map(&tb, b->codes, false, k, n, k, 128, kPairBN / 2)) != LPQ_OK) return st;
+      g.idesc = (g.idesc & ~(31u << 24)) | (16u << 24);  // M = 256
+      return run_pair<kKindF8F6F4, true>(ta, tb, ta, tb, g, s);
+    }
     return run<kKindF8F6F4, BN, 2>(ta, tb, g, s);
   }
   if (fa == LPQ_MXFP8) {
@@ -663,6 +1001,14 @@ lpq_status launch_gemm(const lpq_qview* a, const lpq_qview* b, void* c, int32_t 
     g.sfa_kt = sf_kt_atoms(LPQ_MXFP8, k);
     g.sfb_kt = g.sfa_kt;
     g.sfb_groups = sf_row_groups(n);
+    if (use_pair(kKindMXF8) && m >= 256) {
+      CUtensorMap tsa, tsb;
+      if ((st = make_map(&tb, b->codes, false, k, n, k, 128, kPairBN / 2)) != LPQ_OK) return st;
+      if ((st = make_sf_map(&tsa, g.sfa, sf_row_groups(m) * g.sfa_kt, 1)) != LPQ_OK) return st;
+      if ((st = make_sf_map(&tsb, g.sfb, g.sfb_groups * g.sfb_kt, 1)) != LPQ_OK) return st;
+      g.idesc = (g.idesc & ~(31u << 24)) | (16u << 24);
+      return run_pair<kKindMXF8, true>(ta, tb, tsa, tsb, g, s);
+    }
     if (nv_bn == 128) {
       if ((st = make_map(&tb, b->codes, false, k, n, k, 128, 128)) != LPQ_OK) return st;
       g.idesc = idesc_block_scaled(0, 0, 1, 128);
@@ -682,6 +1028,14 @@ lpq_status launch_gemm(const lpq_qview* a, const lpq_qview* b, void* c, int32_t 
     g.sfb_groups = sf_row_groups(n);
     g.alpha_a = a->tensor_scale;
     g.alpha_b = b->tensor_scale;
+    if (use_pair(kKindNVF4) && m >= 256) {
+      CUtensorMap tsa, tsb;
+      if ((st = make_map(&tb, b->codes, false, k / 2, n, k / 2, 128, kPairBN / 2)) != LPQ_OK) return st;
+      if ((st = make_sf_map(&tsa, g.sfa, sf_row_groups(m) * g.sfa_kt, 4)) != LPQ_OK) return st;
+      if ((st = make_sf_map(&tsb, g.sfb, g.sfb_groups * g.sfb_kt, 4)) != LPQ_OK) return st;
+      g.idesc = (g.idesc & ~(31u << 24)) | (16u << 24);
+      return run_pair<kKindNVF4, true>(ta, tb, tsa, tsb, g, s);
+    }
     if (nv_bn == 128) {
       if ((st = make_map(&tb, b->codes, false, k / 2, n, k / 2, 128, 128)) != LPQ_OK) return st;
       g.idesc = idesc_block_scaled(1, 1, 0, 128);

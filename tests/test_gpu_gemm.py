@@ -34,11 +34,15 @@ def check(a, b, M, N, K, out_fp32, layout=lpq.FPROP):
     assert nbad == 0, f"{nbad} elements outside the gate (worst {worst:.3g}x)"
 
 
+@pytest.mark.parametrize("path", ["single", "pair"])
 @pytest.mark.parametrize("out_fp32", [True, False])
 @pytest.mark.parametrize("shape", SHAPES)
 @pytest.mark.parametrize("fmts", [(lpq.BF16, lpq.BF16), (lpq.FP8_E4M3, lpq.FP8_E4M3), (lpq.FP8_E5M2, lpq.FP8_E4M3),
                                   (lpq.MXFP8, lpq.MXFP8), (lpq.NVFP4, lpq.NVFP4), (lpq.NVFP4, lpq.NVFP4_2D)])
-def test_gemm_parity(fmts, shape, out_fp32):
+def test_gemm_parity(fmts, shape, out_fp32, path, monkeypatch):
+    """Both kernel paths: one CTA per 128 x 256 tile, and CTA pairs
+    (cta_group::2) per 256 x 256 tile."""
+    monkeypatch.setenv("LPQ_GEMM_PAIR", "1" if path == "pair" else "0")
     M, K, N = shape
     if fmts[1] == lpq.NVFP4_2D and N % 16:
         pytest.skip("2D weight tiles need N % 16 == 0")
@@ -128,15 +132,18 @@ def test_fprop_dgrad_wgrad_layouts(fmt):
     check(qd.col, qx.col, N, K, M, True, lpq.WGRAD)      # dW [N, K]
 
 
-@pytest.mark.parametrize("fmt", [lpq.NVFP4, lpq.MXFP8])
+@pytest.mark.parametrize("fmt", [lpq.NVFP4, lpq.MXFP8, lpq.FP8_E4M3, lpq.BF16])
 def test_full_size_sampled(fmt):
     """QKV Fprop at the layer's size (15872 x 4096 x 12288): the first and last
     128 x 128 output tiles and 4096 uniformly sampled elements."""
     M, K, N = 15872, 4096, 12288
     X, _ = bf16_input((M, K), std=1.0, seed=30)
     W, _ = bf16_input((N, K), std=0.02, seed=31)
-    qx = lpq.quantize(X, fmt, lpq.ROWWISE)
-    qw = lpq.quantize(W, lpq.NVFP4_2D if fmt == lpq.NVFP4 else fmt, lpq.ROWWISE)
+    if fmt == lpq.BF16:
+        qx, qw = lpq.QTensor(lpq.Copy.of_bf16(X)), lpq.QTensor(lpq.Copy.of_bf16(W))
+    else:
+        qx = lpq.quantize(X, fmt, lpq.ROWWISE)
+        qw = lpq.quantize(W, lpq.NVFP4_2D if fmt == lpq.NVFP4 else fmt, lpq.ROWWISE)
     c = lpq.gemm(lpq.FPROP, qx.row, qw.row)
     torch.cuda.synchronize()
     rng = np.random.default_rng(0)
