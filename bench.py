@@ -420,7 +420,7 @@ def run_reference(args, rank, world):
     proj = []
     t0 = time.perf_counter()
     for s in range(args.steps):
-        sec, _ = oracle_sample(shapes, M, lins, rows=1, cols=64, slab=16, seed=args.warmup + s)
+        sec, _ = oracle_sample(shapes, M, lins, rows=2, cols=128, slab=16, seed=args.warmup + s)
         proj.append(sec)
     wall = time.perf_counter() - t0
     sec = statistics.mean(proj)
@@ -433,7 +433,7 @@ def run_reference(args, rank, world):
                                    "intermediate 16384)", "global_batch": args.micro_batch_size,
                        "seq_len": args.sequence_length, "parallelism": "replicas"},
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": o.num_threads(), "kind": "oracle",
-                             "sample": "per step: per GEMM 1x64 outputs of the FP64 oracle GEMM on NVFP4 operands "
+                             "sample": "per step: per GEMM 2x128 outputs of the FP64 oracle GEMM on NVFP4 operands "
                                        "and their NVFP4 quantization, projected to the full layer",
                              "wall_s": wall},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -561,11 +561,11 @@ def run_lpq(args, rank, world, local):
         lins = [(n, K, N) for n, (K, N) in layer.linears.items()]
         shapes = [(n, lay, m, k, nn) for n, lay, m, k, nn in layer.shapes]
         t0 = time.perf_counter()
-        sec, info = oracle_sample(shapes, layer.M, lins, rows=2, cols=128, slab=16)
+        sec, info = oracle_sample(shapes, layer.M, lins, rows=32, cols=256, slab=16)
         wall = time.perf_counter() - t0
         cpu = {"value": layer.flops / sec / 1e12, "unit": "TFLOP/s", "cores": o.num_threads(), "kind": "oracle",
-               "sample": "per GEMM 2x128 outputs of the FP64 oracle GEMM on NVFP4 operands plus their NVFP4 "
-                         "quantization, projected to the full layer (quantize share %.0f%%)"
+               "sample": "per GEMM 32x256 outputs of the FP64 oracle GEMM on NVFP4 operands plus the NVFP4 "
+                         "quantization of those operand rows, projected to the full layer (quantize share %.0f%%)"
                          % (100 * info["quant_s"] / sec),
                "wall_s": wall}
 
