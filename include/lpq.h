@@ -232,7 +232,8 @@ lpq_status lpq_selftest_wait(uint64_t limit_ns, lpq_stream_t stream);
  * block-scaled (K 64).  with_scale_copies adds the per-step tcgen05.cp of the
  * scale factors (kinds 2, 3): 1 = all of a step's copies before its MMAs,
  * 2 = the same into two alternating TMEM regions, 3 = each MMA's copies
- * right before it (NVFP4).  FLOPs = SMs * iters * 4 * 2 * 128 * 256 * K;
+ * right before it, 4 = the scale columns rewritten by four other warps with
+ * tcgen05.st while the MMAs run (NVFP4; throughput only).  FLOPs = SMs * iters * 4 * 2 * 128 * 256 * K;
  * the caller times the launch with events on `stream`. */
 lpq_status lpq_mma_peak(int32_t kind, int32_t iters, int32_t with_scale_copies, lpq_stream_t stream);
 

@@ -39,7 +39,7 @@ namespace {
 constexpr int kBM = 128;
 constexpr int kKBytes = 128;  // bytes of K per pipeline stage (one 128-byte swizzle row)
 
-template <int KIND, int BN, int NACC>
+template <int KIND, int BN, int NACC, bool SFST = false>
 struct Cfg {
   static constexpr int kSfAtoms = KIND == kKindNVF4 ? 4 : (KIND == kKindMXF8 ? 1 : 0);  // per 128 rows
   static constexpr int kA = kBM * kKBytes;
@@ -51,7 +51,8 @@ struct Cfg {
   static constexpr int kSmem = kStages * kStage + 1024 /*align slack*/ + 512 /*barriers*/;
   static constexpr int kSfaCols = kSfAtoms * 4;
   static constexpr int kSfbCols = kSfAtoms * 4 * (BN / 128);
-  static constexpr int kCols = NACC * BN + kSfaCols + kSfbCols;
+  static constexpr int kSlots = SFST ? 4 : 1;  // TMEM scale slots (SFST: written by the scale warps)
+  static constexpr int kCols = NACC * BN + kSlots * (kSfaCols + kSfbCols);
   static constexpr int kTmemCols = kCols <= 32 ? 32 : kCols <= 64 ? 64 : kCols <= 128 ? 128 : kCols <= 256 ? 256 : 512;
   static_assert(kCols <= 512, "TMEM holds 512 columns");
   static_assert(BN % 128 == 0 || kSfAtoms == 0, "scale atoms cover 128 rows");
@@ -60,6 +61,7 @@ struct Cfg {
 constexpr int kGroupM = 16;  // tiles along M that share a band of B tiles (L2 reuse)
 constexpr int kEpiWarps = 8;  // two per TMEM lane quarter, each owning half of the tile's columns
 constexpr int kThreadsGemm = 64 + 32 * kEpiWarps;
+constexpr int kSfWarps = 4;  // scale-store warps of the NVFP4 kernel, one per TMEM lane quarter
 
 struct GemmArgs {
   const uint8_t* sfa;  // tensor-core scale layout of A (block-scaled kinds)
@@ -93,10 +95,10 @@ __device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int
 // 32 * (w % 4) ..).  The shared-memory ring runs continuously across the
 // CTA's tiles; NACC accumulators in TMEM let the epilogue of one tile overlap
 // the main loop of the next.
-template <int KIND, int BN, int NACC>
-__global__ void __launch_bounds__(kThreadsGemm, 1)
+template <int KIND, int BN, int NACC, bool SFST>
+__global__ void __launch_bounds__(kThreadsGemm + (SFST ? 32 * kSfWarps : 0))
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const GemmArgs g) {
-  using CF = Cfg<KIND, BN, NACC>;
+  using CF = Cfg<KIND, BN, NACC, SFST>;
   constexpr int S = CF::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -108,7 +110,9 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
   uint64_t* empty = full + S;
   uint64_t* acc_full = empty + S;
   uint64_t* acc_empty = acc_full + NACC;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + NACC);
+  uint64_t* sf_full = acc_empty + NACC;     // [kSlots] (SFST)
+  uint64_t* sf_empty = sf_full + CF::kSlots;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sf_empty + CF::kSlots);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -117,11 +121,15 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+      mbar_init(&empty[s], SFST ? 1 + kSfWarps : 1);  // MMA commit (+ the scale warps' reads)
     }
     for (int a = 0; a < NACC; ++a) {
       mbar_init(&acc_full[a], 1);
       mbar_init(&acc_empty[a], kEpiWarps);  // one arrive per epilogue warp
+    }
+    for (int i = 0; i < CF::kSlots; ++i) {
+      mbar_init(&sf_full[i], kSfWarps);
+      mbar_init(&sf_empty[i], 1);
     }
     *abort_flag = 0;
     fence_barrier_init();
@@ -178,7 +186,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
       const uint32_t kHiSf = (uint32_t)(smem_desc(0, 0, 128, 0) >> 32);
       const uint32_t a0 = kLoSw | (smem_u32(sA) >> 4), b0 = kLoSw | (smem_u32(sB) >> 4);
       const uint32_t fa0 = smem_u32(sSfa) >> 4, fb0 = smem_u32(sSfb) >> 4;
-      uint32_t s = 0, ph = 0, lt = 0;
+      uint32_t s = 0, ph = 0, lt = 0, slot = 0, sph = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++lt) {
         const uint32_t a = lt % NACC, aph = (lt / NACC) & 1u;
@@ -187,6 +195,9 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
         const uint32_t tmem_d = tmem_base + a * BN;
         for (int kt = 0; kt < g.num_k; ++kt) {
           if (!(ok = mbar_wait_bounded(&full[s], ph, abort_flag, &g_device_error))) break;
+          if constexpr (SFST) {
+            if (!(ok = mbar_wait_bounded(&sf_full[slot], sph, abort_flag, &g_device_error))) break;
+          }
           tc_fence_after();
           const uint32_t alo = a0 + s * (CF::kA >> 4), blo = b0 + s * (CF::kB >> 4);
           const uint32_t falo = fa0 + s * (CF::kSfa >> 4), fblo = fb0 + s * (CF::kSfb >> 4);
@@ -204,6 +215,9 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
               mma_ss<KIND>(tmem_d, ad, bd, g.idesc, acc);
             } else if constexpr (KIND == kKindMXF8) {
               mma_bs<KIND>(tmem_d, ad, bd, g.idesc | ((uint32_t)j << 4) | ((uint32_t)j << 29), tmem_sfa, tmem_sfb, acc);
+            } else if constexpr (SFST) {
+              const uint32_t base = tmem_sfa + slot * (CF::kSfaCols + CF::kSfbCols);
+              mma_bs<KIND>(tmem_d, ad, bd, g.idesc, base + 4 * j, base + CF::kSfaCols + 4 * (BN / 128) * j, acc);
             } else {
               tmem_cp_sf(tmem_sfa + 4 * j, ((uint64_t)kHiSf << 32) | (falo + j * 32));
 #pragma unroll
@@ -213,12 +227,59 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
             }
           }
           tc_commit(&empty[s]);
+          if constexpr (SFST) {
+            tc_commit(&sf_empty[slot]);
+            if (++slot == (uint32_t)CF::kSlots) { slot = 0; sph ^= 1u; }
+          }
           if (++s == (uint32_t)S) { s = 0; ph ^= 1u; }
         }
         if (ok) tc_commit(&acc_full[a]);
       }
     }
-  } else {
+  } else if (SFST && warp >= 2 + kEpiWarps) {
+    // ------------------------------------------------------------ scale warps (NVFP4)
+    // Per k-step: this warp's lane quarter of the step's 12 scale atoms goes from
+    // shared memory into a TMEM slot with tcgen05.st (replicated in every
+    // quarter); the slot is handed to the MMA warp and the stage released.
+    const int q = warp & 3;
+    const uint32_t lanes = (uint32_t)(q * 32) << 16;
+    uint32_t s = 0, ph = 0, slot = 0, sph = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+      for (int kt = 0; kt < g.num_k; ++kt) {
+        if (!(ok = mbar_wait_bounded(&full[s], ph, abort_flag, &g_device_error))) break;
+        if (!(ok = mbar_wait_bounded(&sf_empty[slot], sph ^ 1u, abort_flag, &g_device_error))) break;
+        __syncwarp();
+        tc_fence_after();
+        const uint4* fa = reinterpret_cast<const uint4*>(sSfa + s * CF::kSfa) + lane;  // atom j line `lane`
+        const uint4* fb = reinterpret_cast<const uint4*>(sSfb + s * CF::kSfb) + lane;
+        uint32_t va[16], vb[32];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint4 x = fa[j * 32];
+          va[4 * j] = x.x; va[4 * j + 1] = x.y; va[4 * j + 2] = x.z; va[4 * j + 3] = x.w;
+#pragma unroll
+          for (int i = 0; i < BN / 128; ++i) {
+            const uint4 y = fb[(i * 4 + j) * 32];
+            const int c = 4 * (BN / 128) * j + 4 * i;
+            vb[c] = y.x; vb[c + 1] = y.y; vb[c + 2] = y.z; vb[c + 3] = y.w;
+          }
+        }
+        const uint32_t base = tmem_base + NACC * BN + slot * (CF::kSfaCols + CF::kSfbCols) + lanes;
+        tmem_st16(base, va);
+        tmem_st32(base + CF::kSfaCols, vb);
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&sf_full[slot]);
+          mbar_arrive(&empty[s]);
+        }
+        if (++slot == (uint32_t)CF::kSlots) { slot = 0; sph ^= 1u; }
+        if (++s == (uint32_t)S) { s = 0; ph ^= 1u; }
+      }
+    }
+  } else if (warp >= 2) {
     // ------------------------------------------------------------ epilogue
     // Warp w reads TMEM lanes 32 * (w % 4) .. of columns [half * BN/2, +BN/2).
     constexpr int HALF = BN / 2;
@@ -354,12 +415,12 @@ uint32_t idesc_block_scaled(uint32_t afmt, uint32_t bfmt, uint32_t e8m0, int n) 
 
 int g_sms = 0;
 
-template <int KIND, int BN, int NACC>
+template <int KIND, int BN, int NACC, bool SFST = false>
 lpq_status run(const CUtensorMap& ta, const CUtensorMap& tb, GemmArgs g, cudaStream_t s) {
-  using CF = Cfg<KIND, BN, NACC>;
+  using CF = Cfg<KIND, BN, NACC, SFST>;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<KIND, BN, NACC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<KIND, BN, NACC, SFST>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          CF::kSmem);
     if (e != cudaSuccess) return cuda_check(e, "cudaFuncSetAttribute(gemm smem)");
     attr_set = true;
@@ -375,9 +436,10 @@ lpq_status run(const CUtensorMap& ta, const CUtensorMap& tb, GemmArgs g, cudaStr
   g.tiles_m = (int)tm;
   g.tiles_n = (int)tn;
   const int grid = (int)std::min<int64_t>(tm * tn, g_sms);
-  gemm_kernel<KIND, BN, NACC><<<grid, kThreadsGemm, CF::kSmem, s>>>(ta, tb, g);
+  gemm_kernel<KIND, BN, NACC, SFST><<<grid, kThreadsGemm + (SFST ? 32 * kSfWarps : 0), CF::kSmem, s>>>(ta, tb, g);
   return cuda_check(cudaGetLastError(), "gemm kernel launch");
 }
+
 
 // CTA-pair GEMM (cta_group::2).  A cluster of two CTAs on two SMs computes a
 // 256 x 256 output tile: each CTA loads its own 128 rows of A and its own 128
@@ -1041,7 +1103,9 @@ lpq_status launch_gemm(const lpq_qview* a, const lpq_qview* b, void* c, int32_t 
       g.idesc = idesc_block_scaled(1, 1, 0, 128);
       return run<kKindNVF4, 128, 2>(ta, tb, g, s);
     }
-    return run<kKindNVF4, BN, 1>(ta, tb, g, s);
+    const char* e = getenv("LPQ_GEMM_SFCP");  // =1: scale copies by the MMA thread (tcgen05.cp)
+    if (e && e[0] == '1') return run<kKindNVF4, BN, 1>(ta, tb, g, s);
+    return run<kKindNVF4, BN, 1, true>(ta, tb, g, s);
   }
   if (fa == LPQ_FP8_BLOCK_1x128 || fa == LPQ_FP8_BLOCK_128x128) {
     BlockArgs bg{};
