@@ -454,7 +454,7 @@ lpq_status run(const CUtensorMap& ta, const CUtensorMap& tb, GemmArgs g, cudaStr
 // copies (tcgen05.cp.cta_group::2) move into each CTA's TMEM.
 constexpr int kPairBN = 256;
 
-template <int KIND, bool kSfbFull>
+template <int KIND, bool kSfbFull, bool SFST = false>
 struct PairCfg {
   static constexpr int kSfAtoms = KIND == kKindNVF4 ? 4 : (KIND == kKindMXF8 ? 1 : 0);
   static constexpr int kA = kBM * kKBytes;
@@ -468,6 +468,8 @@ struct PairCfg {
   static constexpr int kNacc = kSfAtoms == 0 ? 2 : 1;
   static constexpr int kSfaCols = kSfAtoms * 4;
   static constexpr int kSfbCols = kSfAtoms * 4 * kSfbGroups;
+  static constexpr int kSlots = SFST ? 4 : 1;
+  static_assert(kNacc * kPairBN + kSlots * (kSfaCols + kSfbCols) <= 512, "TMEM holds 512 columns");
 };
 
 template <int KIND>
@@ -489,12 +491,12 @@ __device__ __forceinline__ void tmem_cp_sf_pair(uint32_t taddr, uint64_t sdesc) 
   asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
 }
 
-template <int KIND, bool kSfbFull>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm, 1)
+template <int KIND, bool kSfbFull, bool SFST>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm + (SFST ? 32 * kSfWarps : 0))
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmSfa, const __grid_constant__ CUtensorMap tmSfb,
                      const GemmArgs g) {
-  using PC = PairCfg<KIND, kSfbFull>;
+  using PC = PairCfg<KIND, kSfbFull, SFST>;
   constexpr int S = PC::kStages, NACC = PC::kNacc;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -506,7 +508,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm, 1)
   uint64_t* empty = full + S;
   uint64_t* acc_full = empty + S;
   uint64_t* acc_empty = acc_full + NACC;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + NACC);
+  uint64_t* sf_full = acc_empty + NACC;  // [kSlots] (SFST): scale warps of both CTAs
+  uint64_t* sf_empty = sf_full + PC::kSlots;
+  uint64_t* sfd = sf_empty + PC::kSlots;  // [S] (SFST): this CTA's scale atoms landed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sfd + S);
   uint32_t* peer_base = tmem_slot + 1;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 2);
 
@@ -519,12 +524,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+      mbar_init(&empty[s], SFST ? 1 + kSfWarps : 1);  // MMA commit (+ this CTA's scale warps)
     }
     for (int a = 0; a < NACC; ++a) {
       mbar_init(&acc_full[a], 1);
       mbar_init(&acc_empty[a], 2 * kEpiWarps);  // the epilogue warps of both CTAs
     }
+    for (int i = 0; i < PC::kSlots; ++i) {
+      mbar_init(&sf_full[i], 2 * kSfWarps);  // the scale warps of both CTAs
+      mbar_init(&sf_empty[i], 1);
+    }
+    for (int s = 0; s < S; ++s) mbar_init(&sfd[s], 1);
     *abort_flag = 0;
     fence_barrier_init();
     prefetch_tmap(&tmA);
@@ -545,6 +555,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm, 1)
   const bool run = *abort_flag == 0;
   const uint32_t full_leader = mapa_shared(smem_u32(full), 0);
   const uint32_t acc_empty_leader = mapa_shared(smem_u32(acc_empty), 0);
+  const uint32_t sf_full_leader = mapa_shared(smem_u32(sf_full), 0);
   const uint32_t tmem_sfa = tmem_base + NACC * kPairBN;
   const uint32_t tmem_sfb = tmem_sfa + PC::kSfaCols;
 
@@ -559,20 +570,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm, 1)
         const int32_t arow = mt * 256 + (int32_t)rank * 128, brow = nt * kPairBN + (int32_t)rank * 128;
         for (int kt = 0; kt < g.num_k; ++kt) {
           if (!(ok = mbar_wait_bounded(&empty[s], ph ^ 1u, abort_flag, &g_device_error))) break;
-          if (leader) mbar_arrive_expect_tx(&full[s], 2 * PC::kStage);
+          if (leader) mbar_arrive_expect_tx(&full[s], SFST ? 2 * (PC::kA + PC::kB) : 2 * PC::kStage);
           const uint32_t fb = full_leader + 8 * s;
           tma_load_2d_pair(sA + s * PC::kA, &tmA, kt * elem_per_kt, arow, fb);
           tma_load_2d_pair(sB + s * PC::kB, &tmB, kt * elem_per_kt, brow, fb);
           if constexpr (PC::kSfAtoms > 0) {
-            // scale atoms: rows of a 2D map are 512-byte atoms (128 x u32)
+            // scale atoms: rows of a 2D map are 512-byte atoms (128 x u32).  With
+            // scale warps they land on this CTA's own barrier (its scale warps
+            // read them); otherwise on the even CTA's full barrier (pair copies).
             const int32_t ga = mt * 2 + (int32_t)rank;
-            tma_load_2d_pair(sSfa + s * PC::kSfa, &tmSfa, 0, (int32_t)(ga * g.sfa_kt + kt * PC::kSfAtoms), fb);
+            if constexpr (SFST) mbar_arrive_expect_tx(&sfd[s], PC::kSfa + PC::kSfb);
+            const int32_t ya = (int32_t)(ga * g.sfa_kt + kt * PC::kSfAtoms);
+            if constexpr (SFST) tma_load_2d(sSfa + s * PC::kSfa, &tmSfa, 0, ya, &sfd[s]);
+            else tma_load_2d_pair(sSfa + s * PC::kSfa, &tmSfa, 0, ya, fb);
 #pragma unroll
             for (int i = 0; i < PC::kSfbGroups; ++i) {
               int64_t gb = kSfbFull ? (int64_t)nt * 2 + i : (int64_t)nt * 2 + rank;
               if (gb >= g.sfb_groups) gb = g.sfb_groups - 1;
-              tma_load_2d_pair(sSfb + s * PC::kSfb + i * PC::kSfAtoms * 512, &tmSfb, 0,
-                               (int32_t)(gb * g.sfb_kt + kt * PC::kSfAtoms), fb);
+              const int32_t yb = (int32_t)(gb * g.sfb_kt + kt * PC::kSfAtoms);
+              if constexpr (SFST) tma_load_2d(sSfb + s * PC::kSfb + i * PC::kSfAtoms * 512, &tmSfb, 0, yb, &sfd[s]);
+              else tma_load_2d_pair(sSfb + s * PC::kSfb + i * PC::kSfAtoms * 512, &tmSfb, 0, yb, fb);
             }
           }
           if (++s == (uint32_t)S) { s = 0; ph ^= 1u; }
@@ -586,7 +603,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm, 1)
       const uint32_t a0 = (uint32_t)smem_desc(smem_u32(sA), 16, 1024, 2);
       const uint32_t b0 = (uint32_t)smem_desc(smem_u32(sB), 16, 1024, 2);
       const uint32_t fa0 = smem_u32(sSfa) >> 4, fb0 = smem_u32(sSfb) >> 4;
-      uint32_t s = 0, ph = 0, lt = 0;
+      uint32_t s = 0, ph = 0, lt = 0, slot = 0, sph = 0;
       bool ok = true;
       for (int t = pair; t < total && ok; t += npairs, ++lt) {
         const uint32_t a = lt % NACC, aph = (lt / NACC) & 1u;
@@ -595,6 +612,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm, 1)
         const uint32_t tmem_d = tmem_base + a * kPairBN;
         for (int kt = 0; kt < g.num_k; ++kt) {
           if (!(ok = mbar_wait_bounded(&full[s], ph, abort_flag, &g_device_error))) break;
+          if constexpr (SFST) {
+            if (!(ok = mbar_wait_bounded(&sf_full[slot], sph, abort_flag, &g_device_error))) break;
+          }
           tc_fence_after();
           const uint32_t alo = a0 + s * (PC::kA >> 4), blo = b0 + s * (PC::kB >> 4);
           const uint32_t falo = fa0 + s * (PC::kSfa >> 4), fblo = fb0 + s * (PC::kSfb >> 4);
@@ -614,6 +634,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm, 1)
             } else if constexpr (KIND == kKindMXF8) {
               mma_pair_bs<KIND>(tmem_d, ad, bd, g.idesc | ((uint32_t)j << 4) | ((uint32_t)j << 29), tmem_sfa, tmem_sfb,
                                 acc);
+            } else if constexpr (SFST) {
+              const uint32_t base = tmem_sfa + slot * (PC::kSfaCols + PC::kSfbCols);
+              mma_pair_bs<KIND>(tmem_d, ad, bd, g.idesc, base + 4 * j, base + PC::kSfaCols + 4 * PC::kSfbGroups * j, acc);
             } else {
               tmem_cp_sf_pair(tmem_sfa + 4 * j, ((uint64_t)kHiSf << 32) | (falo + j * 32));
 #pragma unroll
@@ -624,9 +647,55 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm, 1)
             }
           }
           tc_commit_pair(&empty[s], 0x3);
+          if constexpr (SFST) {
+            tc_commit_pair(&sf_empty[slot], 0x3);
+            if (++slot == (uint32_t)PC::kSlots) { slot = 0; sph ^= 1u; }
+          }
           if (++s == (uint32_t)S) { s = 0; ph ^= 1u; }
         }
         if (ok) tc_commit_pair(&acc_full[a], 0x3);
+      }
+    }
+  } else if (run && SFST && warp >= 2 + kEpiWarps) {
+    // scale warps: this CTA's lane quarter of the step's scale atoms (its own A
+    // rows, all 256 B rows) from shared memory into the TMEM slot; both CTAs'
+    // scale warps report to the even CTA's slot barrier
+    const int q = warp & 3;
+    const uint32_t lanes = (uint32_t)(q * 32) << 16;
+    uint32_t s = 0, ph = 0, slot = 0, sph = 0;
+    bool ok = true;
+    for (int t = pair; t < total && ok; t += npairs) {
+      for (int kt = 0; kt < g.num_k; ++kt) {
+        if (!(ok = mbar_wait_bounded(&sfd[s], ph, abort_flag, &g_device_error))) break;  // own scale atoms
+        if (!(ok = mbar_wait_bounded(&sf_empty[slot], sph ^ 1u, abort_flag, &g_device_error))) break;
+        __syncwarp();
+        tc_fence_after();
+        const uint4* fa = reinterpret_cast<const uint4*>(sSfa + s * PC::kSfa) + lane;
+        const uint4* fb = reinterpret_cast<const uint4*>(sSfb + s * PC::kSfb) + lane;
+        uint32_t va[16], vb[32];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint4 x = fa[j * 32];
+          va[4 * j] = x.x; va[4 * j + 1] = x.y; va[4 * j + 2] = x.z; va[4 * j + 3] = x.w;
+#pragma unroll
+          for (int i = 0; i < PC::kSfbGroups; ++i) {
+            const uint4 y = fb[(i * 4 + j) * 32];
+            const int c = 4 * PC::kSfbGroups * j + 4 * i;
+            vb[c] = y.x; vb[c + 1] = y.y; vb[c + 2] = y.z; vb[c + 3] = y.w;
+          }
+        }
+        const uint32_t base = tmem_sfa + slot * (PC::kSfaCols + PC::kSfbCols) + lanes;
+        tmem_st16(base, va);
+        tmem_st32(base + PC::kSfaCols, vb);
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if (leader) mbar_arrive(&sf_full[slot]); else mbar_arrive_remote(sf_full_leader + 8 * slot);
+          mbar_arrive(&empty[s]);
+        }
+        if (++slot == (uint32_t)PC::kSlots) { slot = 0; sph ^= 1u; }
+        if (++s == (uint32_t)S) { s = 0; ph ^= 1u; }
       }
     }
   } else if (run && warp >= 2) {
@@ -733,14 +802,14 @@ lpq_status make_sf_map(CUtensorMap* map, const void* base, int64_t total_atoms, 
   return LPQ_OK;
 }
 
-template <int KIND, bool kSfbFull>
+template <int KIND, bool kSfbFull, bool SFST = false>
 lpq_status run_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tsa, const CUtensorMap& tsb,
                     GemmArgs g, cudaStream_t s) {
-  using PC = PairCfg<KIND, kSfbFull>;
+  using PC = PairCfg<KIND, kSfbFull, SFST>;
   static bool attr = false;
   if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_pair_kernel<KIND, kSfbFull>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         PC::kSmem);
+    cudaError_t e = cudaFuncSetAttribute(gemm_pair_kernel<KIND, kSfbFull, SFST>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, PC::kSmem);
     if (e != cudaSuccess) return cuda_check(e, "cudaFuncSetAttribute(pair gemm)");
     attr = true;
   }
@@ -754,7 +823,8 @@ lpq_status run_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensor
   g.tiles_m = (int)tm;
   g.tiles_n = (int)tn;
   const int pairs = (int)std::min<int64_t>(tm * tn, g_sms / 2);
-  gemm_pair_kernel<KIND, kSfbFull><<<2 * pairs, kThreadsGemm, PC::kSmem, s>>>(ta, tb, tsa, tsb, g);
+  gemm_pair_kernel<KIND, kSfbFull, SFST>
+      <<<2 * pairs, kThreadsGemm + (SFST ? 32 * kSfWarps : 0), PC::kSmem, s>>>(ta, tb, tsa, tsb, g);
   return cuda_check(cudaGetLastError(), "pair gemm launch");
 }
 
@@ -1096,7 +1166,9 @@ lpq_status launch_gemm(const lpq_qview* a, const lpq_qview* b, void* c, int32_t 
       if ((st = make_sf_map(&tsa, g.sfa, sf_row_groups(m) * g.sfa_kt, 4)) != LPQ_OK) return st;
       if ((st = make_sf_map(&tsb, g.sfb, g.sfb_groups * g.sfb_kt, 4)) != LPQ_OK) return st;
       g.idesc = (g.idesc & ~(31u << 24)) | (16u << 24);
-      return run_pair<kKindNVF4, true>(ta, tb, tsa, tsb, g, s);
+      const char* e = getenv("LPQ_GEMM_SFCP");
+      if (e && e[0] == '1') return run_pair<kKindNVF4, true>(ta, tb, tsa, tsb, g, s);
+      return run_pair<kKindNVF4, true, true>(ta, tb, tsa, tsb, g, s);
     }
     if (nv_bn == 128) {
       if ((st = make_map(&tb, b->codes, false, k / 2, n, k / 2, 128, 128)) != LPQ_OK) return st;
