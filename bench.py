@@ -482,7 +482,9 @@ def run_lpq(args, rank, world, local):
         algo_bytes += (m * k + n * k) * per + m * n * 2
     traffic = profiled_traffic(os.path.join(ROOT, "precision_transformer_gemms_gb300", "csrc", "gemm.cu"), recipe)
     roof = {"bound": "tensor", "achieved": gemm_achieved, "peak": peak, "unit": "TFLOP/s",
-            "frac": gemm_achieved / peak, "traffic": traffic, "kernel": f"gemm_kernel ({recipe})",
+            "frac": gemm_achieved / peak, "traffic": traffic,
+            "kernel": ("gemm_kernel" if os.environ.get("LPQ_GEMM_PAIR", "1")[:1] == "0" else "gemm_pair_kernel")
+            + f" ({recipe})",
             "peak_source": peak_src, "algorithmic_bytes_per_launch": algo_bytes / len(layer.shapes)}
     hbm = peaks["hbm_gbs"] if peaks else 6800.0
 

@@ -51,7 +51,7 @@ struct Cfg {
   static constexpr int kSmem = kStages * kStage + 1024 /*align slack*/ + 512 /*barriers*/;
   static constexpr int kSfaCols = kSfAtoms * 4;
   static constexpr int kSfbCols = kSfAtoms * 4 * (BN / 128);
-  static constexpr int kSlots = SFST ? 4 : 1;  // TMEM scale slots (SFST: written by the scale warps)
+  static constexpr int kSlots = SFST ? 5 : 1;  // TMEM scale slots (SFST: written by the scale warps)
   static constexpr int kCols = NACC * BN + kSlots * (kSfaCols + kSfbCols);
   static constexpr int kTmemCols = kCols <= 32 ? 32 : kCols <= 64 ? 64 : kCols <= 128 ? 128 : kCols <= 256 ? 256 : 512;
   static_assert(kCols <= 512, "TMEM holds 512 columns");
@@ -90,6 +90,15 @@ __device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int
   nt = r / gsize;
 }
 
+// After an abort: wait (bounded, whatever the abort flag says) until the loads
+// issued for ring uses [from, to) have landed, so that none is in flight when
+// the CTA exits.  Use k of a ring of `n` entries completes phase k / n of
+// barrier k % n.
+__device__ __forceinline__ void drain_stages(uint64_t* bars, int n, uint32_t from, uint32_t to) {
+  volatile int no_abort = 0;
+  for (uint32_t k = from; k < to; ++k) mbar_wait_bounded(&bars[k % n], (k / n) & 1u, &no_abort, &g_device_error);
+}
+
 // Persistent warp-specialized GEMM.  Warp 0: TMA producer; warp 1: TMEM
 // allocator and MMA issuer; warps 2..5: epilogue (warp w reads TMEM lanes
 // 32 * (w % 4) ..).  The shared-memory ring runs continuously across the
@@ -112,7 +121,8 @@ __global__ void __launch_bounds__(kThreadsGemm + (SFST ? 32 * kSfWarps : 0))
   uint64_t* acc_empty = acc_full + NACC;
   uint64_t* sf_full = acc_empty + NACC;     // [kSlots] (SFST)
   uint64_t* sf_empty = sf_full + CF::kSlots;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sf_empty + CF::kSlots);
+  uint64_t* sfd = sf_empty + CF::kSlots;    // [S] (SFST): the stage's scale atoms landed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sfd + S);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -122,6 +132,7 @@ __global__ void __launch_bounds__(kThreadsGemm + (SFST ? 32 * kSfWarps : 0))
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], SFST ? 1 + kSfWarps : 1);  // MMA commit (+ the scale warps' reads)
+      mbar_init(&sfd[s], 1);
     }
     for (int a = 0; a < NACC; ++a) {
       mbar_init(&acc_full[a], 1);
@@ -158,22 +169,28 @@ __global__ void __launch_bounds__(kThreadsGemm + (SFST ? 32 * kSfWarps : 0))
           const int s = it % S;
           const uint32_t ph = (it / S) & 1u;
           if (!(ok = mbar_wait_bounded(&empty[s], ph ^ 1u, abort_flag, &g_device_error))) break;
-          mbar_arrive_expect_tx(&full[s], CF::kStage);
-          tma_load_2d(sA + s * CF::kA, &tmA, kt * elem_per_kt, m0, &full[s]);
-          tma_load_2d(sB + s * CF::kB, &tmB, kt * elem_per_kt, n0, &full[s]);
+          // Scale atoms first; with scale warps they land on a barrier of their
+          // own, so the warps move them into TMEM while A and B still arrive.
+          uint64_t* sbar = SFST ? &sfd[s] : &full[s];
+          if constexpr (SFST) mbar_arrive_expect_tx(&sfd[s], CF::kSfa + CF::kSfb);
+          mbar_arrive_expect_tx(&full[s], SFST ? CF::kA + CF::kB : CF::kStage);
           if constexpr (CF::kSfAtoms > 0) {
             bulk_load(sSfa + s * CF::kSfa, g.sfa + ((int64_t)mt * g.sfa_kt + (int64_t)kt * CF::kSfAtoms) * 512,
-                      CF::kSfa, &full[s]);
+                      CF::kSfa, sbar);
 #pragma unroll
             for (int i = 0; i < BN / 128; ++i) {
               int64_t gb = (int64_t)n0 / 128 + i;
               if (gb >= g.sfb_groups) gb = g.sfb_groups - 1;
               bulk_load(sSfb + s * CF::kSfb + i * CF::kSfAtoms * 512,
-                        g.sfb + (gb * g.sfb_kt + (int64_t)kt * CF::kSfAtoms) * 512, CF::kSfAtoms * 512, &full[s]);
+                        g.sfb + (gb * g.sfb_kt + (int64_t)kt * CF::kSfAtoms) * 512, CF::kSfAtoms * 512, sbar);
             }
           }
+          tma_load_2d(sA + s * CF::kA, &tmA, kt * elem_per_kt, m0, &full[s]);
+          tma_load_2d(sB + s * CF::kB, &tmB, kt * elem_per_kt, n0, &full[s]);
         }
       }
+      // After an abort, let the loads still in flight land before the CTA exits.
+      if (!ok) drain_stages(full, S, it > (uint32_t)S ? it - S : 0u, it);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -247,7 +264,7 @@ __global__ void __launch_bounds__(kThreadsGemm + (SFST ? 32 * kSfWarps : 0))
     bool ok = true;
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
       for (int kt = 0; kt < g.num_k; ++kt) {
-        if (!(ok = mbar_wait_bounded(&full[s], ph, abort_flag, &g_device_error))) break;
+        if (!(ok = mbar_wait_bounded(&sfd[s], ph, abort_flag, &g_device_error))) break;
         if (!(ok = mbar_wait_bounded(&sf_empty[slot], sph ^ 1u, abort_flag, &g_device_error))) break;
         __syncwarp();
         tc_fence_after();
@@ -267,7 +284,14 @@ __global__ void __launch_bounds__(kThreadsGemm + (SFST ? 32 * kSfWarps : 0))
         }
         const uint32_t base = tmem_base + NACC * BN + slot * (CF::kSfaCols + CF::kSfbCols) + lanes;
         tmem_st16(base, va);
-        tmem_st32(base + CF::kSfaCols, vb);
+        if constexpr (BN == 256) {
+          tmem_st32(base + CF::kSfaCols, vb);
+        } else {
+          uint32_t vb16[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) vb16[i] = vb[i];
+          tmem_st16(base + CF::kSfaCols, vb16);
+        }
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
@@ -468,7 +492,7 @@ struct PairCfg {
   static constexpr int kNacc = kSfAtoms == 0 ? 2 : 1;
   static constexpr int kSfaCols = kSfAtoms * 4;
   static constexpr int kSfbCols = kSfAtoms * 4 * kSfbGroups;
-  static constexpr int kSlots = SFST ? 4 : 1;
+  static constexpr int kSlots = SFST ? 5 : 1;
   static_assert(kNacc * kPairBN + kSlots * (kSfaCols + kSfbCols) <= 512, "TMEM holds 512 columns");
 };
 
@@ -562,7 +586,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm + (SFST
   if (run && warp == 0) {
     if (lane == 0) {
       const int elem_per_kt = KIND == kKindF16 ? kKBytes / 2 : kKBytes;
-      uint32_t s = 0, ph = 0;
+      uint32_t s = 0, ph = 0, it = 0;
       bool ok = true;
       for (int t = pair; t < total && ok; t += npairs) {
         int mt, nt;
@@ -572,8 +596,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm + (SFST
           if (!(ok = mbar_wait_bounded(&empty[s], ph ^ 1u, abort_flag, &g_device_error))) break;
           if (leader) mbar_arrive_expect_tx(&full[s], SFST ? 2 * (PC::kA + PC::kB) : 2 * PC::kStage);
           const uint32_t fb = full_leader + 8 * s;
-          tma_load_2d_pair(sA + s * PC::kA, &tmA, kt * elem_per_kt, arow, fb);
-          tma_load_2d_pair(sB + s * PC::kB, &tmB, kt * elem_per_kt, brow, fb);
           if constexpr (PC::kSfAtoms > 0) {
             // scale atoms: rows of a 2D map are 512-byte atoms (128 x u32).  With
             // scale warps they land on this CTA's own barrier (its scale warps
@@ -592,9 +614,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm + (SFST
               else tma_load_2d_pair(sSfb + s * PC::kSfb + i * PC::kSfAtoms * 512, &tmSfb, 0, yb, fb);
             }
           }
+          tma_load_2d_pair(sA + s * PC::kA, &tmA, kt * elem_per_kt, arow, fb);
+          tma_load_2d_pair(sB + s * PC::kB, &tmB, kt * elem_per_kt, brow, fb);
+          ++it;
           if (++s == (uint32_t)S) { s = 0; ph ^= 1u; }
         }
       }
+      // After an abort, the even CTA lets the pair's loads in flight land
+      // (they all signal its full barriers) before either CTA exits.
+      if (!ok && leader) drain_stages(full, S, it > (uint32_t)S ? it - S : 0u, it);
     }
   } else if (run && warp == 1) {
     if (lane == 0 && leader) {
@@ -691,7 +719,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm + (SFST
         tc_fence_before();
         __syncwarp();
         if (lane == 0) {
-          if (leader) mbar_arrive(&sf_full[slot]); else mbar_arrive_remote(sf_full_leader + 8 * slot);
+          if (leader) mbar_arrive(&sf_full[slot]); else mbar_arrive_remote_relaxed(sf_full_leader + 8 * slot);
           mbar_arrive(&empty[s]);
         }
         if (++slot == (uint32_t)PC::kSlots) { slot = 0; sph ^= 1u; }
@@ -734,7 +762,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm + (SFST
         tc_fence_before();
         __syncwarp();
         if (lane == 0) {
-          if (leader) mbar_arrive(&acc_empty[a]); else mbar_arrive_remote(acc_empty_leader + 8 * a);
+          if (leader) mbar_arrive(&acc_empty[a]); else mbar_arrive_remote_relaxed(acc_empty_leader + 8 * a);
         }
         if (row < g.M && ncols > 0) {
           __nv_bfloat16* out = static_cast<__nv_bfloat16*>(g.c) + row * g.N + c0;
@@ -760,7 +788,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm + (SFST
           tc_fence_before();
           __syncwarp();
           if (lane == 0) {
-            if (leader) mbar_arrive(&acc_empty[a]); else mbar_arrive_remote(acc_empty_leader + 8 * a);
+            if (leader) mbar_arrive(&acc_empty[a]); else mbar_arrive_remote_relaxed(acc_empty_leader + 8 * a);
           }
         }
         const int64_t col0 = c0 + cc * 32;
@@ -828,15 +856,13 @@ lpq_status run_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensor
   return cuda_check(cudaGetLastError(), "pair gemm launch");
 }
 
-// Kernel path per GEMM: the CTA-pair kernel (256 x 256 tiles) for bf16, FP8
-// and MXFP8, the single-CTA kernel for NVFP4 (its scale-factor copies leave
-// nothing to gain from pairs).  LPQ_GEMM_PAIR=0 forces single CTAs, =1 pairs
-// for every kind; read on every call so both paths can be exercised.
-bool use_pair(int kind) {
+// Kernel path per GEMM: the CTA-pair kernel (256 x 256 tiles) for every kind
+// when M >= 256 (each SM streams half the B bytes of a single-CTA tile).
+// LPQ_GEMM_PAIR=0 forces single CTAs; read on every call so both paths can be
+// exercised.
+bool use_pair(int /*kind*/) {
   const char* e = getenv("LPQ_GEMM_PAIR");
-  if (e && e[0] == '0') return false;
-  if (e && e[0] == '1') return true;
-  return kind != kKindNVF4;
+  return !(e && e[0] == '0');
 }
 // Sub-channel FP8 GEMM ("Faster training throughput in FP8 with NVIDIA NeMo",
 // sub-channel scaling: 1x128 activation and 128x128 weight blocks with FP32
@@ -1064,15 +1090,12 @@ lpq_status run_block_gemm(const CUtensorMap& ta, const CUtensorMap& tb, BlockArg
   return cuda_check(cudaGetLastError(), "block gemm launch");
 }
 
-// Output-tile width of the block-scaled GEMMs: 256 (one TMEM accumulator) or
-// 128 (two accumulators, epilogue overlapped); LPQ_GEMM_BN overrides.
+// Output-tile width of the single-CTA block-scaled GEMMs: 256 (one TMEM
+// accumulator) or 128 (two accumulators, epilogue overlapped); LPQ_GEMM_BN=128
+// selects the latter, read on every call like the other path switches.
 int lpq_gemm_config_bn() {
-  static int bn = -1;
-  if (bn < 0) {
-    const char* e = getenv("LPQ_GEMM_BN");
-    bn = (e && atoi(e) == 128) ? 128 : 256;
-  }
-  return bn;
+  const char* e = getenv("LPQ_GEMM_BN");
+  return (e && atoi(e) == 128) ? 128 : 256;
 }
 
 }  // namespace
@@ -1173,7 +1196,9 @@ lpq_status launch_gemm(const lpq_qview* a, const lpq_qview* b, void* c, int32_t 
     if (nv_bn == 128) {
       if ((st = make_map(&tb, b->codes, false, k / 2, n, k / 2, 128, 128)) != LPQ_OK) return st;
       g.idesc = idesc_block_scaled(1, 1, 0, 128);
-      return run<kKindNVF4, 128, 2>(ta, tb, g, s);
+      const char* e = getenv("LPQ_GEMM_SFCP");
+      if (e && e[0] == '1') return run<kKindNVF4, 128, 2>(ta, tb, g, s);
+      return run<kKindNVF4, 128, 2, true>(ta, tb, g, s);
     }
     const char* e = getenv("LPQ_GEMM_SFCP");  // =1: scale copies by the MMA thread (tcgen05.cp)
     if (e && e[0] == '1') return run<kKindNVF4, BN, 1>(ta, tb, g, s);

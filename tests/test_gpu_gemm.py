@@ -34,19 +34,23 @@ def check(a, b, M, N, K, out_fp32, layout=lpq.FPROP):
     assert nbad == 0, f"{nbad} elements outside the gate (worst {worst:.3g}x)"
 
 
-@pytest.mark.parametrize("path", ["single", "pair", "single_cp"])
+@pytest.mark.parametrize("path", ["single", "pair", "single_cp", "single_bn128"])
 @pytest.mark.parametrize("out_fp32", [True, False])
 @pytest.mark.parametrize("shape", SHAPES)
 @pytest.mark.parametrize("fmts", [(lpq.BF16, lpq.BF16), (lpq.FP8_E4M3, lpq.FP8_E4M3), (lpq.FP8_E5M2, lpq.FP8_E4M3),
                                   (lpq.MXFP8, lpq.MXFP8), (lpq.NVFP4, lpq.NVFP4), (lpq.NVFP4, lpq.NVFP4_2D)])
 def test_gemm_parity(fmts, shape, out_fp32, path, monkeypatch):
     """Every kernel path: one CTA per 128 x 256 tile (NVFP4 scales stored into
-    TMEM by scale warps, or copied by the MMA thread: single_cp), and CTA pairs
-    (cta_group::2) per 256 x 256 tile."""
+    TMEM by scale warps, or copied by the MMA thread: single_cp), one CTA per
+    128 x 128 tile with two accumulators (block-scaled kinds: single_bn128), and
+    CTA pairs (cta_group::2) per 256 x 256 tile."""
     if path == "single_cp" and fmts[0] not in (lpq.NVFP4,):
         pytest.skip("scale-copy variant exists for NVFP4 only")
+    if path == "single_bn128" and fmts[0] not in (lpq.NVFP4, lpq.MXFP8):
+        pytest.skip("128-wide tiles exist for the block-scaled kinds only")
     monkeypatch.setenv("LPQ_GEMM_PAIR", "1" if path == "pair" else "0")
     monkeypatch.setenv("LPQ_GEMM_SFCP", "1" if path == "single_cp" else "0")
+    monkeypatch.setenv("LPQ_GEMM_BN", "128" if path == "single_bn128" else "256")
     M, K, N = shape
     if fmts[1] == lpq.NVFP4_2D and N % 16:
         pytest.skip("2D weight tiles need N % 16 == 0")
