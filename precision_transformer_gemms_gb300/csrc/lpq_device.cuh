@@ -88,6 +88,17 @@ __device__ __forceinline__ int mx_exponent(float a) {
   return e < -127 ? -127 : (e > 127 ? 127 : e);
 }
 
+// Correctly rounded x / 6 for x >= 0 (a block max): the product with
+// RN(1/6), corrected once with the exact residual x - 6 q (an FMA).  Below
+// 2^-120, where the quotient can be subnormal and the correction is not
+// exact, and for infinity, the IEEE division itself.  Equal to the IEEE
+// quotient for every non-negative float (checked exhaustively on the device).
+__device__ __forceinline__ float div6_rn(float x) {
+  if (!(x >= 7.52316385e-37f && x < __int_as_float(0x7F800000))) return __fdiv_rn(x, 6.0f);  // 2^-120
+  const float q = __fmul_rn(x, 0.16666667f);
+  return __fmaf_rn(__fmaf_rn(-q, 6.0f, x), 0.16666667f, q);
+}
+
 // ------------------------------------------------------------------ Philox-4x32-10
 // Salmon et al., SC'11: per round the even words are multiplied by the two
 // multipliers, hi/lo halves mixed with the odd words and the round key; the
@@ -142,12 +153,18 @@ __device__ __forceinline__ uint32_t rht_signs(uint32_t rht_seed) {
   return philox4x32_10(make_uint4(0u, 0u, 2u, 0u), rht_seed, 0u).x & 0xFFFFu;
 }
 
+// The 16 random signs as factors +1 / -1 (bit j of `signs` set: -1), so that
+// the sign flip is a multiply (exact) rather than a select.
+__device__ __forceinline__ void rht_sign_factors(uint32_t signs, float sgn[16]) {
+#pragma unroll
+  for (int j = 0; j < 16; ++j) sgn[j] = ((signs >> j) & 1u) ? -1.0f : 1.0f;
+}
+
 // 16-point random-sign Hadamard: sign flip, butterfly stages h = 1, 2, 4, 8
 // ((t_i, t_{i+h}) -> (t_i + t_{i+h}, t_i - t_{i+h})), then * 1/4.
-__device__ __forceinline__ void rht16(float t[16], uint32_t signs) {
+__device__ __forceinline__ void rht16(float t[16], const float sgn[16]) {
 #pragma unroll
-  for (int j = 0; j < 16; ++j)
-    if ((signs >> j) & 1u) t[j] = -t[j];
+  for (int j = 0; j < 16; ++j) t[j] = __fmul_rn(sgn[j], t[j]);
 #pragma unroll
   for (int h = 1; h < 16; h <<= 1)
 #pragma unroll
@@ -163,22 +180,22 @@ __device__ __forceinline__ void rht16(float t[16], uint32_t signs) {
 
 // Stochastic E2M1 code of y with random word r: between adjacent magnitudes
 // lo <= |y| <= hi, round up iff float(r >> 8) < ((|y| - lo) / (hi - lo)) * 2^24.
-// hi - lo is 0.5, 1 or 2, so the quotient times 2^24 is the exact product
-// (|y| - lo) * 2^24 / (hi - lo) (Sterbenz subtraction, power-of-two scaling).
-// Written with selects rather than branches: lanes of a warp fall on
-// different grid segments.
+// Branch- and select-light (the SR quantizers are bound by the integer/logic
+// pipe): clamping to [-6, 6] saturates (a NaN clamps to +6); the grid spacing
+// d = hi - lo is 2^(max(E, 127) - 128) for the biased exponent E of |y|
+// (0.5 below 2, 1 in [2, 4), 2 in [4, 6]); q = |y| / d is exact, and adding
+// 2^23 with round-toward-zero leaves floor(q) in the low bits.  Every value
+// is exact, so (q - floor(q)) * 2^24 is the threshold of the definition.
 __device__ __forceinline__ uint32_t sr_e2m1(float y, uint32_t r) {
-  const uint32_t s = (__float_as_uint(y) >> 31) << 3;
-  const float a = fabsf(y);
-  const bool seg0 = a < 2.0f, seg1 = a < 4.0f;
-  const float t = seg0 ? __fmul_rn(a, 2.0f) : a;                  // exact
-  const uint32_t q = (uint32_t)__float2int_rz(t);                  // 0..3 (seg0), 2..3 (seg1)
-  const uint32_t lo = seg0 ? q : (seg1 ? q + 2u : 6u);
-  const float vlo = seg0 ? __fmul_rn((float)q, 0.5f) : (seg1 ? (float)q : 4.0f);
-  const float scale = seg0 ? 33554432.0f : (seg1 ? 16777216.0f : 8388608.0f);
-  const bool up = (float)(r >> 8) < __fmul_rn(__fsub_rn(a, vlo), scale);
-  const uint32_t code = (a >= 6.0f || a != a) ? 7u : (up ? lo + 1u : lo);
-  return (a != a) ? 7u : (s | code);
+  const float c = fmaxf(fminf(y, 6.0f), -6.0f);
+  const uint32_t cb = __float_as_uint(c);
+  const uint32_t m = max((cb >> 23) & 0xFFu, 127u);             // 127, 128 or 129
+  const float q = __fmul_rn(fabsf(c), __uint_as_float((255u - m) << 23));  // |y| / d in [0, 4)
+  const float tq = __fadd_rz(q, 8388608.0f);                   // 2^23 + floor(q)
+  const float thr = __fmul_rn(__fsub_rn(q, __fsub_rn(tq, 8388608.0f)), 16777216.0f);
+  const uint32_t up = (float)(r >> 8) < thr ? 1u : 0u;
+  // grid index: floor(q) plus 0 / 2 / 4 for the three spacings, sign in bit 3
+  return (__float_as_uint(tq) & 3u) + 2u * (m - 127u) + up + ((cb >> 31) << 3);
 }
 
 // ------------------------------------------------------------------ warp helpers

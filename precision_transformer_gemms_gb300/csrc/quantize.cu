@@ -86,8 +86,19 @@ __device__ __forceinline__ float block_max(float v, float* red) {
 
 // NVFP4 block scale (E4M3 code) for block max `bmax` and encode scale s_enc.
 __device__ __forceinline__ uint32_t nv_block_scale(float bmax, float s_enc) {
-  float d = __fmul_rn(__fdiv_rn(bmax, 6.0f), s_enc);
+  float d = __fmul_rn(div6_rn(bmax), s_enc);
   return cvt_e4m3x2(d, 0.f) & 0xFFu;
+}
+
+// Per-CTA table of the encode factors s_enc / dec(S) for the 128 E4M3 codes S
+// a block scale can take (0 for S = 0, whose block is all zeros; the NaN code
+// is never produced by the saturating conversion): the per-block division
+// becomes a shared-memory lookup with the same values.
+__device__ __forceinline__ void nv_factor_table(float* tab, float s_enc, int t) {
+  if (t >= 0 && t < 128) {
+    const float Sd = t < 127 ? e4m3_value((uint32_t)t) : 0.f;
+    tab[t] = Sd == 0.f ? 0.f : __fdiv_rn(s_enc, Sd);
+  }
 }
 
 // E2M1 codes of 8 values y[i] = v[i] * f packed into 32 bits (nibble i = value
@@ -126,14 +137,19 @@ __device__ __forceinline__ float nv_ts_dec(const float* amax) {
   return finite_pos(a) ? __fdiv_rn(a, 2688.0f) : 1.0f;
 }
 
-template <int KIND, bool kE5M2>
-__global__ void __launch_bounds__(kThreads) quant_tile_kernel(const QParams p) {
+// NVO (NVFP4 options, compile-time so that the plain paths carry none of the
+// registers of the others): bit 0 stochastic rounding, bit 1 RHT of the
+// column-wise copy.
+template <int KIND, bool kE5M2, int NVO = 0>
+__global__ void __launch_bounds__(kThreads, KIND != QK_NV ? 1 : (NVO == 0 ? 6 : 5)) quant_tile_kernel(const QParams p) {
+  constexpr bool kSR = (NVO & 1) != 0, kRHT = (NVO & 2) != 0;
   constexpr int TR = (KIND == QK_BLK1 || KIND == QK_BLK128) ? 128 : 64;
   __shared__ __align__(16) uint16_t tile[TR][kTC];
   __shared__ float red[kThreads / 32];
   __shared__ float part[2][kTC];
   __shared__ float tile_f[32];
   __shared__ uint32_t tile_s[32];
+  __shared__ float fb_tab[2][128];  // NVFP4: s_enc / dec(S) for the row and column copies
 
   const int t = threadIdx.x;
   const int64_t r0 = (int64_t)blockIdx.y * TR, c0 = (int64_t)blockIdx.x * kTC;
@@ -158,7 +174,7 @@ __global__ void __launch_bounds__(kThreads) quant_tile_kernel(const QParams p) {
     }
   }
   float s_enc_row = 1.f, s_enc_col = 1.f;
-  uint32_t signs = 0;
+  float sgn[16];
   if constexpr (KIND == QK_NV || KIND == QK_NV2D) {
     if (p.row_codes) s_enc_row = nv_s_enc(p.amax_row);
     if (p.col_codes) s_enc_col = nv_s_enc(p.amax_col);
@@ -166,9 +182,12 @@ __global__ void __launch_bounds__(kThreads) quant_tile_kernel(const QParams p) {
       if (p.row_ts) *p.row_ts = nv_ts_dec(p.amax_row);
       if (p.col_ts) *p.col_ts = nv_ts_dec(p.amax_col);
     }
-    if (KIND == QK_NV && p.rht) signs = rht_signs(p.rht_seed);
+    if constexpr (kRHT) rht_sign_factors(rht_signs(p.rht_seed), sgn);
+    nv_factor_table(fb_tab[0], s_enc_row, t);
+    nv_factor_table(fb_tab[1], s_enc_col, t - 128);
+    __syncthreads();
   }
-  const PhiloxKeys keys(p.seed);
+  const PhiloxKeys keys(kSR ? p.seed : 0);  // dead (and free) without stochastic rounding
 
   // ---------------------------------------------------------------- load (+ row-wise copy)
   const int lr = t >> 4;        // row within a 16-row slab
@@ -221,15 +240,14 @@ __global__ void __launch_bounds__(kThreads) quant_tile_kernel(const QParams p) {
       for (int i = 0; i < 8; ++i) m = absmax_acc(m, f[i]);
       m = warp_max_xor(m, 2);
       const uint32_t S = nv_block_scale(m, s_enc_row);
-      const float Sd = e4m3_value(S);
-      const float fb = Sd == 0.f ? 0.f : __fdiv_rn(s_enc_row, Sd);
+      const float fb = fb_tab[0][S];
       uint4 w0 = make_uint4(0, 0, 0, 0), w1 = w0;
-      if (p.sr) {
+      if constexpr (kSR) {
         const uint64_t g = (p.ctr_off + (uint64_t)(r * C + c0 + lc)) >> 2;
         w0 = keys.words(g, 0u);
         w1 = keys.words(g + 1, 0u);
       }
-      const uint32_t q = nv_codes8(f, fb, p.sr, w0, w1);
+      const uint32_t q = nv_codes8(f, fb, kSR, w0, w1);
       if (ok) {
         *reinterpret_cast<uint32_t*>(p.row_codes + r * (C >> 1) + ((c0 + lc) >> 1)) = q;
         if ((t & 1) == 0) {
@@ -284,9 +302,8 @@ __global__ void __launch_bounds__(kThreads) quant_tile_kernel(const QParams p) {
       if (sub == 0) {
         const float s_enc = p.row_codes ? s_enc_row : s_enc_col;
         const uint32_t S = nv_block_scale(m, s_enc);
-        const float Sd = e4m3_value(S);
         tile_s[tid] = S;
-        tile_f[tid] = Sd == 0.f ? 0.f : __fdiv_rn(s_enc, Sd);
+        tile_f[tid] = fb_tab[p.row_codes ? 0 : 1][S];
       }
     }
     __syncthreads();
@@ -445,22 +462,21 @@ __global__ void __launch_bounds__(kThreads) quant_tile_kernel(const QParams p) {
       float f[16];
 #pragma unroll
       for (int i = 0; i < 16; ++i) f[i] = tile_val(tile[rh * 32 + hb * 16 + i], cl);
-      if (p.rht) rht16(f, signs);
+      if constexpr (kRHT) rht16(f, sgn);
       float m = 0.f;
 #pragma unroll
       for (int i = 0; i < 16; ++i) m = absmax_acc(m, f[i]);
       const uint32_t S = nv_block_scale(m, s_enc_col);
-      const float Sd = e4m3_value(S);
-      const float fb = Sd == 0.f ? 0.f : __fdiv_rn(s_enc_col, Sd);
+      const float fb = fb_tab[1][S];
       const int64_t rr = rbase + hb * 16;
       uint4 w[4] = {uint4{}, uint4{}, uint4{}, uint4{}};
-      if (p.sr) {
+      if constexpr (kSR) {
         const uint64_t g = (p.ctr_off + (uint64_t)(c * R + rr)) >> 2;
 #pragma unroll
         for (int j = 0; j < 4; ++j) w[j] = keys.words(g + j, 1u);
       }
-      const uint32_t a = nv_codes8(f, fb, p.sr, w[0], w[1]);
-      const uint32_t b = nv_codes8(f + 8, fb, p.sr, w[2], w[3]);
+      const uint32_t a = nv_codes8(f, fb, kSR, w[0], w[1]);
+      const uint32_t b = nv_codes8(f + 8, fb, kSR, w[2], w[3]);
       *reinterpret_cast<uint2*>(p.col_codes + c * (R >> 1) + (rr >> 1)) = make_uint2(a, b);
       const int64_t kb = rr >> 4;
       const int64_t off = p.col_gemm ? sf_gemm_offset(c, kb, p.col_kt) : c * (R >> 4) + kb;
@@ -499,7 +515,8 @@ __global__ void __launch_bounds__(kThreads) amax_kernel(const uint16_t* __restri
       for (int j = 0; j < 8; ++j) m = absmax_acc(m, f[j]);
     }
   } else {
-    const uint32_t signs = rht_signs(rht_seed);
+    float sgn[16];
+    rht_sign_factors(rht_signs(rht_seed), sgn);
     const int64_t n = (R >> 4) * chunks;  // units of 16 rows x 8 columns
     for (int64_t u = (int64_t)blockIdx.x * kThreads + threadIdx.x; u < n; u += (int64_t)gridDim.x * kThreads) {
       const int64_t rg = u / chunks, cc = u - rg * chunks;
@@ -515,7 +532,7 @@ __global__ void __launch_bounds__(kThreads) amax_kernel(const uint16_t* __restri
           t[i] = (col & 1) ? bf16_hi(w) : bf16_lo(w);
           m = absmax_acc(m, t[i]);
         }
-        rht16(t, signs);
+        rht16(t, sgn);
 #pragma unroll
         for (int i = 0; i < 16; ++i) mh = absmax_acc(mh, t[i]);
       }
@@ -574,12 +591,12 @@ int num_sms() {
   return g_num_sms;
 }
 
-template <int KIND, bool kE5M2>
+template <int KIND, bool kE5M2, int NVO = 0>
 lpq_status run_tile(const QParams& p, cudaStream_t s) {
   constexpr int TR = (KIND == QK_BLK1 || KIND == QK_BLK128) ? 128 : 64;
   dim3 grid((unsigned)((p.C + kTC - 1) / kTC), (unsigned)((p.R + TR - 1) / TR));
   if (grid.y > 65535u) return set_error(LPQ_ERR_SHAPE, "too many rows (%lld) for one launch", (long long)p.R);
-  quant_tile_kernel<KIND, kE5M2><<<grid, kThreads, 0, s>>>(p);
+  quant_tile_kernel<KIND, kE5M2, NVO><<<grid, kThreads, 0, s>>>(p);
   return cuda_check(cudaGetLastError(), "quantize kernel launch");
 }
 
@@ -712,7 +729,13 @@ lpq_status launch_quantize(const void* xv, int64_t R, int64_t C, int32_t fmt, in
       if ((st = run_amax(p.x, R, C, raw0, raw1, rh, rht_seed, s)) != LPQ_OK) return st;
       p.amax_row = rv ? rv->amax : nullptr;
       p.amax_col = cv ? cv->amax : nullptr;
-      return fmt == LPQ_NVFP4 ? run_tile<QK_NV, false>(p, s) : run_tile<QK_NV2D, false>(p, s);
+      if (fmt == LPQ_NVFP4_2D) return run_tile<QK_NV2D, false>(p, s);
+      switch ((p.sr ? 1 : 0) | (p.rht ? 2 : 0)) {
+        case 0: return run_tile<QK_NV, false, 0>(p, s);
+        case 1: return run_tile<QK_NV, false, 1>(p, s);
+        case 2: return run_tile<QK_NV, false, 2>(p, s);
+        default: return run_tile<QK_NV, false, 3>(p, s);
+      }
     }
     case LPQ_FP8_BLOCK_1x128:
       return run_tile<QK_BLK1, false>(p, s);
