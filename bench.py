@@ -616,6 +616,7 @@ def run_mma_peaks(args):
             out[kind + "_scale_copies_two_regions"] = lpq.mma_peak(kind, iters=iters, with_scale_copies=2)
             out[kind + "_scale_copies_interleaved"] = lpq.mma_peak(kind, iters=iters, with_scale_copies=3)
             out[kind + "_scales_stored_by_warps"] = lpq.mma_peak(kind, iters=iters, with_scale_copies=4)
+            out[kind + "_scale_copies_by_other_warp"] = lpq.mma_peak(kind, iters=iters, with_scale_copies=5)
     out["clocks"] = clocks.stop()
     out["unit"] = "TFLOP/s"
     print(json.dumps(out), flush=True)

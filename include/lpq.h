@@ -233,7 +233,10 @@ lpq_status lpq_selftest_wait(uint64_t limit_ns, lpq_stream_t stream);
  * scale factors (kinds 2, 3): 1 = all of a step's copies before its MMAs,
  * 2 = the same into two alternating TMEM regions, 3 = each MMA's copies
  * right before it, 4 = the scale columns rewritten by four other warps with
- * tcgen05.st while the MMAs run (NVFP4; throughput only).  FLOPs = SMs * iters * 4 * 2 * 128 * 256 * K;
+ * tcgen05.st while the MMAs run, 5 = the step's copies issued by a thread of
+ * another warp while the MMAs run (4 and 5: NVFP4 only, unsynchronised with
+ * the MMAs, throughput only).  Other values give LPQ_ERR_INVALID_ARG.
+ * FLOPs = SMs * iters * 4 * 2 * 128 * 256 * K;
  * the caller times the launch with events on `stream`. */
 lpq_status lpq_mma_peak(int32_t kind, int32_t iters, int32_t with_scale_copies, lpq_stream_t stream);
 

@@ -277,6 +277,8 @@ lpq_status lpq_selftest_wait(uint64_t limit_ns, lpq_stream_t stream) {
 lpq_status lpq_mma_peak(int32_t kind, int32_t iters, int32_t with_scale_copies, lpq_stream_t stream) {
   if (kind < 0 || kind > 3) return set_error(LPQ_ERR_INVALID_ARG, "kind %d", kind);
   if (iters < 1 || iters > (1 << 24)) return set_error(LPQ_ERR_INVALID_ARG, "iters %d", iters);
+  if (with_scale_copies < 0 || with_scale_copies > 5 || (with_scale_copies > 1 && kind != 3))
+    return set_error(LPQ_ERR_INVALID_ARG, "with_scale_copies %d for kind %d", with_scale_copies, kind);
   lpq_status st = check_arch();
   if (st != LPQ_OK) return st;
   return launch_mma_peak(kind, iters, with_scale_copies, reinterpret_cast<cudaStream_t>(stream));

@@ -1229,7 +1229,7 @@ lpq_status launch_gemm(const lpq_qview* a, const lpq_qview* b, void* c, int32_t 
 // traffic), optionally with the per-step scale-factor copies of the
 // block-scaled kinds.  Operands are zero; the FLOP count is what is timed.
 template <int KIND, int MODE>
-__global__ void __launch_bounds__(128, 1) mma_peak_kernel(int iters, uint32_t idesc) {
+__global__ void __launch_bounds__(256, 1) mma_peak_kernel(int iters, uint32_t idesc) {
   constexpr int with_sf = MODE;
   constexpr int BN = 256;
   using CF = Cfg<KIND, BN, 1>;
@@ -1238,14 +1238,15 @@ __global__ void __launch_bounds__(128, 1) mma_peak_kernel(int iters, uint32_t id
   uint8_t* sA = smem;
   uint8_t* sB = sA + CF::kA;
   uint8_t* sSf = sB + CF::kB;
-  uint64_t* bar = reinterpret_cast<uint64_t*>(sSf + CF::kSfa + CF::kSfb);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 1);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sSf + CF::kSfa + CF::kSfb);  // [2]: MMAs, other-warp copies
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 2);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
   const int warp = threadIdx.x >> 5;
   for (int i = threadIdx.x; i < (CF::kA + CF::kB + CF::kSfa + CF::kSfb) / 16; i += blockDim.x)
     reinterpret_cast<uint4*>(smem)[i] = make_uint4(0, 0, 0, 0);
   if (threadIdx.x == 0) {
     mbar_init(bar, 1);
+    mbar_init(bar + 1, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -1256,8 +1257,38 @@ __global__ void __launch_bounds__(128, 1) mma_peak_kernel(int iters, uint32_t id
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
   // with_sf: 0 none, 1 all copies of a step before its MMAs, 2 the same into
-  // two alternating TMEM regions, 3 each MMA's copies right before it
+  // two alternating TMEM regions, 3 each MMA's copies right before it,
+  // 4 (NVFP4) the scale columns rewritten with tcgen05.st by warps 4..7 while
+  // the MMAs run, 5 (NVFP4) the step's 12 copies issued by warp 4 while the
+  // MMAs run.  Modes 4 and 5 are unsynchronised with the MMAs: a rate probe.
   const uint32_t region = CF::kSfaCols + CF::kSfbCols;
+  if (MODE >= 4 && warp >= 4) {
+    const uint32_t tsfa = tbase + BN, tsfb = tsfa + CF::kSfaCols;
+    if constexpr (MODE == 4) {
+      uint32_t z16[16], z32[32];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) z16[i] = 0x38383838u;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) z32[i] = 0x38383838u;
+      const uint32_t lanes = (uint32_t)((warp & 3) * 32) << 16;
+      for (int it = 0; it < iters; ++it) {
+        tmem_st16(tsfa + lanes, z16);
+        tmem_st32(tsfb + lanes, z32);
+        tmem_wait_st();
+      }
+    } else if (MODE == 5 && warp == 4 && (threadIdx.x & 31) == 0) {
+      const uint32_t kHiSf = (uint32_t)(smem_desc(0, 0, 128, 0) >> 32);
+      const uint32_t flo = smem_u32(sSf) >> 4;
+      for (int it = 0; it < iters; ++it)
+        for (int j = 0; j < 4; ++j) {
+          tmem_cp_sf(tsfa + 4 * j, ((uint64_t)kHiSf << 32) | (flo + j * 32));
+          tmem_cp_sf(tsfb + 8 * j, ((uint64_t)kHiSf << 32) | (flo + 128 + j * 32));
+          tmem_cp_sf(tsfb + 8 * j + 4, ((uint64_t)kHiSf << 32) | (flo + 256 + j * 32));
+        }
+      tc_commit(bar + 1);
+      mbar_wait_bounded(bar + 1, 0, abort_flag, &g_device_error);
+    }
+  }
   if (threadIdx.x == 0) {
     const uint32_t kHiSw = (uint32_t)(smem_desc(0, 16, 1024, 2) >> 32);
     const uint32_t kHiSf = (uint32_t)(smem_desc(0, 0, 128, 0) >> 32);
@@ -1320,7 +1351,7 @@ lpq_status run_peak(int iters, uint32_t idesc, cudaStream_t s) {
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  mma_peak_kernel<KIND, MODE><<<sms, 128, smem, s>>>(iters, idesc);
+  mma_peak_kernel<KIND, MODE><<<sms, MODE >= 4 ? 256 : 128, smem, s>>>(iters, idesc);
   return cuda_check(cudaGetLastError(), "peak kernel launch");
 }
 
@@ -1335,7 +1366,10 @@ lpq_status launch_mma_peak(int32_t kind, int32_t iters, int32_t with_sf, cudaStr
         case 0: return run_peak<kKindNVF4, 0>(iters, nv, s);
         case 1: return run_peak<kKindNVF4, 1>(iters, nv, s);
         case 2: return run_peak<kKindNVF4, 2>(iters, nv, s);
-        default: return run_peak<kKindNVF4, 3>(iters, nv, s);
+        case 3: return run_peak<kKindNVF4, 3>(iters, nv, s);
+        case 4: return run_peak<kKindNVF4, 4>(iters, nv, s);
+        case 5: return run_peak<kKindNVF4, 5>(iters, nv, s);
+        default: return set_error(LPQ_ERR_INVALID_ARG, "with_scale_copies %d", with_sf);
       }
   }
   return set_error(LPQ_ERR_INVALID_ARG, "kind %d", kind);

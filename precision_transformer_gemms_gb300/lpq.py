@@ -245,7 +245,7 @@ def mma_peak(kind, iters=20000, with_scale_copies=True, stream=None):
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     _check(lib().lpq_mma_peak(k, 64, int(with_scale_copies), _stream(stream)))  # warm-up
     e0.record()
-    _check(lib().lpq_mma_peak(k, iters, int(with_scale_copies), _stream(stream)))  # noqa: E501 (mode 0..3)
+    _check(lib().lpq_mma_peak(k, iters, int(with_scale_copies), _stream(stream)))  # mode 0..5
     e1.record()
     torch.cuda.synchronize()
     sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count

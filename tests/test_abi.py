@@ -95,3 +95,12 @@ def test_scale_update_and_selftest_validation():
     assert L.lpq_scale_update(ctypes.byref(st), None, 448.0, None) == lpq.ERR_INVALID_ARG
     assert L.lpq_selftest_wait(0, None) == lpq.ERR_INVALID_ARG
     assert L.lpq_selftest_wait(5_000_000_000, None) == lpq.ERR_INVALID_ARG
+
+
+def test_mma_peak_validation():
+    """Rate-probe arguments are checked before any device call."""
+    L = lpq.lib()
+    assert L.lpq_mma_peak(4, 10, 0, None) == lpq.ERR_INVALID_ARG     # no such kind
+    assert L.lpq_mma_peak(3, 0, 0, None) == lpq.ERR_INVALID_ARG      # iters
+    assert L.lpq_mma_peak(3, 10, 6, None) == lpq.ERR_INVALID_ARG     # no such mode
+    assert L.lpq_mma_peak(2, 10, 4, None) == lpq.ERR_INVALID_ARG     # modes 2..5 are NVFP4 only

@@ -194,3 +194,15 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     x, bits = bf16_input((64, 128), seed=41)
     q = lpq.quantize(x, lpq.MXFP8, lpq.ROWWISE)
     assert np.array_equal(q.row.codes_matrix().cpu().numpy(), o.mxfp8(bits, colwise=False)["row"])
+
+
+@pytest.mark.parametrize("kind,mode", [("bf16", 0), ("fp8", 0), ("mxfp8", 0), ("mxfp8", 1), ("nvfp4", 0), ("nvfp4", 1),
+                                       ("nvfp4", 2), ("nvfp4", 3), ("nvfp4", 4), ("nvfp4", 5)])
+def test_mma_peak_modes_run(kind, mode):
+    """Every rate-probe mode runs to completion with a clean device status and
+    a rate below the nominal dense peak of its kind (x1.2 for clock slack)."""
+    rate = lpq.mma_peak(kind, iters=256, with_scale_copies=mode)
+    torch.cuda.synchronize()
+    assert lpq.device_status() == 0
+    nominal = {"bf16": 2250, "fp8": 4500, "mxfp8": 4500, "nvfp4": 13500}[kind]
+    assert 0 < rate < 1.2 * nominal
