@@ -178,24 +178,27 @@ __device__ __forceinline__ void rht16(float t[16], const float sgn[16]) {
   for (int j = 0; j < 16; ++j) t[j] = __fmul_rn(0.25f, t[j]);
 }
 
-// Stochastic E2M1 code of y with random word r: between adjacent magnitudes
-// lo <= |y| <= hi, round up iff float(r >> 8) < ((|y| - lo) / (hi - lo)) * 2^24.
-// Branch- and select-light (the SR quantizers are bound by the integer/logic
-// pipe): clamping to [-6, 6] saturates (a NaN clamps to +6); the grid spacing
-// d = hi - lo is 2^(max(E, 127) - 128) for the biased exponent E of |y|
-// (0.5 below 2, 1 in [2, 4), 2 in [4, 6]); q = |y| / d is exact, and adding
-// 2^23 with round-toward-zero leaves floor(q) in the low bits.  Every value
-// is exact, so (q - floor(q)) * 2^24 is the threshold of the definition.
-__device__ __forceinline__ uint32_t sr_e2m1(float y, uint32_t r) {
+// Stochastic E2M1 rounding of y with random word r: between adjacent
+// magnitudes lo <= |y| <= hi, round up iff float(r >> 8) < ((|y| - lo) /
+// (hi - lo)) * 2^24.  Returned as the rounded value (a grid point with the
+// sign of y; +6 for NaN, saturating at 6), which cvt.rn.satfinite.e2m1x2
+// encodes exactly.  Written for the FMA pipe (the SR quantizers are bound by
+// the integer/logic pipe): the spacing d = hi - lo is 2^(k-1) for 2^k the
+// power-of-two part of max(|y|, 1) (0.5 below 2, 1 in [2, 4), 2 in [4, 6]);
+// q = |y| / d is exact and adding 2^23 with round-toward-zero leaves floor(q);
+// every value is exact, so (q - floor(q)) * 2^24 is the threshold of the
+// definition, and the up/down decision is the saturated product of the exact
+// difference thr - float(r >> 8) scaled by 2^128 (1 when positive, else 0).
+__device__ __forceinline__ float sr_e2m1_value(float y, uint32_t r) {
   const float c = fmaxf(fminf(y, 6.0f), -6.0f);
-  const uint32_t cb = __float_as_uint(c);
-  const uint32_t m = max((cb >> 23) & 0xFFu, 127u);             // 127, 128 or 129
-  const float q = __fmul_rn(fabsf(c), __uint_as_float((255u - m) << 23));  // |y| / d in [0, 4)
-  const float tq = __fadd_rz(q, 8388608.0f);                   // 2^23 + floor(q)
-  const float thr = __fmul_rn(__fsub_rn(q, __fsub_rn(tq, 8388608.0f)), 16777216.0f);
-  const uint32_t up = (float)(r >> 8) < thr ? 1u : 0u;
-  // grid index: floor(q) plus 0 / 2 / 4 for the three spacings, sign in bit 3
-  return (__float_as_uint(tq) & 3u) + 2u * (m - 127u) + up + ((cb >> 31) << 3);
+  const uint32_t e = __float_as_uint(fmaxf(fabsf(c), 1.0f)) & 0x7F800000u;  // 2^k, k = 0, 1, 2
+  const float d = __fmul_rn(__uint_as_float(e), 0.5f);                        // spacing 2^(k-1)
+  const float q = __fmul_rn(fabsf(c), __uint_as_float(0x7F800000u - e));      // |y| / d, exact
+  const float fl = __fsub_rn(__fadd_rz(q, 8388608.0f), 8388608.0f);           // floor(q)
+  const float thr = __fmul_rn(__fsub_rn(q, fl), 16777216.0f);
+  const float up = __saturatef(__fmul_rn(__fmul_rn(__fsub_rn(thr, (float)(r >> 8)), 1.8446744e19f), 1.8446744e19f));
+  const float v = __fmul_rn(__fadd_rn(fl, up), d);
+  return __uint_as_float(__float_as_uint(v) | (__float_as_uint(c) & 0x80000000u));
 }
 
 // ------------------------------------------------------------------ warp helpers

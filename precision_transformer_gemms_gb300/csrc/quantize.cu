@@ -112,7 +112,8 @@ __device__ __forceinline__ uint32_t nv_codes8(const float v[8], float f, bool sr
   if (sr) {
     const uint32_t w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
-    for (int i = 0; i < 8; ++i) out |= sr_e2m1(y[i], w[i]) << (4 * i);
+    for (int i = 0; i < 4; ++i)
+      out |= cvt_e2m1x2(sr_e2m1_value(y[2 * i], w[2 * i]), sr_e2m1_value(y[2 * i + 1], w[2 * i + 1])) << (8 * i);
   } else {
 #pragma unroll
     for (int i = 0; i < 4; ++i) out |= cvt_e2m1x2(y[2 * i], y[2 * i + 1]) << (8 * i);
