@@ -527,21 +527,56 @@ def run_lpq(args, rank, world, local):
                     if f"{mode}_ms_per_layer" in res:
                         res[f"{mode}_speedup_vs_bf16"] = recipes["bf16"]["prequant_ms_per_layer"] / res[f"{mode}_ms_per_layer"]
 
-    # e2e: pinned host inputs -> device, step, outputs -> host, every step
+    # e2e: every step copies its bf16 inputs from pinned host memory and its
+    # outputs back to pinned host memory.  Copies run on their own streams,
+    # double-buffered (inputs of step s+1 and outputs of step s-1 move while
+    # step s computes); events order each buffer's reuse.
     e2e = None
     if not args.no_e2e:
         host_in = {lin: {r: t.cpu().pin_memory() for r, t in d.items()} for lin, d in layer.inp.items()}
-        host_out = {n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for n, t in layer.out.items()}
+        host_out = [{n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for n, t in layer.out.items()}
+                    for _ in range(2)]
+        inp_sets = [layer.inp, {lin: {r: torch.empty_like(t) for r, t in d.items()} for lin, d in layer.inp.items()}]
+        out_sets = [layer.out, {n: torch.empty_like(t) for n, t in layer.out.items()}]
         bi, bo = layer.step_io_bytes()
         steps = max(3, args.steps // 2)
+        comp = torch.cuda.current_stream()
+        nlanes = int(os.environ.get("LPQ_E2E_COPY_STREAMS", "1"))  # copy streams per direction (more were slower)
+        s_in = [torch.cuda.Stream() for _ in range(nlanes)]
+        s_out = [torch.cuda.Stream() for _ in range(nlanes)]
+        ev_comp, ev_out = [None, None], [[], []]
+        in_list = [(lin, r) for lin, d in layer.inp.items() for r in d]
+        out_list = list(layer.out)
 
         def e2e_step(s):
-            for lin, d in layer.inp.items():
-                for r, t in d.items():
-                    t.copy_(host_in[lin][r], non_blocking=True)
+            k = s % 2
+            ev_in = []
+            for j, st in enumerate(s_in):
+                with torch.cuda.stream(st):
+                    if ev_comp[k] is not None:
+                        st.wait_event(ev_comp[k])  # step s-2 no longer reads input set k
+                    for lin, r in in_list[j::nlanes]:
+                        inp_sets[k][lin][r].copy_(host_in[lin][r], non_blocking=True)
+                    ev = torch.cuda.Event()
+                    ev.record(st)
+                    ev_in.append(ev)
+            for ev in ev_in:
+                comp.wait_event(ev)
+            for ev in ev_out[k]:
+                comp.wait_event(ev)  # outputs of step s-2 have left output set k
+            layer.inp, layer.out = inp_sets[k], out_sets[k]
             layer.step(recipe, autocast, s)
-            for n, t in layer.out.items():
-                host_out[n].copy_(t, non_blocking=True)
+            ev_comp[k] = torch.cuda.Event()
+            ev_comp[k].record(comp)
+            ev_out[k] = []
+            for j, st in enumerate(s_out):
+                with torch.cuda.stream(st):
+                    st.wait_event(ev_comp[k])
+                    for n in out_list[j::nlanes]:
+                        host_out[k][n].copy_(out_sets[k][n], non_blocking=True)
+                    ev = torch.cuda.Event()
+                    ev.record(st)
+                    ev_out[k].append(ev)
 
         for w in range(2):
             e2e_step(w)
@@ -553,9 +588,12 @@ def run_lpq(args, rank, world, local):
         torch.cuda.synchronize()
         barrier(world)
         dt = max_over_ranks((time.perf_counter() - t0) / steps, world)
+        layer.inp, layer.out = inp_sets[0], out_sets[0]
         e2e = {"value": layer.flops * world / dt / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": bi,
-               "d2h_bytes_per_step": bo, "ms_per_step": dt * 1e3}
-        del host_in, host_out
+               "d2h_bytes_per_step": bo, "ms_per_step": dt * 1e3,
+               "copies": f"pinned host <-> device on {nlanes} copy streams per direction, double-buffered against "
+                         "the compute stream"}
+        del host_in, host_out, inp_sets, out_sets
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
