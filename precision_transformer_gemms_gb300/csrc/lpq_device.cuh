@@ -185,18 +185,21 @@ __device__ __forceinline__ void rht16(float t[16], const float sgn[16]) {
 // encodes exactly.  Written for the FMA pipe (the SR quantizers are bound by
 // the integer/logic pipe): the spacing d = hi - lo is 2^(k-1) for 2^k the
 // power-of-two part of max(|y|, 1) (0.5 below 2, 1 in [2, 4), 2 in [4, 6]);
-// q = |y| / d is exact and adding 2^23 with round-toward-zero leaves floor(q);
-// every value is exact, so (q - floor(q)) * 2^24 is the threshold of the
-// definition, and the up/down decision is the saturated product of the exact
-// difference thr - float(r >> 8) scaled by 2^128 (1 when positive, else 0).
+// q = |y| / d and floor(q) are exact, so (q - floor(q)) * 2^24 is the
+// threshold of the definition, and the up/down decision is the saturated
+// product of the difference thr - float(r >> 8) (its sign exact) scaled by
+// 2^127 (1 when positive, else 0).
 __device__ __forceinline__ float sr_e2m1_value(float y, uint32_t r) {
   const float c = fmaxf(fminf(y, 6.0f), -6.0f);
   const uint32_t e = __float_as_uint(fmaxf(fabsf(c), 1.0f)) & 0x7F800000u;  // 2^k, k = 0, 1, 2
   const float d = __fmul_rn(__uint_as_float(e), 0.5f);                        // spacing 2^(k-1)
   const float q = __fmul_rn(fabsf(c), __uint_as_float(0x7F800000u - e));      // |y| / d, exact
-  const float fl = __fsub_rn(__fadd_rz(q, 8388608.0f), 8388608.0f);           // floor(q)
-  const float thr = __fmul_rn(__fsub_rn(q, fl), 16777216.0f);
-  const float up = __saturatef(__fmul_rn(__fmul_rn(__fsub_rn(thr, (float)(r >> 8)), 1.8446744e19f), 1.8446744e19f));
+  const float fl = floorf(q);
+  // (q - fl) * 2^24 - float(r >> 8) in one rounding: the product is exact, so
+  // the sign is that of thr - float(r >> 8), and a positive value is at least
+  // 2^-124 (thr >= 2^-124 when r >> 8 is 0, else an ulp of thr >= 1).
+  const float diff = __fmaf_rn(__fsub_rn(q, fl), 16777216.0f, -(float)(r >> 8));
+  const float up = __saturatef(__fmul_rn(diff, 1.70141183e38f));  // * 2^127: >= 8 when positive
   const float v = __fmul_rn(__fadd_rn(fl, up), d);
   return __uint_as_float(__float_as_uint(v) | (__float_as_uint(c) & 0x80000000u));
 }

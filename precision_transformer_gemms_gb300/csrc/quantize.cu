@@ -142,7 +142,7 @@ __device__ __forceinline__ float nv_ts_dec(const float* amax) {
 // registers of the others): bit 0 stochastic rounding, bit 1 RHT of the
 // column-wise copy.
 template <int KIND, bool kE5M2, int NVO = 0>
-__global__ void __launch_bounds__(kThreads, KIND != QK_NV ? 1 : (NVO == 0 ? 6 : 5)) quant_tile_kernel(const QParams p) {
+__global__ void __launch_bounds__(kThreads, KIND == QK_NV2D ? 5 : (KIND != QK_NV ? 1 : (NVO == 0 ? 6 : 5))) quant_tile_kernel(const QParams p) {
   constexpr bool kSR = (NVO & 1) != 0, kRHT = (NVO & 2) != 0;
   constexpr int TR = (KIND == QK_BLK1 || KIND == QK_BLK128) ? 128 : 64;
   __shared__ __align__(16) uint16_t tile[TR][kTC];
@@ -298,7 +298,12 @@ __global__ void __launch_bounds__(kThreads, KIND != QK_NV ? 1 : (NVO == 0 ? 6 : 
 #pragma unroll
       for (int rr = 0; rr < 2; ++rr)
 #pragma unroll
-        for (int i = 0; i < 16; ++i) m = absmax_acc(m, tile_val(tile[tr * 16 + sub * 2 + rr], tc * 16 + i));
+        for (int h = 0; h < 2; ++h) {  // 16-byte shared loads of 8 values
+          float f[8];
+          unpack8(*reinterpret_cast<const uint4*>(&tile[tr * 16 + sub * 2 + rr][tc * 16 + 8 * h]), f);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) m = absmax_acc(m, f[i]);
+        }
       m = warp_max_xor(m, 8);
       if (sub == 0) {
         const float s_enc = p.row_codes ? s_enc_row : s_enc_col;
@@ -316,8 +321,7 @@ __global__ void __launch_bounds__(kThreads, KIND != QK_NV ? 1 : (NVO == 0 ? 6 : 
         if (!(col_ok && r < R)) continue;
         const int tid = (rl >> 4) * 8 + (lc >> 4);
         float f[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) f[i] = tile_val(tile[rl], lc + i);
+        unpack8(vbuf[it], f);  // this thread's own loaded values of the row
         const uint32_t q = nv_codes8(f, tile_f[tid], false, uint4{}, uint4{});
         *reinterpret_cast<uint32_t*>(p.row_codes + r * (C >> 1) + ((c0 + lc) >> 1)) = q;
         if ((t & 1) == 0) {
@@ -328,32 +332,33 @@ __global__ void __launch_bounds__(kThreads, KIND != QK_NV ? 1 : (NVO == 0 ? 6 : 
       }
     }
     if (p.col_codes) {
-      const int cl = t & 127, rh = t >> 7;
-      const int64_t c = c0 + cl, rbase = r0 + rh * 32;
-      if (c < C && rbase < R) {
-        uint32_t q[2];
+      // Two adjacent columns per thread, one 16-row block: each 4-byte shared
+      // load gives a row's values of both columns (both in the same 16x16 tile).
+      const int cp = t & 63, rq = t >> 6;
+      const int cl = 2 * cp;
+      const int64_t c = c0 + cl, rr = r0 + rq * 16;
+      if (c < C && rr < R) {
+        const int tid = rq * 8 + (cl >> 4);
+        float f0[16], f1[16];
 #pragma unroll
-        for (int hb = 0; hb < 2; ++hb) {
-          const int rl = rh * 32 + hb * 16;
-          const int tid = (rl >> 4) * 8 + (cl >> 4);
-          float f0[8], f1[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            f0[i] = tile_val(tile[rl + i], cl);
-            f1[i] = tile_val(tile[rl + 8 + i], cl);
-          }
-          const float fb = tile_f[tid];
-          const uint32_t a = nv_codes8(f0, fb, false, uint4{}, uint4{});
-          const uint32_t b = nv_codes8(f1, fb, false, uint4{}, uint4{});
-          q[hb] = 0;
-          if (rbase + hb * 16 < R) {
-            *reinterpret_cast<uint2*>(p.col_codes + c * (R >> 1) + ((rbase + hb * 16) >> 1)) = make_uint2(a, b);
-            const int64_t kb = (rbase + hb * 16) >> 4;
-            const int64_t off = p.col_gemm ? sf_gemm_offset(c, kb, p.col_kt) : c * (R >> 4) + kb;
-            p.col_sf[off] = (uint8_t)tile_s[tid];
-          }
+        for (int i = 0; i < 16; ++i) {
+          const uint32_t w = *reinterpret_cast<const uint32_t*>(&tile[rq * 16 + i][cl]);
+          f0[i] = bf16_lo(w);
+          f1[i] = bf16_hi(w);
         }
-        (void)q;
+        const float fb = tile_f[tid];
+        const int64_t kb = rr >> 4;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int64_t cc = c + h;
+          if (cc >= C) break;
+          const float* v = h ? f1 : f0;
+          const uint32_t a = nv_codes8(v, fb, false, uint4{}, uint4{});
+          const uint32_t b = nv_codes8(v + 8, fb, false, uint4{}, uint4{});
+          *reinterpret_cast<uint2*>(p.col_codes + cc * (R >> 1) + (rr >> 1)) = make_uint2(a, b);
+          const int64_t off = p.col_gemm ? sf_gemm_offset(cc, kb, p.col_kt) : cc * (R >> 4) + kb;
+          p.col_sf[off] = (uint8_t)tile_s[tid];
+        }
       }
     }
     return;
