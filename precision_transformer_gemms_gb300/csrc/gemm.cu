@@ -51,7 +51,8 @@ struct Cfg {
   static constexpr int kSmem = kStages * kStage + 1024 /*align slack*/ + 512 /*barriers*/;
   static constexpr int kSfaCols = kSfAtoms * 4;
   static constexpr int kSfbCols = kSfAtoms * 4 * (BN / 128);
-  static constexpr int kSlots = SFST ? 5 : 1;  // TMEM scale slots (SFST: written by the scale warps)
+  // SFST: one TMEM scale slot per stage, written by the scale warps
+  static constexpr int kSlots = SFST ? kStages : 1;
   static constexpr int kCols = NACC * BN + kSlots * (kSfaCols + kSfbCols);
   static constexpr int kTmemCols = kCols <= 32 ? 32 : kCols <= 64 ? 64 : kCols <= 128 ? 128 : kCols <= 256 ? 256 : 512;
   static_assert(kCols <= 512, "TMEM holds 512 columns");
@@ -119,9 +120,7 @@ __global__ void __launch_bounds__(kThreadsGemm + (SFST ? 32 * kSfWarps : 0))
   uint64_t* empty = full + S;
   uint64_t* acc_full = empty + S;
   uint64_t* acc_empty = acc_full + NACC;
-  uint64_t* sf_full = acc_empty + NACC;     // [kSlots] (SFST)
-  uint64_t* sf_empty = sf_full + CF::kSlots;
-  uint64_t* sfd = sf_empty + CF::kSlots;    // [S] (SFST): the stage's scale atoms landed
+  uint64_t* sfd = acc_empty + NACC;         // [S] (SFST): the stage's scale atoms landed
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sfd + S);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -130,17 +129,16 @@ __global__ void __launch_bounds__(kThreadsGemm + (SFST ? 32 * kSfWarps : 0))
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], SFST ? 1 + kSfWarps : 1);  // MMA commit (+ the scale warps' reads)
+      // SFST: the stage is full once its A/B landed and the four scale warps
+      // have written its scale slot; the MMA commit alone empties it (the
+      // scale warps have read the stage's scale atoms before they arrive).
+      mbar_init(&full[s], SFST ? 1 + kSfWarps : 1);
+      mbar_init(&empty[s], 1);
       mbar_init(&sfd[s], 1);
     }
     for (int a = 0; a < NACC; ++a) {
       mbar_init(&acc_full[a], 1);
       mbar_init(&acc_empty[a], kEpiWarps);  // one arrive per epilogue warp
-    }
-    for (int i = 0; i < CF::kSlots; ++i) {
-      mbar_init(&sf_full[i], kSfWarps);
-      mbar_init(&sf_empty[i], 1);
     }
     *abort_flag = 0;
     fence_barrier_init();
@@ -203,7 +201,7 @@ __global__ void __launch_bounds__(kThreadsGemm + (SFST ? 32 * kSfWarps : 0))
       const uint32_t kHiSf = (uint32_t)(smem_desc(0, 0, 128, 0) >> 32);
       const uint32_t a0 = kLoSw | (smem_u32(sA) >> 4), b0 = kLoSw | (smem_u32(sB) >> 4);
       const uint32_t fa0 = smem_u32(sSfa) >> 4, fb0 = smem_u32(sSfb) >> 4;
-      uint32_t s = 0, ph = 0, lt = 0, slot = 0, sph = 0;
+      uint32_t s = 0, ph = 0, lt = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++lt) {
         const uint32_t a = lt % NACC, aph = (lt / NACC) & 1u;
@@ -212,9 +210,6 @@ __global__ void __launch_bounds__(kThreadsGemm + (SFST ? 32 * kSfWarps : 0))
         const uint32_t tmem_d = tmem_base + a * BN;
         for (int kt = 0; kt < g.num_k; ++kt) {
           if (!(ok = mbar_wait_bounded(&full[s], ph, abort_flag, &g_device_error))) break;
-          if constexpr (SFST) {
-            if (!(ok = mbar_wait_bounded(&sf_full[slot], sph, abort_flag, &g_device_error))) break;
-          }
           tc_fence_after();
           const uint32_t alo = a0 + s * (CF::kA >> 4), blo = b0 + s * (CF::kB >> 4);
           const uint32_t falo = fa0 + s * (CF::kSfa >> 4), fblo = fb0 + s * (CF::kSfb >> 4);
@@ -233,7 +228,7 @@ __global__ void __launch_bounds__(kThreadsGemm + (SFST ? 32 * kSfWarps : 0))
             } else if constexpr (KIND == kKindMXF8) {
               mma_bs<KIND>(tmem_d, ad, bd, g.idesc | ((uint32_t)j << 4) | ((uint32_t)j << 29), tmem_sfa, tmem_sfb, acc);
             } else if constexpr (SFST) {
-              const uint32_t base = tmem_sfa + slot * (CF::kSfaCols + CF::kSfbCols);
+              const uint32_t base = tmem_sfa + s * (CF::kSfaCols + CF::kSfbCols);  // the stage's slot
               mma_bs<KIND>(tmem_d, ad, bd, g.idesc, base + 4 * j, base + CF::kSfaCols + 4 * (BN / 128) * j, acc);
             } else {
               tmem_cp_sf(tmem_sfa + 4 * j, ((uint64_t)kHiSf << 32) | (falo + j * 32));
@@ -244,10 +239,6 @@ __global__ void __launch_bounds__(kThreadsGemm + (SFST ? 32 * kSfWarps : 0))
             }
           }
           tc_commit(&empty[s]);
-          if constexpr (SFST) {
-            tc_commit(&sf_empty[slot]);
-            if (++slot == (uint32_t)CF::kSlots) { slot = 0; sph ^= 1u; }
-          }
           if (++s == (uint32_t)S) { s = 0; ph ^= 1u; }
         }
         if (ok) tc_commit(&acc_full[a]);
@@ -255,17 +246,18 @@ __global__ void __launch_bounds__(kThreadsGemm + (SFST ? 32 * kSfWarps : 0))
     }
   } else if (SFST && warp >= 2 + kEpiWarps) {
     // ------------------------------------------------------------ scale warps (NVFP4)
-    // Per k-step: this warp's lane quarter of the step's 12 scale atoms goes from
-    // shared memory into a TMEM slot with tcgen05.st (replicated in every
-    // quarter); the slot is handed to the MMA warp and the stage released.
+    // Per k-step: once the stage's previous MMAs are done (its TMEM scale slot
+    // is free), this warp's lane quarter of the step's 12 scale atoms goes
+    // from shared memory into the slot with tcgen05.st (replicated in every
+    // quarter), and the warp arrives on the stage's full barrier.
     const int q = warp & 3;
     const uint32_t lanes = (uint32_t)(q * 32) << 16;
-    uint32_t s = 0, ph = 0, slot = 0, sph = 0;
+    uint32_t s = 0, ph = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
       for (int kt = 0; kt < g.num_k; ++kt) {
         if (!(ok = mbar_wait_bounded(&sfd[s], ph, abort_flag, &g_device_error))) break;
-        if (!(ok = mbar_wait_bounded(&sf_empty[slot], sph ^ 1u, abort_flag, &g_device_error))) break;
+        if (!(ok = mbar_wait_bounded(&empty[s], ph ^ 1u, abort_flag, &g_device_error))) break;  // slot free
         __syncwarp();
         tc_fence_after();
         const uint4* fa = reinterpret_cast<const uint4*>(sSfa + s * CF::kSfa) + lane;  // atom j line `lane`
@@ -282,7 +274,7 @@ __global__ void __launch_bounds__(kThreadsGemm + (SFST ? 32 * kSfWarps : 0))
             vb[c] = y.x; vb[c + 1] = y.y; vb[c + 2] = y.z; vb[c + 3] = y.w;
           }
         }
-        const uint32_t base = tmem_base + NACC * BN + slot * (CF::kSfaCols + CF::kSfbCols) + lanes;
+        const uint32_t base = tmem_base + NACC * BN + s * (CF::kSfaCols + CF::kSfbCols) + lanes;
         tmem_st16(base, va);
         if constexpr (BN == 256) {
           tmem_st32(base + CF::kSfaCols, vb);
@@ -295,11 +287,7 @@ __global__ void __launch_bounds__(kThreadsGemm + (SFST ? 32 * kSfWarps : 0))
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&sf_full[slot]);
-          mbar_arrive(&empty[s]);
-        }
-        if (++slot == (uint32_t)CF::kSlots) { slot = 0; sph ^= 1u; }
+        if (lane == 0) mbar_arrive(&full[s]);
         if (++s == (uint32_t)S) { s = 0; ph ^= 1u; }
       }
     }
@@ -492,7 +480,7 @@ struct PairCfg {
   static constexpr int kNacc = kSfAtoms == 0 ? 2 : 1;
   static constexpr int kSfaCols = kSfAtoms * 4;
   static constexpr int kSfbCols = kSfAtoms * 4 * kSfbGroups;
-  static constexpr int kSlots = SFST ? 5 : 1;
+  static constexpr int kSlots = SFST ? kStages : 1;  // one TMEM scale slot per stage
   static_assert(kNacc * kPairBN + kSlots * (kSfaCols + kSfbCols) <= 512, "TMEM holds 512 columns");
 };
 
@@ -532,9 +520,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm + (SFST
   uint64_t* empty = full + S;
   uint64_t* acc_full = empty + S;
   uint64_t* acc_empty = acc_full + NACC;
-  uint64_t* sf_full = acc_empty + NACC;  // [kSlots] (SFST): scale warps of both CTAs
-  uint64_t* sf_empty = sf_full + PC::kSlots;
-  uint64_t* sfd = sf_empty + PC::kSlots;  // [S] (SFST): this CTA's scale atoms landed
+  uint64_t* sfd = acc_empty + NACC;      // [S] (SFST): this CTA's scale atoms landed
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sfd + S);
   uint32_t* peer_base = tmem_slot + 1;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 2);
@@ -547,16 +533,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm + (SFST
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], SFST ? 1 + kSfWarps : 1);  // MMA commit (+ this CTA's scale warps)
+      // SFST: full once the pair's A/B landed and the scale warps of both CTAs
+      // have written the stage's scale slot; the MMA commit alone empties it.
+      mbar_init(&full[s], SFST ? 1 + 2 * kSfWarps : 1);
+      mbar_init(&empty[s], 1);
     }
     for (int a = 0; a < NACC; ++a) {
       mbar_init(&acc_full[a], 1);
       mbar_init(&acc_empty[a], 2 * kEpiWarps);  // the epilogue warps of both CTAs
-    }
-    for (int i = 0; i < PC::kSlots; ++i) {
-      mbar_init(&sf_full[i], 2 * kSfWarps);  // the scale warps of both CTAs
-      mbar_init(&sf_empty[i], 1);
     }
     for (int s = 0; s < S; ++s) mbar_init(&sfd[s], 1);
     *abort_flag = 0;
@@ -579,7 +563,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm + (SFST
   const bool run = *abort_flag == 0;
   const uint32_t full_leader = mapa_shared(smem_u32(full), 0);
   const uint32_t acc_empty_leader = mapa_shared(smem_u32(acc_empty), 0);
-  const uint32_t sf_full_leader = mapa_shared(smem_u32(sf_full), 0);
   const uint32_t tmem_sfa = tmem_base + NACC * kPairBN;
   const uint32_t tmem_sfb = tmem_sfa + PC::kSfaCols;
 
@@ -631,7 +614,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm + (SFST
       const uint32_t a0 = (uint32_t)smem_desc(smem_u32(sA), 16, 1024, 2);
       const uint32_t b0 = (uint32_t)smem_desc(smem_u32(sB), 16, 1024, 2);
       const uint32_t fa0 = smem_u32(sSfa) >> 4, fb0 = smem_u32(sSfb) >> 4;
-      uint32_t s = 0, ph = 0, lt = 0, slot = 0, sph = 0;
+      uint32_t s = 0, ph = 0, lt = 0;
       bool ok = true;
       for (int t = pair; t < total && ok; t += npairs, ++lt) {
         const uint32_t a = lt % NACC, aph = (lt / NACC) & 1u;
@@ -640,9 +623,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm + (SFST
         const uint32_t tmem_d = tmem_base + a * kPairBN;
         for (int kt = 0; kt < g.num_k; ++kt) {
           if (!(ok = mbar_wait_bounded(&full[s], ph, abort_flag, &g_device_error))) break;
-          if constexpr (SFST) {
-            if (!(ok = mbar_wait_bounded(&sf_full[slot], sph, abort_flag, &g_device_error))) break;
-          }
           tc_fence_after();
           const uint32_t alo = a0 + s * (PC::kA >> 4), blo = b0 + s * (PC::kB >> 4);
           const uint32_t falo = fa0 + s * (PC::kSfa >> 4), fblo = fb0 + s * (PC::kSfb >> 4);
@@ -663,7 +643,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm + (SFST
               mma_pair_bs<KIND>(tmem_d, ad, bd, g.idesc | ((uint32_t)j << 4) | ((uint32_t)j << 29), tmem_sfa, tmem_sfb,
                                 acc);
             } else if constexpr (SFST) {
-              const uint32_t base = tmem_sfa + slot * (PC::kSfaCols + PC::kSfbCols);
+              const uint32_t base = tmem_sfa + s * (PC::kSfaCols + PC::kSfbCols);  // the stage's slot
               mma_pair_bs<KIND>(tmem_d, ad, bd, g.idesc, base + 4 * j, base + PC::kSfaCols + 4 * PC::kSfbGroups * j, acc);
             } else {
               tmem_cp_sf_pair(tmem_sfa + 4 * j, ((uint64_t)kHiSf << 32) | (falo + j * 32));
@@ -675,10 +655,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm + (SFST
             }
           }
           tc_commit_pair(&empty[s], 0x3);
-          if constexpr (SFST) {
-            tc_commit_pair(&sf_empty[slot], 0x3);
-            if (++slot == (uint32_t)PC::kSlots) { slot = 0; sph ^= 1u; }
-          }
           if (++s == (uint32_t)S) { s = 0; ph ^= 1u; }
         }
         if (ok) tc_commit_pair(&acc_full[a], 0x3);
@@ -690,12 +666,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm + (SFST
     // scale warps report to the even CTA's slot barrier
     const int q = warp & 3;
     const uint32_t lanes = (uint32_t)(q * 32) << 16;
-    uint32_t s = 0, ph = 0, slot = 0, sph = 0;
+    uint32_t s = 0, ph = 0;
     bool ok = true;
     for (int t = pair; t < total && ok; t += npairs) {
       for (int kt = 0; kt < g.num_k; ++kt) {
         if (!(ok = mbar_wait_bounded(&sfd[s], ph, abort_flag, &g_device_error))) break;  // own scale atoms
-        if (!(ok = mbar_wait_bounded(&sf_empty[slot], sph ^ 1u, abort_flag, &g_device_error))) break;
+        if (!(ok = mbar_wait_bounded(&empty[s], ph ^ 1u, abort_flag, &g_device_error))) break;  // slot free
         __syncwarp();
         tc_fence_after();
         const uint4* fa = reinterpret_cast<const uint4*>(sSfa + s * PC::kSfa) + lane;
@@ -712,17 +688,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm + (SFST
             vb[c] = y.x; vb[c + 1] = y.y; vb[c + 2] = y.z; vb[c + 3] = y.w;
           }
         }
-        const uint32_t base = tmem_sfa + slot * (PC::kSfaCols + PC::kSfbCols) + lanes;
+        const uint32_t base = tmem_sfa + s * (PC::kSfaCols + PC::kSfbCols) + lanes;
         tmem_st16(base, va);
         tmem_st32(base + PC::kSfaCols, vb);
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) {
-          if (leader) mbar_arrive(&sf_full[slot]); else mbar_arrive_remote_relaxed(sf_full_leader + 8 * slot);
-          mbar_arrive(&empty[s]);
+          if (leader) mbar_arrive(&full[s]); else mbar_arrive_remote_relaxed(full_leader + 8 * s);
         }
-        if (++slot == (uint32_t)PC::kSlots) { slot = 0; sph ^= 1u; }
         if (++s == (uint32_t)S) { s = 0; ph ^= 1u; }
       }
     }
