@@ -72,6 +72,7 @@ struct GemmArgs {
   void* c;
   int64_t M, N, K;
   int c_fp32;
+  int c_tma;             // bf16 C written by TMA tile stores (pair kernel; N % 8 == 0)
   const float* alpha_a;  // per-tensor factors (may be NULL)
   const float* alpha_b;
   uint32_t idesc;
@@ -427,6 +428,12 @@ uint32_t idesc_block_scaled(uint32_t afmt, uint32_t bfmt, uint32_t e8m0, int n) 
 
 int g_sms = 0;
 
+// An environment switch set to something other than "0" (read per call).
+bool getenv_flag(const char* name) {
+  const char* e = getenv(name);
+  return e && e[0] && e[0] != '0';
+}
+
 template <int KIND, int BN, int NACC, bool SFST = false>
 lpq_status run(const CUtensorMap& ta, const CUtensorMap& tb, GemmArgs g, cudaStream_t s) {
   using CF = Cfg<KIND, BN, NACC, SFST>;
@@ -475,8 +482,14 @@ struct PairCfg {
   static constexpr int kSfa = kSfAtoms * 512;
   static constexpr int kSfb = kSfAtoms * 512 * kSfbGroups;
   static constexpr int kStage = kA + kB + kSfa + kSfb;
-  static constexpr int kStages = (220 * 1024) / kStage > 8 ? 8 : (220 * 1024) / kStage;
-  static constexpr int kSmem = kStages * kStage + 1024 + 512;
+  // Epilogue staging for TMA stores: per epilogue warp one 32 x 64 bf16 tile
+  // (128-byte rows, 128-byte swizzle).  The stage ring takes what is left of
+  // the 227 KB a CTA can have.
+  static constexpr int kStgWarp = 32 * 128;
+  static constexpr int kStg = kEpiWarps * kStgWarp;
+  static constexpr int kRing = 232448 - 1024 /*align*/ - 512 /*barriers*/ - kStg - 1024 /*staging align*/;
+  static constexpr int kStages = kRing / kStage > 8 ? 8 : kRing / kStage;
+  static constexpr int kSmem = kStages * kStage + 1024 + 512 + kStg + 1024;
   static constexpr int kNacc = kSfAtoms == 0 ? 2 : 1;
   static constexpr int kSfaCols = kSfAtoms * 4;
   static constexpr int kSfbCols = kSfAtoms * 4 * kSfbGroups;
@@ -507,7 +520,7 @@ template <int KIND, bool kSfbFull, bool SFST>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm + (SFST ? 32 * kSfWarps : 0))
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmSfa, const __grid_constant__ CUtensorMap tmSfb,
-                     const GemmArgs g) {
+                     const __grid_constant__ CUtensorMap tmC, const GemmArgs g) {
   using PC = PairCfg<KIND, kSfbFull, SFST>;
   constexpr int S = PC::kStages, NACC = PC::kNacc;
   extern __shared__ uint8_t smem_raw[];
@@ -516,7 +529,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm + (SFST
   uint8_t* sB = sA + S * PC::kA;
   uint8_t* sSfa = sB + S * PC::kB;
   uint8_t* sSfb = sSfa + S * PC::kSfa;
-  uint64_t* full = reinterpret_cast<uint64_t*>(sSfb + S * PC::kSfb);
+  uint8_t* stage_c = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(sSfb + S * PC::kSfb) + 1023) & ~uintptr_t(1023));  // epilogue staging
+  uint64_t* full = reinterpret_cast<uint64_t*>(stage_c + PC::kStg);
   uint64_t* empty = full + S;
   uint64_t* acc_full = empty + S;
   uint64_t* acc_empty = acc_full + NACC;
@@ -738,6 +753,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm + (SFST
         if (lane == 0) {
           if (leader) mbar_arrive(&acc_empty[a]); else mbar_arrive_remote_relaxed(acc_empty_leader + 8 * a);
         }
+        if (g.c_tma) {
+          // The warp's 32 rows x 128 columns leave as two TMA stores of 32 x 64
+          // tiles staged in shared memory (128-byte swizzle: 16-byte chunk i of
+          // row r at chunk position i ^ (r & 7)); the stores clip at M and N.
+          uint8_t* stg = stage_c + (warp - 2) * PC::kStgWarp;
+          const int32_t y = mt * 256 + (int32_t)rank * 128 + q * 32;
+#pragma unroll
+          for (int ch = 0; ch < 2; ++ch) {
+            if (lane == 0) bulk_wait_group_read0();  // the previous store has read the buffer
+            __syncwarp();
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              *reinterpret_cast<uint4*>(stg + lane * 128 + ((i ^ (lane & 7)) << 4)) =
+                  make_uint4(pk[32 * ch + 4 * i], pk[32 * ch + 4 * i + 1], pk[32 * ch + 4 * i + 2],
+                             pk[32 * ch + 4 * i + 3]);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&tmC, stg, (int32_t)(c0 + ch * 64), y);
+              bulk_commit_group();
+            }
+          }
+          continue;
+        }
         if (row < g.M && ncols > 0) {
           __nv_bfloat16* out = static_cast<__nv_bfloat16*>(g.c) + row * g.N + c0;
           if (vec_ok && ncols >= HALF) {
@@ -779,6 +818,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm + (SFST
         }
       }
     }
+    if (lane == 0) bulk_wait_group0();  // this warp's TMA stores complete before the CTA exits
+    __syncwarp();
   }
   tc_fence_before();
   cluster_sync_all();  // no CTA leaves while its peer may still signal its barriers
@@ -825,8 +866,17 @@ lpq_status run_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensor
   g.tiles_m = (int)tm;
   g.tiles_n = (int)tn;
   const int pairs = (int)std::min<int64_t>(tm * tn, g_sms / 2);
+  // bf16 C leaves through TMA tile stores (32 x 64 boxes) when its row pitch
+  // allows a tensor map (N % 8 == 0); otherwise the epilogue stores directly.
+  CUtensorMap tc = ta;
+  g.c_tma = 0;
+  if (!g.c_fp32 && g.N % 8 == 0 && !getenv_flag("LPQ_GEMM_DIRECT_STORE")) {
+    lpq_status st = make_map(&tc, g.c, true, g.N, g.M, g.N * 2, 64, 32);
+    if (st != LPQ_OK) return st;
+    g.c_tma = 1;
+  }
   gemm_pair_kernel<KIND, kSfbFull, SFST>
-      <<<2 * pairs, kThreadsGemm + (SFST ? 32 * kSfWarps : 0), PC::kSmem, s>>>(ta, tb, tsa, tsb, g);
+      <<<2 * pairs, kThreadsGemm + (SFST ? 32 * kSfWarps : 0), PC::kSmem, s>>>(ta, tb, tsa, tsb, tc, g);
   return cuda_check(cudaGetLastError(), "pair gemm launch");
 }
 

@@ -34,7 +34,7 @@ def check(a, b, M, N, K, out_fp32, layout=lpq.FPROP):
     assert nbad == 0, f"{nbad} elements outside the gate (worst {worst:.3g}x)"
 
 
-@pytest.mark.parametrize("path", ["single", "pair", "single_cp", "single_bn128"])
+@pytest.mark.parametrize("path", ["single", "pair", "pair_direct", "single_cp", "single_bn128"])
 @pytest.mark.parametrize("out_fp32", [True, False])
 @pytest.mark.parametrize("shape", SHAPES)
 @pytest.mark.parametrize("fmts", [(lpq.BF16, lpq.BF16), (lpq.FP8_E4M3, lpq.FP8_E4M3), (lpq.FP8_E5M2, lpq.FP8_E4M3),
@@ -43,12 +43,14 @@ def test_gemm_parity(fmts, shape, out_fp32, path, monkeypatch):
     """Every kernel path: one CTA per 128 x 256 tile (NVFP4 scales stored into
     TMEM by scale warps, or copied by the MMA thread: single_cp), one CTA per
     128 x 128 tile with two accumulators (block-scaled kinds: single_bn128), and
-    CTA pairs (cta_group::2) per 256 x 256 tile."""
+    CTA pairs (cta_group::2) per 256 x 256 tile, whose bf16 output leaves
+    through TMA tile stores (pair) or direct stores (pair_direct)."""
     if path == "single_cp" and fmts[0] not in (lpq.NVFP4,):
         pytest.skip("scale-copy variant exists for NVFP4 only")
     if path == "single_bn128" and fmts[0] not in (lpq.NVFP4, lpq.MXFP8):
         pytest.skip("128-wide tiles exist for the block-scaled kinds only")
-    monkeypatch.setenv("LPQ_GEMM_PAIR", "1" if path == "pair" else "0")
+    monkeypatch.setenv("LPQ_GEMM_PAIR", "1" if path.startswith("pair") else "0")
+    monkeypatch.setenv("LPQ_GEMM_DIRECT_STORE", "1" if path == "pair_direct" else "0")
     monkeypatch.setenv("LPQ_GEMM_SFCP", "1" if path == "single_cp" else "0")
     monkeypatch.setenv("LPQ_GEMM_BN", "128" if path == "single_bn128" else "256")
     M, K, N = shape
@@ -206,3 +208,14 @@ def test_mma_peak_modes_run(kind, mode):
     assert lpq.device_status() == 0
     nominal = {"bf16": 2250, "fp8": 4500, "mxfp8": 4500, "nvfp4": 13500}[kind]
     assert 0 < rate < 1.2 * nominal
+
+
+@pytest.mark.parametrize("fmts", [(lpq.BF16, lpq.BF16), (lpq.FP8_E4M3, lpq.FP8_E4M3), (lpq.MXFP8, lpq.MXFP8)])
+def test_pair_gemm_ragged_n_direct_stores(fmts, monkeypatch):
+    """N not a multiple of 8: no tensor map fits the output rows, so the pair
+    kernel's epilogue stores directly (bf16 and FP32 outputs)."""
+    monkeypatch.setenv("LPQ_GEMM_PAIR", "1")
+    M, K, N = 512, 256, 100
+    a, b = quantize_pair(*fmts, M, K, N, seed=11)
+    for out_fp32 in (False, True):
+        check(a, b, M, N, K, out_fp32)
