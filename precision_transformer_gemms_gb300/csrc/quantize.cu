@@ -142,7 +142,7 @@ __device__ __forceinline__ float nv_ts_dec(const float* amax) {
 // registers of the others): bit 0 stochastic rounding, bit 1 RHT of the
 // column-wise copy.
 template <int KIND, bool kE5M2, int NVO = 0>
-__global__ void __launch_bounds__(kThreads, KIND == QK_NV2D ? 5 : (KIND != QK_NV ? 1 : (NVO == 0 ? 6 : 5))) quant_tile_kernel(const QParams p) {
+__global__ void __launch_bounds__(kThreads, KIND == QK_NV2D ? 5 : (KIND != QK_NV ? 1 : (NVO == 0 ? 6 : (NVO >= 2 ? 4 : 5)))) quant_tile_kernel(const QParams p) {
   constexpr bool kSR = (NVO & 1) != 0, kRHT = (NVO & 2) != 0;
   constexpr int TR = (KIND == QK_BLK1 || KIND == QK_BLK128) ? 128 : 64;
   __shared__ __align__(16) uint16_t tile[TR][kTC];
@@ -197,6 +197,55 @@ __global__ void __launch_bounds__(kThreads, KIND == QK_NV2D ? 5 : (KIND != QK_NV
   float local_amax = 0.f;
   // all of this thread's 16-byte loads first, so they are in flight together
   uint4 vbuf[TR / 16];
+  if constexpr (KIND == QK_NV) {
+    // NVFP4 1D: one thread per 16-value block (8 threads per 128-column row,
+    // 32 rows a pass), so each block's scale is computed once, without a
+    // shuffle, and the stochastic-rounding words come from four independent
+    // Philox blocks.
+    const int wr = t >> 3, wc = (t & 7) * 16;
+    const bool wcol_ok = c0 + wc < C;  // C is a multiple of 16: whole blocks
+#pragma unroll
+    for (int it = 0; it < TR / 32; ++it) {
+      const int64_t r = r0 + it * 32 + wr;
+      const bool ok = wcol_ok && r < R;
+      const uint16_t* src = p.x + r * C + c0 + wc;
+      vbuf[2 * it] = ok ? ld_stream(src) : make_uint4(0u, 0u, 0u, 0u);
+      vbuf[2 * it + 1] = ok ? ld_stream(src + 8) : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int it = 0; it < TR / 32; ++it) {
+      const int rl = it * 32 + wr;
+      const int64_t r = r0 + rl;
+      const bool ok = wcol_ok && r < R;
+      if (kNeedTile) {
+        *reinterpret_cast<uint4*>(&tile[rl][wc]) = vbuf[2 * it];
+        *reinterpret_cast<uint4*>(&tile[rl][wc + 8]) = vbuf[2 * it + 1];
+      }
+      if (!p.row_codes) continue;
+      float f[16];
+      unpack8(vbuf[2 * it], f);
+      unpack8(vbuf[2 * it + 1], f + 8);
+      float m = 0.f;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) m = absmax_acc(m, f[i]);
+      const uint32_t S = nv_block_scale(m, s_enc_row);
+      const float fb = fb_tab[0][S];
+      uint4 w[4] = {uint4{}, uint4{}, uint4{}, uint4{}};
+      if constexpr (kSR) {
+        const uint64_t g = (p.ctr_off + (uint64_t)(r * C + c0 + wc)) >> 2;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) w[j] = keys.words(g + j, 0u);
+      }
+      const uint32_t q0 = nv_codes8(f, fb, kSR, w[0], w[1]);
+      const uint32_t q1 = nv_codes8(f + 8, fb, kSR, w[2], w[3]);
+      if (ok) {
+        *reinterpret_cast<uint2*>(p.row_codes + r * (C >> 1) + ((c0 + wc) >> 1)) = make_uint2(q0, q1);
+        const int64_t kb = (c0 + wc) >> 4;
+        const int64_t off = p.row_gemm ? sf_gemm_offset(r, kb, p.row_kt) : r * (C >> 4) + kb;
+        p.row_sf[off] = (uint8_t)S;
+      }
+    }
+  } else {
 #pragma unroll
   for (int it = 0; it < TR / 16; ++it) {
     const int64_t r = r0 + it * 16 + lr;
@@ -235,28 +284,6 @@ __global__ void __launch_bounds__(kThreads, KIND == QK_NV2D ? 5 : (KIND != QK_NV
           p.row_sf[off] = (uint8_t)(e + 127);
         }
       }
-    } else if constexpr (KIND == QK_NV) {
-      float m = 0.f;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) m = absmax_acc(m, f[i]);
-      m = warp_max_xor(m, 2);
-      const uint32_t S = nv_block_scale(m, s_enc_row);
-      const float fb = fb_tab[0][S];
-      uint4 w0 = make_uint4(0, 0, 0, 0), w1 = w0;
-      if constexpr (kSR) {
-        const uint64_t g = (p.ctr_off + (uint64_t)(r * C + c0 + lc)) >> 2;
-        w0 = keys.words(g, 0u);
-        w1 = keys.words(g + 1, 0u);
-      }
-      const uint32_t q = nv_codes8(f, fb, kSR, w0, w1);
-      if (ok) {
-        *reinterpret_cast<uint32_t*>(p.row_codes + r * (C >> 1) + ((c0 + lc) >> 1)) = q;
-        if ((t & 1) == 0) {
-          const int64_t kb = (c0 + lc) >> 4;
-          const int64_t off = p.row_gemm ? sf_gemm_offset(r, kb, p.row_kt) : r * (C >> 4) + kb;
-          p.row_sf[off] = (uint8_t)S;
-        }
-      }
     } else if constexpr (KIND == QK_BLK1) {
       float m = 0.f;
 #pragma unroll
@@ -277,6 +304,7 @@ __global__ void __launch_bounds__(kThreads, KIND == QK_NV2D ? 5 : (KIND != QK_NV
     }
   }
 
+  }  // load + row-wise copy, other kinds
   if constexpr (KIND == QK_FP8) {
     if (p.fused_amax0) {  // delayed scaling: amax measured in this pass
       float m = block_max(local_amax, red);
