@@ -76,7 +76,10 @@ enum {
   LPQ_ROWWISE = 1,     /* emit the row-wise copy [rows, cols] */
   LPQ_COLWISE = 2,     /* emit the column-wise copy [cols, rows] (re-blocked along rows) */
   LPQ_RHT_COLWISE = 4, /* NVFP4: 16-point random-sign Hadamard on the column-wise copy */
-  LPQ_STOCHASTIC = 8   /* NVFP4: stochastic rounding of the E2M1 codes (both copies) */
+  LPQ_STOCHASTIC = 8,  /* NVFP4: stochastic rounding of the E2M1 codes (both copies) */
+  LPQ_GIVEN_AMAX = 16  /* per-tensor FP8 (current scaling) and NVFP4: the views' amax fields
+                          already hold the amax to scale with (e.g. the MAX over all shards of a
+                          token-sharded tensor); no amax pass is run and they are left as given */
 };
 
 /* Scale-factor layouts of a copy. */
@@ -155,6 +158,15 @@ lpq_status lpq_copy_bytes(int32_t fmt, int64_t rows, int64_t cols, int32_t sf_la
  *                  Philox(key = (rht_seed, 0), counter = (0, 0, 2, 0)).
  *   out            views to fill; out->row used if LPQ_ROWWISE, out->col if
  *                  LPQ_COLWISE.  Each view's rows/cols/fmt must match.
+ *                  With LPQ_GIVEN_AMAX the amax of each requested view is an
+ *                  input (NVFP4: the row view's the raw amax, the column
+ *                  view's the amax of its own values, after the RHT when
+ *                  LPQ_RHT_COLWISE is set; FP8: the row view's, else the
+ *                  column view's, for both copies).  Quantizing the shards of
+ *                  a tensor with the MAX of their amaxes gives exactly the
+ *                  codes and scales of the whole tensor (for the row-wise
+ *                  copy with stochastic rounding, pass counter_offset =
+ *                  first row * cols).
  * Shape rules: cols a multiple of the row-wise block (16 NVFP4, 32 MXFP8, 128
  * FP8 block, 16 NVFP4_2D), rows a multiple of the column-wise block when
  * LPQ_COLWISE is set (same numbers; 128x128 needs neither rows nor cols beyond

@@ -139,7 +139,7 @@ lpq_status lpq_quantize(const void* x, int64_t rows, int64_t cols, int32_t fmt, 
   if (!valid_fmt(fmt)) return set_error(LPQ_ERR_INVALID_ARG, "unknown format %d", fmt);
   if (!out) return set_error(LPQ_ERR_INVALID_ARG, "out is NULL");
   if (rows < 0 || cols < 0) return set_error(LPQ_ERR_SHAPE, "negative dimension");
-  if (flags & ~uint32_t(LPQ_ROWWISE | LPQ_COLWISE | LPQ_RHT_COLWISE | LPQ_STOCHASTIC))
+  if (flags & ~uint32_t(LPQ_ROWWISE | LPQ_COLWISE | LPQ_RHT_COLWISE | LPQ_STOCHASTIC | LPQ_GIVEN_AMAX))
     return set_error(LPQ_ERR_INVALID_ARG, "unknown flag bits 0x%x", flags);
   const bool do_row = flags & LPQ_ROWWISE, do_col = flags & LPQ_COLWISE;
   if (!do_row && !do_col) return set_error(LPQ_ERR_INVALID_ARG, "neither LPQ_ROWWISE nor LPQ_COLWISE requested");
@@ -153,6 +153,8 @@ lpq_status lpq_quantize(const void* x, int64_t rows, int64_t cols, int32_t fmt, 
     return set_error(LPQ_ERR_INVALID_ARG, "scaling %d", scaling);
   if (!pt && scaling != LPQ_SCALING_CURRENT)
     return set_error(LPQ_ERR_UNSUPPORTED, "delayed scaling applies to per-tensor FP8 only");
+  if ((flags & LPQ_GIVEN_AMAX) && !((pt && scaling == LPQ_SCALING_CURRENT) || is_nvfp4(fmt)))
+    return set_error(LPQ_ERR_UNSUPPORTED, "LPQ_GIVEN_AMAX applies to current-scaled FP8 and NVFP4 only");
   if (pt && scaling == LPQ_SCALING_DELAYED) {
     if (!state || !state->scale || !state->scale_inv || !state->amax_history || !state->pos || state->len < 1 ||
         state->len > 1024)

@@ -586,6 +586,27 @@ __global__ void __launch_bounds__(kThreads) amax_kernel(const uint16_t* __restri
   }
 }
 
+// ---------------------------------------------------------------- tensor scales of an empty shard
+// With a given amax and nothing to quantize, the copies' FP32 tensor scales
+// still follow from it: 1 / (fmax / amax) for per-tensor FP8, amax / 2688 for
+// NVFP4 (1 when the amax is 0 or not finite).
+__global__ void given_amax_scales_kernel(int nvfp4, float fmax, const float* amax_row, const float* amax_col,
+                                         float* ts_row, float* ts_col) {
+  if (threadIdx.x != 0 || blockIdx.x != 0) return;
+  const float* am[2] = {amax_row, amax_col};
+  float* ts[2] = {ts_row, ts_col};
+  for (int i = 0; i < 2; ++i) {
+    if (!ts[i] || !am[i]) continue;
+    const float a = *am[i];
+    if (nvfp4) {
+      *ts[i] = finite_pos(a) ? __fdiv_rn(a, 2688.0f) : 1.0f;
+    } else {
+      const float scale = finite_pos(a) ? __fdiv_rn(fmax, a) : 1.0f;
+      *ts[i] = __fdiv_rn(1.0f, scale);
+    }
+  }
+}
+
 // ---------------------------------------------------------------- delayed-scaling update
 __global__ void scale_update_kernel(float* hist, int32_t* pos, float* scale, float* scale_inv, int32_t len,
                                     const float* amax, float fmax) {
@@ -659,6 +680,7 @@ lpq_status launch_quantize(const void* xv, int64_t R, int64_t C, int32_t fmt, in
                            uint64_t seed, uint64_t counter_offset, uint32_t rht_seed,
                            const lpq_delayed_state* state, lpq_qtensor* out, cudaStream_t s) {
   const bool do_row = flags & LPQ_ROWWISE, do_col = flags & LPQ_COLWISE;
+  const bool given = flags & LPQ_GIVEN_AMAX;  // the views' amax fields are inputs
   lpq_qview* rv = do_row ? &out->row : nullptr;
   lpq_qview* cv = do_col ? &out->col : nullptr;
   QParams p{};
@@ -703,6 +725,16 @@ lpq_status launch_quantize(const void* xv, int64_t R, int64_t C, int32_t fmt, in
 
   if (R == 0 || C == 0) {
     // Nothing to quantize; scalar outputs take their empty-tensor values.
+    if (given) {
+      const bool nv = fmt == LPQ_NVFP4 || fmt == LPQ_NVFP4_2D;
+      const float* a_row = rv ? rv->amax : nullptr;
+      const float* a_col = cv ? cv->amax : nullptr;
+      if (!nv && !a_row) a_row = a_col;  // FP8: one amax for both copies
+      if (!nv && !a_col) a_col = a_row;
+      given_amax_scales_kernel<<<1, 32, 0, s>>>(nv ? 1 : 0, fmt == LPQ_FP8_E5M2 ? 57344.0f : 448.0f, a_row, a_col,
+                                                rv ? rv->tensor_scale : nullptr, cv ? cv->tensor_scale : nullptr);
+      return cuda_check(cudaGetLastError(), "tensor scales from the given amax");
+    }
     if (fmt == LPQ_FP8_E4M3 || fmt == LPQ_FP8_E5M2 || fmt == LPQ_NVFP4 || fmt == LPQ_NVFP4_2D) {
       for (lpq_qview* v : {rv, cv}) {
         if (!v) continue;
@@ -734,6 +766,10 @@ lpq_status launch_quantize(const void* xv, int64_t R, int64_t C, int32_t fmt, in
       const bool e5 = fmt == LPQ_FP8_E5M2;
       float* a0 = rv ? rv->amax : cv->amax;
       float* a1 = (rv && cv) ? cv->amax : nullptr;
+      if (given) {  // current scaling with the amax the caller measured (e.g. over all shards)
+        p.amax_row = a0;
+        return e5 ? run_tile<QK_FP8, true>(p, s) : run_tile<QK_FP8, false>(p, s);
+      }
       if ((st = zero_f32(a0, s)) != LPQ_OK || (st = zero_f32(a1, s)) != LPQ_OK) return st;
       if (scaling == LPQ_SCALING_DELAYED) {
         p.delayed_scale = state->scale;
@@ -757,10 +793,12 @@ lpq_status launch_quantize(const void* xv, int64_t R, int64_t C, int32_t fmt, in
       float* raw0 = rv ? rv->amax : (rht ? nullptr : cv->amax);
       float* raw1 = (rv && cv && !rht) ? cv->amax : nullptr;
       float* rh = rht ? cv->amax : nullptr;
-      if ((st = zero_f32(raw0, s)) != LPQ_OK || (st = zero_f32(raw1, s)) != LPQ_OK ||
-          (st = zero_f32(rh, s)) != LPQ_OK)
-        return st;
-      if ((st = run_amax(p.x, R, C, raw0, raw1, rh, rht_seed, s)) != LPQ_OK) return st;
+      if (!given) {
+        if ((st = zero_f32(raw0, s)) != LPQ_OK || (st = zero_f32(raw1, s)) != LPQ_OK ||
+            (st = zero_f32(rh, s)) != LPQ_OK)
+          return st;
+        if ((st = run_amax(p.x, R, C, raw0, raw1, rh, rht_seed, s)) != LPQ_OK) return st;
+      }
       p.amax_row = rv ? rv->amax : nullptr;
       p.amax_col = cv ? cv->amax : nullptr;
       if (fmt == LPQ_NVFP4_2D) return run_tile<QK_NV2D, false>(p, s);

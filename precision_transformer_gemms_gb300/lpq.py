@@ -16,7 +16,7 @@ from . import build as _build
 OK, ERR_INVALID_ARG, ERR_SHAPE, ERR_ALIGN, ERR_UNSUPPORTED, ERR_ARCH, ERR_CUDA, ERR_TIMEOUT = range(8)
 BF16, FP8_E4M3, FP8_E5M2, MXFP8, NVFP4, NVFP4_2D, FP8_BLOCK_1x128, FP8_BLOCK_128x128 = range(8)
 SCALING_CURRENT, SCALING_DELAYED = 0, 1
-ROWWISE, COLWISE, RHT_COLWISE, STOCHASTIC = 1, 2, 4, 8
+ROWWISE, COLWISE, RHT_COLWISE, STOCHASTIC, GIVEN_AMAX = 1, 2, 4, 8, 16
 SF_PLAIN, SF_GEMM = 0, 1
 FPROP, DGRAD, WGRAD = 0, 1, 2
 

@@ -104,3 +104,11 @@ def test_mma_peak_validation():
     assert L.lpq_mma_peak(3, 0, 0, None) == lpq.ERR_INVALID_ARG      # iters
     assert L.lpq_mma_peak(3, 10, 6, None) == lpq.ERR_INVALID_ARG     # no such mode
     assert L.lpq_mma_peak(2, 10, 4, None) == lpq.ERR_INVALID_ARG     # modes 2..5 are NVFP4 only
+
+
+def test_given_amax_validation():
+    """LPQ_GIVEN_AMAX applies to current-scaled per-tensor FP8 and NVFP4 only."""
+    assert _quantize_raw(None, 4, 32, lpq.MXFP8, lpq.ROWWISE | lpq.GIVEN_AMAX) == lpq.ERR_UNSUPPORTED
+    assert _quantize_raw(None, 4, 128, lpq.FP8_BLOCK_1x128, lpq.ROWWISE | lpq.GIVEN_AMAX) == lpq.ERR_UNSUPPORTED
+    assert _quantize_raw(None, 4, 32, lpq.FP8_E4M3, lpq.ROWWISE | lpq.GIVEN_AMAX, scaling=1) == lpq.ERR_UNSUPPORTED
+    assert _quantize_raw(None, 4, 32, lpq.NVFP4, lpq.ROWWISE | 32) == lpq.ERR_INVALID_ARG  # unknown bit
