@@ -57,7 +57,7 @@ def parse():
     p.add_argument("--sequence_length", type=int, default=512)
     p.add_argument("--seed", type=int, default=0)
     p.add_argument("-o", "--output", default=None, help="write the per-GEMM table as JSON here")
-    p.add_argument("--workload", choices=["layer", "ksweep", "drift"], default="layer",
+    p.add_argument("--workload", choices=["layer", "ksweep", "drift", "report"], default="layer",
                    help="layer: the contract line; ksweep / drift: the K-sweep and the FP8 drift runs")
     p.add_argument("--verify", action="store_true", help="drift: compare every step with the oracle")
     p.add_argument("--mma-peaks", action="store_true",
@@ -522,10 +522,13 @@ def run_lpq(args, rank, world, local):
                 del layer.bufs[key]
             torch.cuda.empty_cache()
         if "bf16" in recipes:
+            # BF16 does the same work in both modes: the faster run is the baseline
+            b = min(recipes["bf16"]["prequant_ms_per_layer"], recipes["bf16"]["autocast_ms_per_layer"])
+            recipes["bf16"]["baseline_ms_per_layer"] = b
             for r, res in recipes.items():
                 for mode in ("autocast", "prequant", "fused"):
                     if f"{mode}_ms_per_layer" in res:
-                        res[f"{mode}_speedup_vs_bf16"] = recipes["bf16"]["prequant_ms_per_layer"] / res[f"{mode}_ms_per_layer"]
+                        res[f"{mode}_speedup_vs_bf16"] = b / res[f"{mode}_ms_per_layer"]
 
     # e2e: every step copies its bf16 inputs from pinned host memory and its
     # outputs back to pinned host memory.  Copies run on their own streams,
@@ -773,6 +776,80 @@ def run_drift(args):
     print(json.dumps({"workload": f"FP8 drift, attention-out M={M} K=N={K}, 20 steps", "results": res}), flush=True)
 
 
+def report_tables(per, shapes_list, linears):
+    """Tables of the speed-up analysis from per-GEMM times: per[recipe][mode][gemm] = ms."""
+    shapes = {n: (m, k, nn) for n, _, m, k, nn in shapes_list}
+    names = [n for n, *_ in shapes_list]
+    # BF16 does the same work in both modes; the faster of its two runs is the
+    # baseline (the run order can cost a few percent under the power cap).
+    base = ({n: min(per["bf16"]["autocast"][n], per["bf16"]["prequant"][n]) for n in per["bf16"]["prequant"]}
+            if "bf16" in per else None)
+    out = {"workload": "speed-up analysis, CodonFM-5B layer (12 GEMMs)", "unit": "ms", "per_gemm": per}
+    if base:
+        out["speedup_vs_bf16"] = {r: {m: {n: base[n] / per[r][m][n] for n in names} for m in per[r]} for r in per}
+        out["below_bf16"] = [f"{r}/{m}/{n}" for r in per for m in per[r] for n in names
+                             if r != "bf16" and base[n] / per[r][m][n] < 1.0]
+    if "nvfp4" in per and "mxfp8" in per:
+        fprop = [n for n in names if n.endswith("_fprop")]
+        ratios = {}
+        for m in ("autocast", "prequant"):
+            ratios[m] = {n: per["mxfp8"][m][n] / per["nvfp4"][m][n] for n in fprop}
+            ratios[m]["blended_fprop"] = (sum(per["mxfp8"][m][n] for n in fprop) /
+                                         sum(per["nvfp4"][m][n] for n in fprop))
+        out["nvfp4_vs_mxfp8"] = ratios
+    out["dgrad_vs_fprop"] = {r: {lin: per[r]["autocast"][f"{lin}_dgrad"] / per[r]["autocast"][f"{lin}_fprop"]
+                                 for lin in linears} for r in per}
+    # human-readable tables
+    lines = []
+    for m in ("autocast", "prequant"):
+        lines.append(f"== {m} (ms per GEMM; speed-up vs BF16 in parentheses)")
+        lines.append(f"{'GEMM':16s} {'m x k x n':22s} " + " ".join(f"{r:>16s}" for r in per))
+        for n in names:
+            mm, kk, nn = shapes[n]
+            cells = []
+            for r in per:
+                v = per[r][m][n]
+                cells.append(f"{v:8.3f} ({base[n] / v:4.2f}x)" if base else f"{v:16.3f}")
+            lines.append(f"{n:16s} {f'{mm}x{kk}x{nn}':22s} " + " ".join(f"{c:>16s}" for c in cells))
+    if "nvfp4_vs_mxfp8" in out:
+        for m, rr in out["nvfp4_vs_mxfp8"].items():
+            lines.append(f"NVFP4 vs MXFP8 Fprop ({m}): " + ", ".join(f"{n} {v:.2f}x" for n, v in rr.items()))
+    if base:
+        lines.append("below BF16: " + (", ".join(out["below_bf16"]) or "none"))
+    return out, lines
+
+
+def run_report(args):
+    """The speedup analysis of the pages' tool for the CodonFM-5B layer: every
+    GEMM shape timed separately (Fprop, Dgrad and Wgrad alike) under every
+    enabled precision, in autocast (quantization of the GEMM's two operand
+    copies + GEMM) and pre-quantize (GEMM only) mode.  Prints per-shape tables
+    and speed-ups vs BF16 on stderr, and one JSON line with the numbers:
+    per-shape NVFP4 / MXFP8 Fprop ratios and their blend, Dgrad vs Fprop per
+    linear, and the shapes whose speed-up vs BF16 is below 1 (not faster, or
+    a silent fallback, which lpq does not have)."""
+    import torch
+    torch.cuda.set_device(0)
+    layer = Layer(args, "cuda:0")
+    sweep = [r for r in RECIPES if not (args.no_fp8 and r == "mxfp8") and not (args.no_fp4 and r == "nvfp4")]
+    steps = max(3, args.steps // 4)
+    per = {}  # recipe -> mode -> gemm name -> ms
+    for r in sweep:
+        layer.prequantize(r)
+        per[r] = {}
+        for mode in ("autocast", "prequant"):
+            ac = (mode == "autocast" or r == "fp8_delayed") and r != "bf16"
+            _, events = time_steps(layer, r, ac, steps, 2, 1, per_kernel=True)
+            table = summarize_events(layer, events, steps)
+            per[r][mode] = {n: row["gemm_ms"] + row["quant_ms"] for n, row in table.items()}
+        for key in [k_ for k_ in layer.bufs if k_[0] == r]:
+            del layer.bufs[key]
+        torch.cuda.empty_cache()
+    out, lines = report_tables(per, layer.shapes, layer.linears)
+    print("\n".join(lines), file=sys.stderr, flush=True)
+    print(json.dumps(out), flush=True)
+
+
 def main():
     args = parse()
     if args.mma_peaks:
@@ -783,6 +860,9 @@ def main():
         return
     if args.workload == "drift":
         run_drift(args)
+        return
+    if args.workload == "report":
+        run_report(args)
         return
     rank, world, local = dist_setup(args)
     if args.impl == "reference":
