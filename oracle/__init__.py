@@ -14,10 +14,10 @@ import numpy as np
 from . import build as _build
 
 E4M3, E5M2, E2M1 = 0, 1, 2
-FMAX = {E4M3: 448.0, E5M2: 57344.0}
+FMAX = {E4M3: 448.0, E5M2: 57344.0, E2M1: 6.0}
 
 # Operand kinds of the FP64 GEMM (see OrcOperand in lpq_oracle.cpp).
-K_BF16, K_FP8_E4M3, K_FP8_E5M2, K_MXFP8, K_NVFP4, K_FP8_BLOCK = range(6)
+K_BF16, K_FP8_E4M3, K_FP8_E5M2, K_MXFP8, K_NVFP4, K_FP8_BLOCK, K_MXFP8_E5M2, K_MXFP4 = range(8)
 
 _lib = None
 
@@ -55,6 +55,9 @@ def lib():
         L.orc_fp8_pertensor.argtypes = [P, I64, I64, ctypes.c_int, P, P, P, P, P, P]
         L.orc_scale_update.argtypes = [P, ctypes.c_int32, P, P, P, F, F]
         L.orc_mxfp8.argtypes = [P, I64, I64, P, P, P, P]
+        L.orc_mx.argtypes = [P, I64, I64, ctypes.c_int, P, P, P, P]
+        L.orc_mx_exponent_fmt.restype = ctypes.c_int
+        L.orc_mx_exponent_fmt.argtypes = [F, ctypes.c_int]
         L.orc_nvfp4.argtypes = [P, I64, I64, ctypes.c_uint, U64, U64, U32, P, P, P, P, P, P, P, P]
         L.orc_fp8_block.argtypes = [P, I64, I64, ctypes.c_int, P, P, P, P]
         L.orc_gemm.argtypes = [ctypes.POINTER(_Operand), ctypes.POINTER(_Operand), I64, I64, I64, P, I64, P, P]
@@ -130,8 +133,11 @@ def sr_encode_e2m1(y, r):
     return lib().orc_sr_encode_e2m1(float(y), int(r))
 
 
-def mx_exponent(a):
-    return lib().orc_mx_exponent(float(a))
+def mx_exponent(a, fmt=E4M3):
+    """The MX block exponent: the smallest e with fmax(fmt) * 2^e >= a."""
+    if fmt == E4M3:
+        return lib().orc_mx_exponent(float(a))
+    return lib().orc_mx_exponent_fmt(float(a), fmt)
 
 
 def amax(x_bits):
@@ -182,6 +188,20 @@ def mxfp8(x_bits, rowwise=True, colwise=True):
     lib().orc_mxfp8(x.ctypes.data, R, C, _p(rc), _p(rs), _p(cc), _p(cs))
     out.update(row=rc, row_sf=rs, col=cc, col_sf=cs)
     return out
+
+
+def mx(x_bits, fmt, rowwise=True, colwise=True):
+    """MX quantization with element format fmt (E4M3, E5M2, or E2M1 packed two
+    per byte); returns dict(row, row_sf, col, col_sf) in plain layouts."""
+    x = _bits(x_bits)
+    R, C = x.shape
+    per = 2 if fmt == E2M1 else 1
+    rc = np.zeros((R, C // per), np.uint8) if rowwise else None
+    rs = np.zeros((R, C // 32), np.uint8) if rowwise else None
+    cc = np.zeros((C, R // per), np.uint8) if colwise else None
+    cs = np.zeros((C, R // 32), np.uint8) if colwise else None
+    lib().orc_mx(x.ctypes.data, R, C, fmt, _p(rc), _p(rs), _p(cc), _p(cs))
+    return dict(row=rc, row_sf=rs, col=cc, col_sf=cs)
 
 
 NV_ROW, NV_COL, NV_RHT, NV_SR, NV_2D = 1, 2, 4, 8, 16

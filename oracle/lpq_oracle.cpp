@@ -284,6 +284,21 @@ int mx_exponent(float a) {
   return std::max(-127, std::min(127, e));
 }
 
+// The same rule for an MX element format of largest value fmax = mf * 2^Ef
+// (mf in [1, 2)): the smallest e with fmax * 2^e >= a is Ea - Ef + (ma > mf)
+// for a = ma * 2^Ea.  E4M3 (448 = 1.75 * 2^8) gives mx_exponent; E5M2 (57344 =
+// 1.75 * 2^15) the MXFP8 gradient variant; E2M1 (6 = 1.5 * 2^2) MXFP4 ([NVFP4]:
+// NVFP4 narrows MXFP4's 32-value blocks to 16).
+int mx_exponent_fmt(float a, int fmt) {
+  if (a == 0.f) return -127;
+  if (!std::isfinite(a)) return 127;
+  int ea, ef;
+  double ma = 2.0 * std::frexp((double)a, &ea);
+  double mf = 2.0 * std::frexp((double)fmt_max(fmt), &ef);
+  int e = (ea - 1) - (ef - 1) + (ma > mf ? 1 : 0);
+  return std::max(-127, std::min(127, e));
+}
+
 }  // namespace
 
 // ======================================================================= C API
@@ -380,6 +395,33 @@ static void mxfp8_copy(const std::function<float(int64_t, int64_t)>& v, int64_t 
   });
 }
 
+// MX copy of any element format: blocks of 32 along cols, E8M0 exponent from
+// mx_exponent_fmt, codes = RNE encode of v * 2^-e (nothing saturates).  E2M1
+// codes are packed two per byte, the low nibble holding the even column.
+static void mx_copy(const std::function<float(int64_t, int64_t)>& v, int64_t rows, int64_t cols, int fmt,
+                    uint8_t* codes, uint8_t* sf) {
+  int64_t nb = cols / 32;
+  parallel_for(rows, [&](int64_t lo, int64_t hi) {
+    float blk[32];
+    for (int64_t r = lo; r < hi; ++r)
+      for (int64_t b = 0; b < nb; ++b) {
+        for (int i = 0; i < 32; ++i) blk[i] = v(r, b * 32 + i);
+        int e = mx_exponent_fmt(absmax(blk, 32, 1), fmt);
+        float mult = pow2f(-e);
+        for (int i = 0; i < 32; ++i) {
+          uint8_t q = encode(fmt, blk[i] * mult);
+          if (fmt == E2M1) {
+            uint8_t& byte = codes[r * (cols / 2) + (b * 32 + i) / 2];
+            byte = (i & 1) ? (uint8_t)((byte & 0x0F) | (q << 4)) : (uint8_t)((byte & 0xF0) | q);
+          } else {
+            codes[r * cols + b * 32 + i] = q;
+          }
+        }
+        sf[r * nb + b] = (uint8_t)(e + 127);
+      }
+  });
+}
+
 // MXFP8 ([NeMo] MXFP8: fixed 32-value blocks, E8M0 power-of-two scales).
 // Row-wise copy: codes [R, C] + E8M0 [R, C/32].  Column-wise copy: the
 // transpose re-blocked along R ([NeMo] sub-channel: transposes need
@@ -391,6 +433,18 @@ void orc_mxfp8(const uint16_t* x, int64_t R, int64_t C, uint8_t* row_codes, uint
   if (col_codes)
     mxfp8_copy([&](int64_t r, int64_t c) { return bf16_value(x[c * C + r]); }, C, R, col_codes, col_sf);
 }
+
+// MX quantization of any element format (E4M3 and E5M2: 1 byte per code, E2M1:
+// packed): row-wise codes [R, C (/2)] + E8M0 [R, C/32]; column-wise copy the
+// transpose re-blocked along R.  fmt = E4M3 is orc_mxfp8.
+void orc_mx(const uint16_t* x, int64_t R, int64_t C, int fmt, uint8_t* row_codes, uint8_t* row_sf,
+            uint8_t* col_codes, uint8_t* col_sf) {
+  if (row_codes)
+    mx_copy([&](int64_t r, int64_t c) { return bf16_value(x[r * C + c]); }, R, C, fmt, row_codes, row_sf);
+  if (col_codes)
+    mx_copy([&](int64_t r, int64_t c) { return bf16_value(x[c * C + r]); }, C, R, fmt, col_codes, col_sf);
+}
+int orc_mx_exponent_fmt(float a, int fmt) { return mx_exponent_fmt(a, fmt); }
 
 // ---------------------------------------------------------------- NVFP4
 // Quantizes one copy whose values are already materialised as floats v
@@ -595,7 +649,9 @@ void orc_fp8_block(const uint16_t* x, int64_t R, int64_t C, int block_rows, uint
 // 1 per-tensor FP8 E4M3, 2 per-tensor FP8 E5M2 (value = code * ts),
 // 3 MXFP8 (E4M3 code * 2^(sf - 127), sf [rows, K/32]),
 // 4 NVFP4 (E2M1 nibble * E4M3 sf [rows, K/16] * ts),
-// 5 block FP8 E4M3 (code * sinv[row / block_rows, k / 128]).
+// 5 block FP8 E4M3 (code * sinv[row / block_rows, k / 128]),
+// 6 MXFP8 with E5M2 codes (code * 2^(sf - 127), sf [rows, K/32]),
+// 7 MXFP4 (E2M1 nibble * 2^(sf - 127), sf [rows, K/32]).
 struct OrcOperand {
   int32_t kind;
   int32_t block_rows;
@@ -622,6 +678,16 @@ static inline double deq(const OrcOperand& o, int64_t K, int64_t r, int64_t k) {
     case 5: {
       float s = ((const float*)o.sf)[(r / o.block_rows) * (K / 128) + k / 128];
       return decode(E4M3, ((const uint8_t*)o.codes)[r * K + k]) * (double)s;
+    }
+    case 6: {
+      uint8_t s = ((const uint8_t*)o.sf)[r * (K / 32) + k / 32];
+      return decode(E5M2, ((const uint8_t*)o.codes)[r * K + k]) * std::ldexp(1.0, (int)s - 127);
+    }
+    case 7: {
+      uint8_t b = ((const uint8_t*)o.codes)[r * (K / 2) + k / 2];
+      uint8_t q = (k & 1) ? (b >> 4) : (b & 0xF);
+      uint8_t s = ((const uint8_t*)o.sf)[r * (K / 32) + k / 32];
+      return decode(E2M1, q) * std::ldexp(1.0, (int)s - 127);
     }
   }
   return std::nan("");
