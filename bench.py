@@ -18,8 +18,9 @@ the pre-quantize mode (GEMM only) are measured in the same run and reported
 under "recipes".
 
 Usage (the pages' CLI flags are accepted): python bench.py [--gpus N] [--steps K]
-[--warmup W] [--impl lpq|reference] [--recipe nvfp4|mxfp8|fp8_current|
-fp8_delayed|bf16] [--pre-quantize] [--no-fp8] [--no-fp4] ...
+[--warmup W] [--impl lpq|reference] [--recipe nvfp4|mxfp8|mxfp8_e5m2|mxfp4|
+fp8_current|fp8_delayed|bf16] [--pre-quantize] [--no-fp8] [--no-fp4] ...
+(mxfp8_e5m2: MXFP8 with E5M2 gradients; mxfp4: E2M1 with E8M0 scales per 32.)
 """
 import argparse
 import json
@@ -33,7 +34,17 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-RECIPES = ["bf16", "fp8_delayed", "fp8_current", "mxfp8", "nvfp4"]
+RECIPES = ["bf16", "fp8_delayed", "fp8_current", "mxfp8", "mxfp8_e5m2", "mxfp4", "nvfp4"]
+
+
+def sweep_recipes(args):
+    """Recipes of the sweep, less those --no-fp8 / --no-fp4 leave out."""
+    skip = set()
+    if args.no_fp8:
+        skip |= {"mxfp8", "mxfp8_e5m2"}
+    if args.no_fp4:
+        skip |= {"nvfp4", "mxfp4"}
+    return [r for r in RECIPES if r not in skip]
 
 
 def parse():
@@ -44,8 +55,8 @@ def parse():
     p.add_argument("--impl", choices=["lpq", "reference"], default="lpq")
     p.add_argument("--recipe", choices=RECIPES, default="nvfp4")
     p.add_argument("--pre-quantize", dest="prequant", action="store_true")
-    p.add_argument("--no-fp8", action="store_true", help="skip MXFP8 in the recipe sweep")
-    p.add_argument("--no-fp4", action="store_true", help="skip NVFP4 in the recipe sweep")
+    p.add_argument("--no-fp8", action="store_true", help="skip the MXFP8 recipes in the recipe sweep")
+    p.add_argument("--no-fp4", action="store_true", help="skip NVFP4 and MXFP4 in the recipe sweep")
     p.add_argument("--no-sweep", action="store_true", help="time only the headline recipe")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -183,6 +194,10 @@ class Layer:
             return fmt, 0, L.SCALING_DELAYED if recipe == "fp8_delayed" else L.SCALING_CURRENT
         if recipe == "mxfp8":
             return L.MXFP8, 0, L.SCALING_CURRENT
+        if recipe == "mxfp8_e5m2":  # E5M2 codes for the gradients, E4M3 for X and W
+            return (L.MXFP8_E5M2 if role == "dY" else L.MXFP8), 0, L.SCALING_CURRENT
+        if recipe == "mxfp4":
+            return L.MXFP4, 0, L.SCALING_CURRENT
         if recipe == "nvfp4":
             if role == "W":
                 return L.NVFP4_2D, 0, L.SCALING_CURRENT
@@ -293,7 +308,7 @@ class Layer:
         n = 12  # GEMMs
         if recipe == "bf16" or not (autocast or recipe == "fp8_delayed"):
             return n
-        per_q = {"fp8_current": 2, "fp8_delayed": 2, "mxfp8": 1, "nvfp4": 2}[recipe]  # (amax pass) + tile pass
+        per_q = {"fp8_current": 2, "fp8_delayed": 2, "mxfp8": 1, "mxfp8_e5m2": 1, "mxfp4": 1, "nvfp4": 2}[recipe]  # (amax pass) + tile pass
         if recipe == "fp8_delayed":
             per_q = 2  # tile pass + scale update
         return n + 24 * per_q
@@ -469,7 +484,8 @@ def run_lpq(args, rank, world, local):
     gemm_ms = sum(r["gemm_ms"] for r in table.values())
     quant_ms = sum(r["quant_ms"] for r in table.values())
     gemm_achieved = layer.flops / (gemm_ms * 1e-3) / 1e12
-    ratio = {"bf16": 1, "fp8_current": 2, "fp8_delayed": 2, "mxfp8": 2, "nvfp4": 6}[recipe]
+    ratio = {"bf16": 1, "fp8_current": 2, "fp8_delayed": 2, "mxfp8": 2, "mxfp8_e5m2": 2, "mxfp4": 6,
+             "nvfp4": 6}[recipe]
     if peaks:
         peak = peaks["bf16_tflops_sustained"] * ratio
         peak_src = f"of measured: bf16_tflops_sustained x {ratio} (nominal dense ratio of the format)"
@@ -478,7 +494,8 @@ def run_lpq(args, rank, world, local):
         peak_src = f"of fallback: 1.7 PFLOP/s bf16 sustained x {ratio}"
     algo_bytes = 0
     for name, lay, m, k, n in layer.shapes:
-        per = {"nvfp4": 0.5 + 1 / 16, "mxfp8": 1 + 1 / 32, "fp8_current": 1, "fp8_delayed": 1, "bf16": 2}[recipe]
+        per = {"nvfp4": 0.5 + 1 / 16, "mxfp8": 1 + 1 / 32, "mxfp8_e5m2": 1 + 1 / 32, "mxfp4": 0.5 + 1 / 32,
+               "fp8_current": 1, "fp8_delayed": 1, "bf16": 2}[recipe]
         algo_bytes += (m * k + n * k) * per + m * n * 2
     traffic = profiled_traffic(os.path.join(ROOT, "precision_transformer_gemms_gb300", "csrc", "gemm.cu"), recipe)
     roof = {"bound": "tensor", "achieved": gemm_achieved, "peak": peak, "unit": "TFLOP/s",
@@ -491,7 +508,7 @@ def run_lpq(args, rank, world, local):
     # recipe sweep (fewer steps each)
     recipes = {}
     if not args.no_sweep:
-        sweep = [r for r in RECIPES if not (args.no_fp8 and r == "mxfp8") and not (args.no_fp4 and r == "nvfp4")]
+        sweep = sweep_recipes(args)
         k = max(3, args.steps // 4)
         for r in sweep:
             layer.prequantize(r)
@@ -617,8 +634,8 @@ def run_lpq(args, rank, world, local):
             "metric": "quantize+GEMM TFLOP/s & % of FP8/FP4 peak; ms/layer (CodonFM-5B shape)",
             "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": {"nvfp4": "e2m1", "mxfp8": "e4m3", "fp8_current": "e4m3/e5m2", "fp8_delayed": "e4m3/e5m2",
-                      "bf16": "bf16"}[recipe],
+            "dtype": {"nvfp4": "e2m1", "mxfp8": "e4m3", "mxfp8_e5m2": "e4m3/e5m2", "mxfp4": "e2m1",
+                      "fp8_current": "e4m3/e5m2", "fp8_delayed": "e4m3/e5m2", "bf16": "bf16"}[recipe],
             "data": "synthetic",
             "config": {"workload": f"CodonFM-5B layer, 12 GEMMs, {recipe} {'autocast' if autocast else 'pre-quantize'}"
                                    f" (M={layer.M}, hidden {args.hidden_size}, intermediate {args.intermediate_size})",
@@ -687,7 +704,8 @@ def run_ksweep(args):
     torch.cuda.set_device(0)
     M = N = 8192
     fmts = {"fp8_current": (lpq.FP8_E4M3, lpq.FP8_E4M3), "mxfp8": (lpq.MXFP8, lpq.MXFP8),
-            "fp8_subchannel": (lpq.FP8_BLOCK_1x128, lpq.FP8_BLOCK_128x128), "nvfp4": (lpq.NVFP4, lpq.NVFP4_2D)}
+            "fp8_subchannel": (lpq.FP8_BLOCK_1x128, lpq.FP8_BLOCK_128x128), "nvfp4": (lpq.NVFP4, lpq.NVFP4_2D),
+            "mxfp4": (lpq.MXFP4, lpq.MXFP4)}
     out = {}
     for K in (1024, 2048, 4096, 8192, 16384):
         A = synth.bf16_normal((M, K), 1.0, 50, "cuda", 0.001, 100.0)
@@ -831,7 +849,7 @@ def run_report(args):
     import torch
     torch.cuda.set_device(0)
     layer = Layer(args, "cuda:0")
-    sweep = [r for r in RECIPES if not (args.no_fp8 and r == "mxfp8") and not (args.no_fp4 and r == "nvfp4")]
+    sweep = sweep_recipes(args)
     steps = max(3, args.steps // 4)
     per = {}  # recipe -> mode -> gemm name -> ms
     for r in sweep:

@@ -9,7 +9,8 @@
  *           per-tensor dynamic scaling from the amax; amax history.
  *   [NVFP4] "Accelerate LLM training with NVFP4 on Blackwell" (setupai.cc
  *           summary), "technical deep dive": E2M1 values (range about +-6), an
- *           E4M3 scale per 16-value micro-block plus an FP32 tensor scale.
+ *           E4M3 scale per 16-value micro-block plus an FP32 tensor scale;
+ *           MXFP4, the format it refines, shares one scale per 32 values.
  *   [TE]    "How to optimize Transformer-based models for low-precision
  *           training" (developer.nvidia.cn): config -> 12 GEMM shapes
  *           ("model configuration and training input", "autocast vs
@@ -66,7 +67,9 @@ typedef enum {
   LPQ_NVFP4 = 4,              /* E2M1 codes, E4M3 scale per 16 + FP32 tensor scale [NVFP4] */
   LPQ_NVFP4_2D = 5,           /* NVFP4 with one scale per 16x16 tile (weights) [TE] */
   LPQ_FP8_BLOCK_1x128 = 6,    /* E4M3, FP32 scale per 1x128 block (activations) [NeMo] */
-  LPQ_FP8_BLOCK_128x128 = 7   /* E4M3, FP32 scale per 128x128 block (weights) [NeMo] */
+  LPQ_FP8_BLOCK_128x128 = 7,  /* E4M3, FP32 scale per 128x128 block (weights) [NeMo] */
+  LPQ_MXFP8_E5M2 = 8,         /* E5M2 codes, one E8M0 scale per 32 values (gradients) [NeMo], [FP8] */
+  LPQ_MXFP4 = 9               /* packed E2M1 codes, one E8M0 scale per 32 values [NVFP4] */
 } lpq_format;
 
 typedef enum { LPQ_SCALING_CURRENT = 0, LPQ_SCALING_DELAYED = 1 } lpq_scaling;
@@ -90,9 +93,14 @@ enum {
 
 /* One quantized copy of a matrix.  All pointers are device pointers.
  *   codes        [rows, cols] bytes (FP8 formats), [rows, cols / 2] packed
- *                E2M1 (NVFP4: low nibble = even column), or bf16 [rows, cols].
- *   scales       block scales: u8 E8M0 (MXFP8), u8 E4M3 (NVFP4), FP32
- *                scale_inv (FP8 block); NULL for per-tensor FP8 and bf16.
+ *                E2M1 (NVFP4, MXFP4: low nibble = even column), or bf16
+ *                [rows, cols].
+ *   scales       block scales: u8 E8M0 (MXFP8, MXFP8_E5M2, MXFP4), u8 E4M3
+ *                (NVFP4), FP32 scale_inv (FP8 block); NULL for per-tensor FP8
+ *                and bf16.  An E8M0 scale s stands for 2^(s - 127), where the
+ *                block exponent is the smallest e with fmax * 2^e >= the
+ *                block's max |value| (fmax 448 E4M3, 57344 E5M2, 6 E2M1), so
+ *                that no code saturates.
  *   tensor_scale one FP32 dequantization factor: scale_inv for per-tensor
  *                FP8, the FP32 tensor scale for NVFP4; NULL otherwise.
  *   amax         one FP32: max |value| of this copy's input values (after the
@@ -131,20 +139,22 @@ typedef struct {
 
 /* Bytes of one copy's codes and scales for format `fmt`, a copy of `rows` x
  * `cols` and scale layout `sf_layout`.  Host-only, needs no GPU.
- * LPQ_SF_GEMM layout for MXFP8 / NVFP4: 128-row groups x KT atoms of 512
+ * LPQ_SF_GEMM layout for the MX formats and NVFP4: 128-row groups x KT atoms of 512
  * bytes; atom (g, t) starts at (g * KT + t) * 512 and holds, for row
  * r = 128 g + 32 j + i (i < 32, j < 4), its 4 scales of column-blocks
- * 4t .. 4t+3 at bytes 16 i + 4 j + 0..3.  KT = ceil(cols / 128) for MXFP8 and
- * 4 * ceil(cols / 256) for NVFP4; entries beyond the matrix read as 0.
+ * 4t .. 4t+3 at bytes 16 i + 4 j + 0..3.  KT = ceil(cols / 128) for MXFP8
+ * and MXFP8_E5M2, 2 * ceil(cols / 256) for MXFP4 and 4 * ceil(cols / 256) for
+ * NVFP4; entries beyond the matrix read as 0.
  * LPQ_SF_GEMM for FP8_BLOCK_1x128 is FP32 [cols / 128, rows] (rows fastest);
  * for FP8_BLOCK_128x128 it equals the plain layout. */
 lpq_status lpq_copy_bytes(int32_t fmt, int64_t rows, int64_t cols, int32_t sf_layout,
                           size_t *codes_bytes, size_t *scale_bytes);
 
 /* Quantizes x [rows, cols] bf16 (device) into the copies `flags` selects.
- *   fmt            LPQ_FP8_E4M3/E5M2 (with `scaling`), LPQ_MXFP8, LPQ_NVFP4,
- *                  LPQ_NVFP4_2D, LPQ_FP8_BLOCK_*, or LPQ_BF16 (row-wise =
- *                  copy, column-wise = transpose).
+ *   fmt            LPQ_FP8_E4M3/E5M2 (with `scaling`), LPQ_MXFP8,
+ *                  LPQ_MXFP8_E5M2, LPQ_MXFP4, LPQ_NVFP4, LPQ_NVFP4_2D,
+ *                  LPQ_FP8_BLOCK_*, or LPQ_BF16 (row-wise = copy,
+ *                  column-wise = transpose).
  *   scaling        per-tensor FP8 only.  CURRENT: scale = fmax / amax(x)
  *                  from an extra amax pass.  DELAYED: scale = *state->scale
  *                  from earlier steps; amax(x) is measured in the same pass
@@ -167,7 +177,7 @@ lpq_status lpq_copy_bytes(int32_t fmt, int64_t rows, int64_t cols, int32_t sf_la
  *                  codes and scales of the whole tensor (for the row-wise
  *                  copy with stochastic rounding, pass counter_offset =
  *                  first row * cols).
- * Shape rules: cols a multiple of the row-wise block (16 NVFP4, 32 MXFP8, 128
+ * Shape rules: cols a multiple of the row-wise block (16 NVFP4, 32 MX formats, 128
  * FP8 block, 16 NVFP4_2D), rows a multiple of the column-wise block when
  * LPQ_COLWISE is set (same numbers; 128x128 needs neither rows nor cols beyond
  * cols % 128 == 0 and rows % 128 == 0 for its column copy), and every row of
@@ -196,7 +206,9 @@ typedef enum { LPQ_FPROP = 0, LPQ_DGRAD = 1, LPQ_WGRAD = 2 } lpq_layout;
  * tensor cores (tcgen05), output bf16 (c_is_fp32 = 0) or FP32, row-major with
  * leading dimension n.  a is [m, k], b is [n, k], both contiguous along k.
  * Legal pairings: BF16 x BF16; {E4M3, E5M2} x {E4M3, E5M2} (per-tensor,
- * scale_inv product applied in the epilogue); MXFP8 x MXFP8; {NVFP4,
+ * scale_inv product applied in the epilogue); {MXFP8, MXFP8_E5M2} x {MXFP8,
+ * MXFP8_E5M2} (E5M2 gradients against E4M3 activations or weights);
+ * MXFP4 x MXFP4; {NVFP4,
  * NVFP4_2D} x {NVFP4, NVFP4_2D} (tensor scales in the epilogue); FP8 block
  * (1x128 or 128x128) x FP8 block (FP32 block scales applied per 128-deep
  * slice).  Block-scaled operands must use LPQ_SF_GEMM.  k must be a multiple

@@ -21,12 +21,15 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 bool is_fp8_pertensor(int32_t f) { return f == LPQ_FP8_E4M3 || f == LPQ_FP8_E5M2; }
 bool is_nvfp4(int32_t f) { return f == LPQ_NVFP4 || f == LPQ_NVFP4_2D; }
 bool is_block(int32_t f) { return f == LPQ_FP8_BLOCK_1x128 || f == LPQ_FP8_BLOCK_128x128; }
-bool valid_fmt(int32_t f) { return f >= LPQ_BF16 && f <= LPQ_FP8_BLOCK_128x128; }
+bool is_mx8(int32_t f) { return f == LPQ_MXFP8 || f == LPQ_MXFP8_E5M2; }
+// Formats with u8 block scales in the tensor-core scale layout.
+bool is_u8_scaled(int32_t f) { return is_mx8(f) || f == LPQ_MXFP4 || is_nvfp4(f); }
+bool valid_fmt(int32_t f) { return f >= LPQ_BF16 && f <= LPQ_MXFP4; }
 
 // Column-block length of a format's row-wise scales (0 = none).
 int64_t row_block(int32_t f) {
   switch (f) {
-    case LPQ_MXFP8: return 32;
+    case LPQ_MXFP8: case LPQ_MXFP8_E5M2: case LPQ_MXFP4: return 32;
     case LPQ_NVFP4: case LPQ_NVFP4_2D: return 16;
     case LPQ_FP8_BLOCK_1x128: case LPQ_FP8_BLOCK_128x128: return 128;
   }
@@ -36,7 +39,7 @@ int64_t row_block(int32_t f) {
 // Rows of the input that a column-wise copy needs as a multiple.
 int64_t col_rows_multiple(int32_t f) {
   switch (f) {
-    case LPQ_MXFP8: return 32;
+    case LPQ_MXFP8: case LPQ_MXFP8_E5M2: case LPQ_MXFP4: return 32;
     case LPQ_FP8_BLOCK_1x128: case LPQ_FP8_BLOCK_128x128: return 128;
   }
   return 16;
@@ -120,8 +123,8 @@ lpq_status lpq_copy_bytes(int32_t fmt, int64_t rows, int64_t cols, int32_t sf_la
   switch (fmt) {
     case LPQ_BF16: cb = 2 * n; break;
     case LPQ_FP8_E4M3: case LPQ_FP8_E5M2: cb = n; break;
-    case LPQ_MXFP8: case LPQ_NVFP4: case LPQ_NVFP4_2D:
-      cb = fmt == LPQ_MXFP8 ? n : n / 2;
+    case LPQ_MXFP8: case LPQ_MXFP8_E5M2: case LPQ_MXFP4: case LPQ_NVFP4: case LPQ_NVFP4_2D:
+      cb = is_mx8(fmt) ? n : n / 2;
       sb = sf_layout == LPQ_SF_GEMM ? (size_t)sf_row_groups(rows) * (size_t)sf_kt_atoms(fmt, cols) * 512
                                     : (size_t)rows * (size_t)(cols / blk);
       break;
@@ -205,7 +208,8 @@ lpq_status lpq_gemm(int32_t layout, const lpq_qview* a, const lpq_qview* b, void
                      want_b ? "column-wise" : "row-wise");
   const int32_t fa = a->fmt, fb = b->fmt;
   const bool pair_ok = (fa == LPQ_BF16 && fb == LPQ_BF16) || (is_fp8_pertensor(fa) && is_fp8_pertensor(fb)) ||
-                       (fa == LPQ_MXFP8 && fb == LPQ_MXFP8) || (is_nvfp4(fa) && is_nvfp4(fb)) ||
+                       (is_mx8(fa) && is_mx8(fb)) || (fa == LPQ_MXFP4 && fb == LPQ_MXFP4) ||
+                       (is_nvfp4(fa) && is_nvfp4(fb)) ||
                        (is_block(fa) && is_block(fb));
   if (!pair_ok) return set_error(LPQ_ERR_UNSUPPORTED, "no GEMM for the pairing %d x %d (no fallback)", fa, fb);
   const int64_t kmul = is_block(fa) ? 128 : 32;
@@ -217,7 +221,7 @@ lpq_status lpq_gemm(int32_t layout, const lpq_qview* a, const lpq_qview* b, void
       for (const lpq_qview* v : {a, b}) {
         if (!v->codes) return set_error(LPQ_ERR_INVALID_ARG, "operand codes NULL");
         if (!aligned16(v->codes)) return set_error(LPQ_ERR_ALIGN, "operand codes not 16-byte aligned");
-        if ((v->fmt == LPQ_MXFP8 || is_nvfp4(v->fmt))) {
+        if (is_u8_scaled(v->fmt)) {
           if (v->sf_layout != LPQ_SF_GEMM)
             return set_error(LPQ_ERR_INVALID_ARG, "block-scaled operands need LPQ_SF_GEMM scales");
           if (!v->scales || !aligned16(v->scales)) return set_error(LPQ_ERR_ALIGN, "operand scales NULL/unaligned");

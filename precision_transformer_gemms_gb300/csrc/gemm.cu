@@ -39,9 +39,25 @@ namespace {
 constexpr int kBM = 128;
 constexpr int kKBytes = 128;  // bytes of K per pipeline stage (one 128-byte swizzle row)
 
+// Scale atoms (512 bytes: 4 scales of each of 128 rows) per k-step of
+// kKBytes: 128 FP8 values = 4 MX blocks (one atom); 256 FP4 values = 8 MX
+// blocks (two) or 16 NVFP4 blocks (four).
+constexpr int sf_atoms_per_step(int kind) {
+  return kind == kKindNVF4 ? 4 : kind == kKindMXF4 ? 2 : kind == kKindMXF8 ? 1 : 0;
+}
+// Instruction-descriptor scale selectors of MMA j (K = 32 or 64) of a k-step:
+// MXFP8 (one scale per MMA) takes byte j of the atom's 32-bit column, MXFP4
+// (two per MMA) bytes 2 (j % 2) and 2 (j % 2) + 1 of atom j / 2, NVFP4 (four
+// per MMA) the whole column of atom j.
+template <int KIND>
+__device__ __forceinline__ uint32_t sf_select(int j) {
+  const uint32_t id = KIND == kKindMXF8 ? (uint32_t)j : KIND == kKindMXF4 ? (uint32_t)(j & 1) * 2u : 0u;
+  return (id << 4) | (id << 29);
+}
+
 template <int KIND, int BN, int NACC, bool SFST = false>
 struct Cfg {
-  static constexpr int kSfAtoms = KIND == kKindNVF4 ? 4 : (KIND == kKindMXF8 ? 1 : 0);  // per 128 rows
+  static constexpr int kSfAtoms = sf_atoms_per_step(KIND);  // per 128 rows
   static constexpr int kA = kBM * kKBytes;
   static constexpr int kB = BN * kKBytes;
   static constexpr int kSfa = kSfAtoms * 512;
@@ -229,14 +245,21 @@ __global__ void __launch_bounds__(kThreadsGemm + (SFST ? 32 * kSfWarps : 0))
             } else if constexpr (KIND == kKindMXF8) {
               mma_bs<KIND>(tmem_d, ad, bd, g.idesc | ((uint32_t)j << 4) | ((uint32_t)j << 29), tmem_sfa, tmem_sfb, acc);
             } else if constexpr (SFST) {
+              const int at = j * CF::kSfAtoms / 4;  // the MMA's scale atom
               const uint32_t base = tmem_sfa + s * (CF::kSfaCols + CF::kSfbCols);  // the stage's slot
-              mma_bs<KIND>(tmem_d, ad, bd, g.idesc, base + 4 * j, base + CF::kSfaCols + 4 * (BN / 128) * j, acc);
+              mma_bs<KIND>(tmem_d, ad, bd, g.idesc | sf_select<KIND>(j), base + 4 * at,
+                           base + CF::kSfaCols + 4 * (BN / 128) * at, acc);
             } else {
-              tmem_cp_sf(tmem_sfa + 4 * j, ((uint64_t)kHiSf << 32) | (falo + j * 32));
+              const int at = j * CF::kSfAtoms / 4;
+              if ((j * CF::kSfAtoms) % 4 == 0) {  // first MMA of the atom: copy it
+                tmem_cp_sf(tmem_sfa + 4 * at, ((uint64_t)kHiSf << 32) | (falo + at * 32));
 #pragma unroll
-              for (int i = 0; i < BN / 128; ++i)
-                tmem_cp_sf(tmem_sfb + 4 * (BN / 128) * j + 4 * i, ((uint64_t)kHiSf << 32) | (fblo + (i * 4 + j) * 32));
-              mma_bs<KIND>(tmem_d, ad, bd, g.idesc, tmem_sfa + 4 * j, tmem_sfb + 4 * (BN / 128) * j, acc);
+                for (int i = 0; i < BN / 128; ++i)
+                  tmem_cp_sf(tmem_sfb + 4 * (BN / 128) * at + 4 * i,
+                             ((uint64_t)kHiSf << 32) | (fblo + (i * CF::kSfAtoms + at) * 32));
+              }
+              mma_bs<KIND>(tmem_d, ad, bd, g.idesc | sf_select<KIND>(j), tmem_sfa + 4 * at,
+                           tmem_sfb + 4 * (BN / 128) * at, acc);
             }
           }
           tc_commit(&empty[s]);
@@ -246,6 +269,7 @@ __global__ void __launch_bounds__(kThreadsGemm + (SFST ? 32 * kSfWarps : 0))
       }
     }
   } else if (SFST && warp >= 2 + kEpiWarps) {
+    if constexpr (SFST) {  // only kernels with scale warps carry this code
     // ------------------------------------------------------------ scale warps (NVFP4)
     // Per k-step: once the stage's previous MMAs are done (its TMEM scale slot
     // is free), this warp's lane quarter of the step's 12 scale atoms goes
@@ -261,30 +285,24 @@ __global__ void __launch_bounds__(kThreadsGemm + (SFST ? 32 * kSfWarps : 0))
         if (!(ok = mbar_wait_bounded(&empty[s], ph ^ 1u, abort_flag, &g_device_error))) break;  // slot free
         __syncwarp();
         tc_fence_after();
+        constexpr int NA = CF::kSfAtoms, G = BN / 128;
         const uint4* fa = reinterpret_cast<const uint4*>(sSfa + s * CF::kSfa) + lane;  // atom j line `lane`
         const uint4* fb = reinterpret_cast<const uint4*>(sSfb + s * CF::kSfb) + lane;
-        uint32_t va[16], vb[32];
+        uint32_t va[4 * NA], vb[4 * NA * G];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
+        for (int j = 0; j < NA; ++j) {
           const uint4 x = fa[j * 32];
           va[4 * j] = x.x; va[4 * j + 1] = x.y; va[4 * j + 2] = x.z; va[4 * j + 3] = x.w;
 #pragma unroll
-          for (int i = 0; i < BN / 128; ++i) {
-            const uint4 y = fb[(i * 4 + j) * 32];
-            const int c = 4 * (BN / 128) * j + 4 * i;
+          for (int i = 0; i < G; ++i) {
+            const uint4 y = fb[(i * NA + j) * 32];
+            const int c = 4 * G * j + 4 * i;
             vb[c] = y.x; vb[c + 1] = y.y; vb[c + 2] = y.z; vb[c + 3] = y.w;
           }
         }
         const uint32_t base = tmem_base + NACC * BN + s * (CF::kSfaCols + CF::kSfbCols) + lanes;
-        tmem_st16(base, va);
-        if constexpr (BN == 256) {
-          tmem_st32(base + CF::kSfaCols, vb);
-        } else {
-          uint32_t vb16[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) vb16[i] = vb[i];
-          tmem_st16(base + CF::kSfaCols, vb16);
-        }
+        tmem_st_cols(base, va);
+        tmem_st_cols(base + CF::kSfaCols, vb);
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
@@ -292,6 +310,7 @@ __global__ void __launch_bounds__(kThreadsGemm + (SFST ? 32 * kSfWarps : 0))
         if (++s == (uint32_t)S) { s = 0; ph ^= 1u; }
       }
     }
+    }  // SFST
   } else if (warp >= 2) {
     // ------------------------------------------------------------ epilogue
     // Warp w reads TMEM lanes 32 * (w % 4) .. of columns [half * BN/2, +BN/2).
@@ -475,7 +494,7 @@ constexpr int kPairBN = 256;
 
 template <int KIND, bool kSfbFull, bool SFST = false>
 struct PairCfg {
-  static constexpr int kSfAtoms = KIND == kKindNVF4 ? 4 : (KIND == kKindMXF8 ? 1 : 0);
+  static constexpr int kSfAtoms = sf_atoms_per_step(KIND);
   static constexpr int kA = kBM * kKBytes;
   static constexpr int kB = (kPairBN / 2) * kKBytes;
   static constexpr int kSfbGroups = kSfbFull ? 2 : 1;
@@ -504,6 +523,11 @@ __device__ __forceinline__ void mma_pair_bs(uint32_t d_tmem, uint64_t adesc, uin
     asm volatile(
         "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
         "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
+        ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate) : "memory");
+  } else if constexpr (KIND == kKindMXF4) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
         ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate) : "memory");
   } else {
     asm volatile(
@@ -658,15 +682,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm + (SFST
               mma_pair_bs<KIND>(tmem_d, ad, bd, g.idesc | ((uint32_t)j << 4) | ((uint32_t)j << 29), tmem_sfa, tmem_sfb,
                                 acc);
             } else if constexpr (SFST) {
+              const int at = j * PC::kSfAtoms / 4;  // the MMA's scale atom
               const uint32_t base = tmem_sfa + s * (PC::kSfaCols + PC::kSfbCols);  // the stage's slot
-              mma_pair_bs<KIND>(tmem_d, ad, bd, g.idesc, base + 4 * j, base + PC::kSfaCols + 4 * PC::kSfbGroups * j, acc);
+              mma_pair_bs<KIND>(tmem_d, ad, bd, g.idesc | sf_select<KIND>(j), base + 4 * at,
+                                base + PC::kSfaCols + 4 * PC::kSfbGroups * at, acc);
             } else {
-              tmem_cp_sf_pair(tmem_sfa + 4 * j, ((uint64_t)kHiSf << 32) | (falo + j * 32));
+              const int at = j * PC::kSfAtoms / 4;
+              if ((j * PC::kSfAtoms) % 4 == 0) {  // first MMA of the atom: copy it
+                tmem_cp_sf_pair(tmem_sfa + 4 * at, ((uint64_t)kHiSf << 32) | (falo + at * 32));
 #pragma unroll
-              for (int i = 0; i < PC::kSfbGroups; ++i)
-                tmem_cp_sf_pair(tmem_sfb + 4 * PC::kSfbGroups * j + 4 * i,
-                                ((uint64_t)kHiSf << 32) | (fblo + (i * 4 + j) * 32));
-              mma_pair_bs<KIND>(tmem_d, ad, bd, g.idesc, tmem_sfa + 4 * j, tmem_sfb + 4 * PC::kSfbGroups * j, acc);
+                for (int i = 0; i < PC::kSfbGroups; ++i)
+                  tmem_cp_sf_pair(tmem_sfb + 4 * PC::kSfbGroups * at + 4 * i,
+                                  ((uint64_t)kHiSf << 32) | (fblo + (i * PC::kSfAtoms + at) * 32));
+              }
+              mma_pair_bs<KIND>(tmem_d, ad, bd, g.idesc | sf_select<KIND>(j), tmem_sfa + 4 * at,
+                                tmem_sfb + 4 * PC::kSfbGroups * at, acc);
             }
           }
           tc_commit_pair(&empty[s], 0x3);
@@ -676,6 +706,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm + (SFST
       }
     }
   } else if (run && SFST && warp >= 2 + kEpiWarps) {
+    if constexpr (SFST) {  // only kernels with scale warps carry this code
     // scale warps: this CTA's lane quarter of the step's scale atoms (its own A
     // rows, all 256 B rows) from shared memory into the TMEM slot; both CTAs'
     // scale warps report to the even CTA's slot barrier
@@ -689,23 +720,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm + (SFST
         if (!(ok = mbar_wait_bounded(&empty[s], ph ^ 1u, abort_flag, &g_device_error))) break;  // slot free
         __syncwarp();
         tc_fence_after();
+        constexpr int NA = PC::kSfAtoms, G = PC::kSfbGroups;
         const uint4* fa = reinterpret_cast<const uint4*>(sSfa + s * PC::kSfa) + lane;
         const uint4* fb = reinterpret_cast<const uint4*>(sSfb + s * PC::kSfb) + lane;
-        uint32_t va[16], vb[32];
+        uint32_t va[4 * NA], vb[4 * NA * G];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
+        for (int j = 0; j < NA; ++j) {
           const uint4 x = fa[j * 32];
           va[4 * j] = x.x; va[4 * j + 1] = x.y; va[4 * j + 2] = x.z; va[4 * j + 3] = x.w;
 #pragma unroll
-          for (int i = 0; i < PC::kSfbGroups; ++i) {
-            const uint4 y = fb[(i * 4 + j) * 32];
-            const int c = 4 * PC::kSfbGroups * j + 4 * i;
+          for (int i = 0; i < G; ++i) {
+            const uint4 y = fb[(i * NA + j) * 32];
+            const int c = 4 * G * j + 4 * i;
             vb[c] = y.x; vb[c + 1] = y.y; vb[c + 2] = y.z; vb[c + 3] = y.w;
           }
         }
         const uint32_t base = tmem_sfa + s * (PC::kSfaCols + PC::kSfbCols) + lanes;
-        tmem_st16(base, va);
-        tmem_st32(base + PC::kSfaCols, vb);
+        tmem_st_cols(base, va);
+        tmem_st_cols(base + PC::kSfaCols, vb);
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
@@ -715,6 +747,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm + (SFST
         if (++s == (uint32_t)S) { s = 0; ph ^= 1u; }
       }
     }
+    }  // SFST
   } else if (run && warp >= 2) {
     constexpr int HALF = kPairBN / 2;
     const int q = warp & 3;
@@ -1170,11 +1203,13 @@ lpq_status launch_gemm(const lpq_qview* a, const lpq_qview* b, void* c, int32_t 
     }
     return run<kKindF8F6F4, BN, 2>(ta, tb, g, s);
   }
-  if (fa == LPQ_MXFP8) {
+  if (fa == LPQ_MXFP8 || fa == LPQ_MXFP8_E5M2) {
+    // E4M3 (format 0) or E5M2 (format 1) elements on either side, E8M0 scales
+    const uint32_t af = fa == LPQ_MXFP8_E5M2 ? 1 : 0, bf = fb == LPQ_MXFP8_E5M2 ? 1 : 0;
     g.num_k = (int)((k + kKBytes - 1) / kKBytes);
     if ((st = make_map(&ta, a->codes, false, k, m, k, 128, kBM)) != LPQ_OK) return st;
     if ((st = make_map(&tb, b->codes, false, k, n, k, 128, BN)) != LPQ_OK) return st;
-    g.idesc = idesc_block_scaled(0, 0, 1, BN);  // E4M3 x E4M3, E8M0 scales
+    g.idesc = idesc_block_scaled(af, bf, 1, BN);
     g.sfa = static_cast<const uint8_t*>(a->scales);
     g.sfb = static_cast<const uint8_t*>(b->scales);
     g.sfa_kt = sf_kt_atoms(LPQ_MXFP8, k);
@@ -1190,10 +1225,42 @@ lpq_status launch_gemm(const lpq_qview* a, const lpq_qview* b, void* c, int32_t 
     }
     if (nv_bn == 128) {
       if ((st = make_map(&tb, b->codes, false, k, n, k, 128, 128)) != LPQ_OK) return st;
-      g.idesc = idesc_block_scaled(0, 0, 1, 128);
+      g.idesc = idesc_block_scaled(af, bf, 1, 128);
       return run<kKindMXF8, 128, 2>(ta, tb, g, s);
     }
     return run<kKindMXF8, BN, 1>(ta, tb, g, s);
+  }
+  if (fa == LPQ_MXFP4) {
+    // packed E2M1 (format 1) with an E8M0 scale per 32 values: two scales per
+    // K = 64 MMA, two atoms per 256-value k-step; the scale warps write them
+    // into TMEM as for NVFP4 (LPQ_GEMM_SFCP=1: tcgen05.cp by the MMA thread)
+    g.num_k = (int)((k / 2 + kKBytes - 1) / kKBytes);
+    if ((st = make_map(&ta, a->codes, false, k / 2, m, k / 2, 128, kBM)) != LPQ_OK) return st;
+    if ((st = make_map(&tb, b->codes, false, k / 2, n, k / 2, 128, BN)) != LPQ_OK) return st;
+    g.idesc = idesc_block_scaled(1, 1, 1, BN);
+    g.sfa = static_cast<const uint8_t*>(a->scales);
+    g.sfb = static_cast<const uint8_t*>(b->scales);
+    g.sfa_kt = sf_kt_atoms(LPQ_MXFP4, k);
+    g.sfb_kt = g.sfa_kt;
+    g.sfb_groups = sf_row_groups(n);
+    const bool cp = getenv_flag("LPQ_GEMM_SFCP");
+    if (use_pair(kKindMXF4) && m >= 256) {
+      CUtensorMap tsa, tsb;
+      if ((st = make_map(&tb, b->codes, false, k / 2, n, k / 2, 128, kPairBN / 2)) != LPQ_OK) return st;
+      if ((st = make_sf_map(&tsa, g.sfa, sf_row_groups(m) * g.sfa_kt, 2)) != LPQ_OK) return st;
+      if ((st = make_sf_map(&tsb, g.sfb, g.sfb_groups * g.sfb_kt, 2)) != LPQ_OK) return st;
+      g.idesc = (g.idesc & ~(31u << 24)) | (16u << 24);
+      if (cp) return run_pair<kKindMXF4, true>(ta, tb, tsa, tsb, g, s);
+      return run_pair<kKindMXF4, true, true>(ta, tb, tsa, tsb, g, s);
+    }
+    if (nv_bn == 128) {
+      if ((st = make_map(&tb, b->codes, false, k / 2, n, k / 2, 128, 128)) != LPQ_OK) return st;
+      g.idesc = idesc_block_scaled(1, 1, 1, 128);
+      if (cp) return run<kKindMXF4, 128, 2>(ta, tb, g, s);
+      return run<kKindMXF4, 128, 2, true>(ta, tb, g, s);
+    }
+    if (cp) return run<kKindMXF4, BN, 1>(ta, tb, g, s);
+    return run<kKindMXF4, BN, 1, true>(ta, tb, g, s);
   }
   if (fa == LPQ_NVFP4 || fa == LPQ_NVFP4_2D) {
     g.num_k = (int)((k / 2 + kKBytes - 1) / kKBytes);

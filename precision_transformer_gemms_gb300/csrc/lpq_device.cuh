@@ -68,10 +68,14 @@ __device__ __forceinline__ float pow2_exact(int k) {
   return k >= -126 ? __uint_as_float((uint32_t)(k + 127) << 23) : __uint_as_float(0x00400000u);
 }
 
-// MXFP8 block exponent: the smallest e with 448 * 2^e >= a (a >= 0), from the
-// exact decomposition a = m * 2^E: e = E - 8 + (m > 1.75), clamped to
-// [-127, 127]; a = 0 gives -127, a non-finite amax gives 127.
-__device__ __forceinline__ int mx_exponent(float a) {
+// MX block exponent: the smallest e with fmax * 2^e >= a (a >= 0), where the
+// element format's largest value is fmax = mf * 2^EMAX (E4M3 448 = 1.75 * 2^8,
+// E5M2 57344 = 1.75 * 2^15, E2M1 6 = 1.5 * 2^2).  From the exact
+// decomposition a = m * 2^E: e = E - EMAX + (m > mf), clamped to [-127, 127];
+// a = 0 gives -127, a non-finite amax gives 127.  kMfFrac is the 23-bit
+// fraction of mf.
+template <int EMAX, uint32_t kMfFrac>
+__device__ __forceinline__ int mx_exponent_t(float a) {
   if (a == 0.f) return -127;
   uint32_t b = __float_as_uint(a);
   uint32_t be = (b >> 23) & 0xFF, frac = b & 0x7FFFFF;
@@ -84,9 +88,12 @@ __device__ __forceinline__ int mx_exponent(float a) {
   } else {
     E = (int)be - 127;
   }
-  int e = E - 8 + (frac > 0x600000u ? 1 : 0);
+  int e = E - EMAX + (frac > kMfFrac ? 1 : 0);
   return e < -127 ? -127 : (e > 127 ? 127 : e);
 }
+__device__ __forceinline__ int mx_exponent(float a) { return mx_exponent_t<8, 0x600000u>(a); }       // E4M3
+__device__ __forceinline__ int mx_exponent_e5m2(float a) { return mx_exponent_t<15, 0x600000u>(a); }  // E5M2
+__device__ __forceinline__ int mx_exponent_e2m1(float a) { return mx_exponent_t<2, 0x400000u>(a); }   // E2M1
 
 // Correctly rounded x / 6 for x >= 0 (a block max): the product with
 // RN(1/6), corrected once with the exact residual x - 6 q (an FMA).  Below
@@ -369,6 +376,12 @@ __device__ __forceinline__ void mma_bs(uint32_t d_tmem, uint64_t adesc, uint64_t
         "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
         ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
         : "memory");
+  } else if constexpr (kKind == kKindMXF4) {  // E2M1, E8M0 scale per 32 values: two per K = 64
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
+        ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
   } else {
     asm volatile(
         "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
@@ -389,6 +402,10 @@ __device__ __forceinline__ void tmem_st4(uint32_t taddr, uint32_t a, uint32_t b,
   asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(a), "r"(b), "r"(c),
                "r"(d) : "memory");
 }
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t* v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+               "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]) : "memory");
+}
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 // Store 16 / 32 consecutive 32-bit columns into this warp's 32 TMEM lanes.
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
@@ -405,6 +422,15 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32
       "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]),
       "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]),
       "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31]) : "memory");
+}
+
+// Store N (8, 16 or 32) consecutive 32-bit columns.
+template <int N>
+__device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const uint32_t (&v)[N]) {
+  static_assert(N == 8 || N == 16 || N == 32, "8, 16 or 32 columns");
+  if constexpr (N == 8) tmem_st8(taddr, v);
+  else if constexpr (N == 16) tmem_st16(taddr, v);
+  else tmem_st32(taddr, v);
 }
 
 // Load 32 consecutive fp32 columns of this warp's 32 TMEM lanes.

@@ -12,15 +12,19 @@ namespace lpq {
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 
 // Tensor-core instruction kinds used by the GEMM kernels.
-enum { kKindF16 = 0, kKindF8F6F4 = 1, kKindMXF8 = 2, kKindNVF4 = 3 };
+enum { kKindF16 = 0, kKindF8F6F4 = 1, kKindMXF8 = 2, kKindNVF4 = 3, kKindMXF4 = 4 };
 
 // Thread-local error text (capi.cu).
 lpq_status set_error(lpq_status st, const char* fmt, ...);
 lpq_status cuda_check(cudaError_t e, const char* what);
 
 // Scale-factor geometry of the tensor-core layout.
+// Atoms (4 scales of 128 rows) per 128-row group: one per 128 columns for
+// MXFP8, two per 256 columns for MXFP4 (a 256-value k-step of packed E2M1
+// holds 8 blocks of 32), four per 256 columns for NVFP4 (16 blocks of 16).
 inline int64_t sf_kt_atoms(int32_t fmt, int64_t cols) {
-  if (fmt == LPQ_MXFP8) return (cols + 127) / 128;
+  if (fmt == LPQ_MXFP8 || fmt == LPQ_MXFP8_E5M2) return (cols + 127) / 128;
+  if (fmt == LPQ_MXFP4) return ((cols + 255) / 256) * 2;
   return ((cols + 255) / 256) * 4;  // NVFP4 / NVFP4_2D
 }
 inline int64_t sf_row_groups(int64_t rows) { return (rows + 127) / 128; }

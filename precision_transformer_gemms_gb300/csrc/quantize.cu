@@ -26,7 +26,8 @@ namespace lpq {
 
 namespace {
 
-enum QKind { QK_FP8 = 0, QK_MX = 1, QK_NV = 2, QK_NV2D = 3, QK_BLK1 = 4, QK_BLK128 = 5, QK_BF16 = 6 };
+// QK_MX: MXFP8 (E4M3 codes, or E5M2 with kE5M2); QK_MX4: MXFP4 (packed E2M1).
+enum QKind { QK_FP8 = 0, QK_MX = 1, QK_NV = 2, QK_NV2D = 3, QK_BLK1 = 4, QK_BLK128 = 5, QK_BF16 = 6, QK_MX4 = 7 };
 
 struct QParams {
   const uint16_t* x;
@@ -127,6 +128,14 @@ __device__ __forceinline__ uint2 fp8_codes8(const float v[8], float s) {
 #pragma unroll
   for (int i = 0; i < 4; ++i) b[i] = cvt_fp8x2<kE5M2>(__fmul_rn(v[2 * i], s), __fmul_rn(v[2 * i + 1], s));
   return make_uint2(b[0] | (b[1] << 16), b[2] | (b[3] << 16));
+}
+
+// Block exponent of the MX kinds for their element format.
+template <int KIND, bool kE5M2>
+__device__ __forceinline__ int mx_block_exponent(float m) {
+  if constexpr (KIND == QK_MX4) return mx_exponent_e2m1(m);
+  else if constexpr (kE5M2) return mx_exponent_e5m2(m);
+  else return mx_exponent(m);
 }
 
 __device__ __forceinline__ float nv_s_enc(const float* amax) {
@@ -268,16 +277,20 @@ __global__ void __launch_bounds__(kThreads, KIND == QK_NV2D ? 5 : (KIND != QK_NV
     if constexpr (KIND == QK_FP8) {
       uint2 q = fp8_codes8<kE5M2>(f, scale);
       if (ok) *reinterpret_cast<uint2*>(p.row_codes + r * C + c0 + lc) = q;
-    } else if constexpr (KIND == QK_MX) {
+    } else if constexpr (KIND == QK_MX || KIND == QK_MX4) {
+      // 32-value block = 4 neighbouring threads of the row
       float m = 0.f;
 #pragma unroll
       for (int i = 0; i < 8; ++i) m = absmax_acc(m, f[i]);
       m = warp_max_xor(m, 4);
-      const int e = mx_exponent(m);
+      const int e = mx_block_exponent<KIND, kE5M2>(m);
       const float mult = pow2_exact(-e);
-      uint2 q = fp8_codes8<false>(f, mult);
       if (ok) {
-        *reinterpret_cast<uint2*>(p.row_codes + r * C + c0 + lc) = q;
+        if constexpr (KIND == QK_MX4)
+          *reinterpret_cast<uint32_t*>(p.row_codes + r * (C >> 1) + ((c0 + lc) >> 1)) =
+              nv_codes8(f, mult, false, uint4{}, uint4{});
+        else
+          *reinterpret_cast<uint2*>(p.row_codes + r * C + c0 + lc) = fp8_codes8<kE5M2>(f, mult);
         if ((t & 3) == 0) {
           const int64_t kb = (c0 + lc) >> 5;
           const int64_t off = p.row_gemm ? sf_gemm_offset(r, kb, p.row_kt) : r * (C >> 5) + kb;
@@ -465,7 +478,24 @@ __global__ void __launch_bounds__(kThreads, KIND == QK_NV2D ? 5 : (KIND != QK_NV
   const int64_t c = c0 + cl, rbase = r0 + rh * 32;
   if (c >= C || rbase >= R) return;
   const int nvalid = (R - rbase) >= 32 ? 32 : 16;  // R is a multiple of 16 here
-  if constexpr (KIND == QK_FP8 || KIND == QK_MX) {
+  if constexpr (KIND == QK_MX4) {
+    // R is a multiple of 32 here: the thread's 32 rows are one whole block.
+    float f[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) f[i] = tile_val(tile[rh * 32 + i], cl);
+    float m = 0.f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) m = absmax_acc(m, f[i]);
+    const int e = mx_exponent_e2m1(m);
+    const float s = pow2_exact(-e);
+    uint32_t q[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) q[j] = nv_codes8(f + 8 * j, s, false, uint4{}, uint4{});
+    *reinterpret_cast<uint4*>(p.col_codes + c * (R >> 1) + (rbase >> 1)) = make_uint4(q[0], q[1], q[2], q[3]);
+    const int64_t kb = rbase >> 5;
+    const int64_t off = p.col_gemm ? sf_gemm_offset(c, kb, p.col_kt) : c * (R >> 5) + kb;
+    p.col_sf[off] = (uint8_t)(e + 127);
+  } else if constexpr (KIND == QK_FP8 || KIND == QK_MX) {
     float f[32];
 #pragma unroll
     for (int i = 0; i < 32; ++i) f[i] = tile_val(tile[rh * 32 + i], cl);
@@ -475,12 +505,12 @@ __global__ void __launch_bounds__(kThreads, KIND == QK_NV2D ? 5 : (KIND != QK_NV
       float m = 0.f;
 #pragma unroll
       for (int i = 0; i < 32; ++i) m = absmax_acc(m, f[i]);
-      e = mx_exponent(m);
+      e = mx_block_exponent<KIND, kE5M2>(m);
       s = pow2_exact(-e);
     }
     uint2 q[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) q[j] = fp8_codes8 < (KIND == QK_FP8) && kE5M2 > (f + 8 * j, s);
+    for (int j = 0; j < 4; ++j) q[j] = fp8_codes8<kE5M2>(f + 8 * j, s);
     uint8_t* dst = p.col_codes + c * R + rbase;
     *reinterpret_cast<uint4*>(dst) = make_uint4(q[0].x, q[0].y, q[1].x, q[1].y);
     if (nvalid == 32) *reinterpret_cast<uint4*>(dst + 16) = make_uint4(q[2].x, q[2].y, q[3].x, q[3].y);
@@ -683,6 +713,8 @@ lpq_status launch_quantize(const void* xv, int64_t R, int64_t C, int32_t fmt, in
   const bool given = flags & LPQ_GIVEN_AMAX;  // the views' amax fields are inputs
   lpq_qview* rv = do_row ? &out->row : nullptr;
   lpq_qview* cv = do_col ? &out->col : nullptr;
+  const bool mx = fmt == LPQ_MXFP8 || fmt == LPQ_MXFP8_E5M2 || fmt == LPQ_MXFP4;
+  const bool u8_scaled = mx || fmt == LPQ_NVFP4 || fmt == LPQ_NVFP4_2D;  // tensor-core scale layout possible
   QParams p{};
   p.x = static_cast<const uint16_t*>(xv);
   p.R = R;
@@ -693,7 +725,7 @@ lpq_status launch_quantize(const void* xv, int64_t R, int64_t C, int32_t fmt, in
     p.row_sfinv = static_cast<float*>(rv->scales);
     p.row_ts = rv->tensor_scale;
     p.row_gemm = rv->sf_layout == LPQ_SF_GEMM;
-    if (fmt == LPQ_MXFP8 || fmt == LPQ_NVFP4 || fmt == LPQ_NVFP4_2D) p.row_kt = sf_kt_atoms(fmt, C);
+    if (u8_scaled) p.row_kt = sf_kt_atoms(fmt, C);
   }
   if (cv) {
     p.col_codes = static_cast<uint8_t*>(cv->codes);
@@ -701,7 +733,7 @@ lpq_status launch_quantize(const void* xv, int64_t R, int64_t C, int32_t fmt, in
     p.col_sfinv = static_cast<float*>(cv->scales);
     p.col_ts = cv->tensor_scale;
     p.col_gemm = cv->sf_layout == LPQ_SF_GEMM;
-    if (fmt == LPQ_MXFP8 || fmt == LPQ_NVFP4 || fmt == LPQ_NVFP4_2D) p.col_kt = sf_kt_atoms(fmt, R);
+    if (u8_scaled) p.col_kt = sf_kt_atoms(fmt, R);
   }
   p.seed = seed;
   p.ctr_off = counter_offset;
@@ -712,8 +744,8 @@ lpq_status launch_quantize(const void* xv, int64_t R, int64_t C, int32_t fmt, in
   // Zero padding of tensor-core scale layouts so that partial atoms read as 0.
   auto zero_pad = [&](lpq_qview* v) -> lpq_status {
     if (!v || v->sf_layout != LPQ_SF_GEMM) return LPQ_OK;
-    if (!(fmt == LPQ_MXFP8 || fmt == LPQ_NVFP4 || fmt == LPQ_NVFP4_2D)) return LPQ_OK;
-    const int64_t blk = fmt == LPQ_MXFP8 ? 32 : 16;
+    if (!u8_scaled) return LPQ_OK;
+    const int64_t blk = mx ? 32 : 16;
     const int64_t kt = sf_kt_atoms(fmt, v->cols);
     if (v->rows % 128 == 0 && (v->cols / blk) == kt * 4) return LPQ_OK;
     size_t bytes = (size_t)sf_row_groups(v->rows) * (size_t)kt * 512;
@@ -782,11 +814,14 @@ lpq_status launch_quantize(const void* xv, int64_t R, int64_t C, int32_t fmt, in
       return e5 ? run_tile<QK_FP8, true>(p, s) : run_tile<QK_FP8, false>(p, s);
     }
     case LPQ_MXFP8:
+    case LPQ_MXFP8_E5M2:
+    case LPQ_MXFP4:
       if (rv && rv->amax) {  // optional amax output
         if ((st = zero_f32(rv->amax, s)) != LPQ_OK) return st;
         if ((st = run_amax(p.x, R, C, rv->amax, cv ? cv->amax : nullptr, nullptr, 0, s)) != LPQ_OK) return st;
       }
-      return run_tile<QK_MX, false>(p, s);
+      if (fmt == LPQ_MXFP4) return run_tile<QK_MX4, false>(p, s);
+      return fmt == LPQ_MXFP8_E5M2 ? run_tile<QK_MX, true>(p, s) : run_tile<QK_MX, false>(p, s);
     case LPQ_NVFP4:
     case LPQ_NVFP4_2D: {
       const bool rht = p.rht;

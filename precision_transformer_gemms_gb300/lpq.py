@@ -14,7 +14,8 @@ from . import build as _build
 
 # ----------------------------------------------------------------- enums (mirror include/lpq.h)
 OK, ERR_INVALID_ARG, ERR_SHAPE, ERR_ALIGN, ERR_UNSUPPORTED, ERR_ARCH, ERR_CUDA, ERR_TIMEOUT = range(8)
-BF16, FP8_E4M3, FP8_E5M2, MXFP8, NVFP4, NVFP4_2D, FP8_BLOCK_1x128, FP8_BLOCK_128x128 = range(8)
+(BF16, FP8_E4M3, FP8_E5M2, MXFP8, NVFP4, NVFP4_2D, FP8_BLOCK_1x128, FP8_BLOCK_128x128, MXFP8_E5M2,
+ MXFP4) = range(10)
 SCALING_CURRENT, SCALING_DELAYED = 0, 1
 ROWWISE, COLWISE, RHT_COLWISE, STOCHASTIC, GIVEN_AMAX = 1, 2, 4, 8, 16
 SF_PLAIN, SF_GEMM = 0, 1
@@ -23,7 +24,9 @@ FPROP, DGRAD, WGRAD = 0, 1, 2
 STATUS_NAMES = {OK: "OK", ERR_INVALID_ARG: "INVALID_ARG", ERR_SHAPE: "SHAPE", ERR_ALIGN: "ALIGN",
                 ERR_UNSUPPORTED: "UNSUPPORTED", ERR_ARCH: "ARCH", ERR_CUDA: "CUDA", ERR_TIMEOUT: "TIMEOUT"}
 FORMAT_NAMES = {BF16: "bf16", FP8_E4M3: "fp8_e4m3", FP8_E5M2: "fp8_e5m2", MXFP8: "mxfp8", NVFP4: "nvfp4",
-                NVFP4_2D: "nvfp4_2d", FP8_BLOCK_1x128: "fp8_block_1x128", FP8_BLOCK_128x128: "fp8_block_128x128"}
+                NVFP4_2D: "nvfp4_2d", FP8_BLOCK_1x128: "fp8_block_1x128", FP8_BLOCK_128x128: "fp8_block_128x128",
+                MXFP8_E5M2: "mxfp8_e5m2", MXFP4: "mxfp4"}
+PACKED_FP4 = (NVFP4, NVFP4_2D, MXFP4)  # two E2M1 codes per byte
 FMAX = {FP8_E4M3: 448.0, FP8_E5M2: 57344.0}
 
 
@@ -164,10 +167,10 @@ class Copy:
                      self.cols, self.fmt, self.sf_layout, self.colwise, 0)
 
     def codes_matrix(self):
-        """Codes as a [rows, bytes per row] uint8 tensor (packed for NVFP4)."""
+        """Codes as a [rows, bytes per row] uint8 tensor (packed for NVFP4 and MXFP4)."""
         if self.fmt == BF16:
             return self.codes
-        per_row = self.cols // 2 if self.fmt in (NVFP4, NVFP4_2D) else self.cols
+        per_row = self.cols // 2 if self.fmt in PACKED_FP4 else self.cols
         return self.codes[: self.rows * per_row].view(self.rows, per_row)
 
 

@@ -22,9 +22,14 @@ def sf_gemm_to_plain(buf, rows, nblocks, kt):
     return buf[off]
 
 
+MX_FORMATS = (lpq.MXFP8, lpq.MXFP8_E5M2, lpq.MXFP4)
+
+
 def kt_atoms(fmt, cols):
-    if fmt == lpq.MXFP8:
+    if fmt in (lpq.MXFP8, lpq.MXFP8_E5M2):
         return (cols + 127) // 128
+    if fmt == lpq.MXFP4:
+        return ((cols + 255) // 256) * 2
     return ((cols + 255) // 256) * 4
 
 
@@ -35,8 +40,8 @@ def codes(copy):
 def plain_scales(copy):
     """Scales of a Copy in the oracle's plain layout."""
     f = copy.fmt
-    if f in (lpq.MXFP8, lpq.NVFP4, lpq.NVFP4_2D):
-        blk = 32 if f == lpq.MXFP8 else 16
+    if f in MX_FORMATS + (lpq.NVFP4, lpq.NVFP4_2D):
+        blk = 32 if f in MX_FORMATS else 16
         nb = copy.cols // blk
         buf = np_u8(copy.scales)
         if copy.sf_layout == lpq.SF_GEMM:
@@ -74,6 +79,10 @@ def oracle_operand(copy, fmt_override=None):
         return o.Operand(o.K_FP8_E4M3 if f == lpq.FP8_E4M3 else o.K_FP8_E5M2, codes(copy), ts=scalar(copy.tensor_scale))
     if f == lpq.MXFP8:
         return o.Operand(o.K_MXFP8, codes(copy), plain_scales(copy))
+    if f == lpq.MXFP8_E5M2:
+        return o.Operand(o.K_MXFP8_E5M2, codes(copy), plain_scales(copy))
+    if f == lpq.MXFP4:
+        return o.Operand(o.K_MXFP4, codes(copy), plain_scales(copy))
     if f in (lpq.NVFP4, lpq.NVFP4_2D):
         return o.Operand(o.K_NVFP4, codes(copy), plain_scales(copy), scalar(copy.tensor_scale))
     if f == lpq.FP8_BLOCK_1x128:

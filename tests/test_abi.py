@@ -49,6 +49,25 @@ def test_copy_bytes():
     assert e.value.status == lpq.ERR_SHAPE
 
 
+def test_copy_bytes_mx_variants():
+    """MXFP8 with E5M2 codes has MXFP8's sizes; MXFP4 packs two codes a byte
+    with one E8M0 scale per 32 values (4.25 bits per value) and two scale atoms
+    per 256 columns in the tensor-core layout."""
+    for layout in (lpq.SF_PLAIN, lpq.SF_GEMM):
+        assert lpq.copy_bytes(lpq.MXFP8_E5M2, 300, 544, layout) == lpq.copy_bytes(lpq.MXFP8, 300, 544, layout)
+    cb, sb = lpq.copy_bytes(lpq.MXFP4, 1024, 4096, lpq.SF_PLAIN)
+    assert (cb, sb) == (1024 * 2048, 1024 * 128)
+    assert (cb + sb) * 8 / (1024 * 4096) == 4.25
+    assert lpq.copy_bytes(lpq.MXFP4, 300, 544, lpq.SF_GEMM) == (300 * 272, 3 * (2 * 3) * 512)
+    for fmt in (lpq.MXFP8_E5M2, lpq.MXFP4):
+        with pytest.raises(lpq.LpqError) as e:
+            lpq.copy_bytes(fmt, 4, 48)
+        assert e.value.status == lpq.ERR_SHAPE
+    with pytest.raises(lpq.LpqError) as e:
+        lpq.copy_bytes(lpq.MXFP4 + 1, 4, 64)
+    assert e.value.status == lpq.ERR_INVALID_ARG
+
+
 def _quantize_raw(x_ptr, rows, cols, fmt, flags, scaling=0, ctr=0, out=None, state=None):
     out = out or lpq.QTensorC()
     return lpq.lib().lpq_quantize(x_ptr, rows, cols, fmt, scaling, flags, 0, ctr, 0, state, ctypes.byref(out), None)
@@ -66,6 +85,10 @@ def test_quantize_validation_codes():
     assert _quantize_raw(ctypes.c_void_p(8), 4, 32, lpq.MXFP8, lpq.ROWWISE) == lpq.ERR_ALIGN
     assert _quantize_raw(ctypes.c_void_p(16), 4, 40, lpq.MXFP8, lpq.ROWWISE) == lpq.ERR_SHAPE
     assert _quantize_raw(ctypes.c_void_p(16), 40, 32, lpq.MXFP8, lpq.COLWISE) == lpq.ERR_SHAPE  # rows % 32
+    for fmt in (lpq.MXFP8_E5M2, lpq.MXFP4):
+        assert _quantize_raw(None, 4, 32, fmt, lpq.ROWWISE | lpq.STOCHASTIC) == lpq.ERR_UNSUPPORTED
+        assert _quantize_raw(ctypes.c_void_p(16), 4, 48, fmt, lpq.ROWWISE) == lpq.ERR_SHAPE
+        assert _quantize_raw(ctypes.c_void_p(16), 48, 32, fmt, lpq.COLWISE) == lpq.ERR_SHAPE
     # a view that does not match the request
     out = lpq.QTensorC()
     out.row = lpq.QView(16, 16, 16, 16, 4, 64, lpq.MXFP8, lpq.SF_GEMM, 0, 0)
@@ -87,6 +110,18 @@ def test_gemm_validation_codes():
     assert call(7, a, a, 128, 128, 256) == lpq.ERR_INVALID_ARG
     assert call(0, view(lpq.MXFP8, 128, 48), view(lpq.MXFP8, 64, 48), 128, 64, 48) == lpq.ERR_SHAPE
     assert call(0, a, view(lpq.MXFP8, 64, 256), 128, 64, 256, c=8) == lpq.ERR_ALIGN
+    # MX variants: E5M2 gradients pair with E4M3 MXFP8 either way; MXFP4 only with MXFP4
+    f4 = view(lpq.MXFP4, 64, 256)
+    for fa, fb in ((lpq.MXFP4, lpq.NVFP4), (lpq.NVFP4, lpq.MXFP4), (lpq.MXFP4, lpq.MXFP8), (lpq.MXFP8, lpq.MXFP4),
+                   (lpq.MXFP8_E5M2, lpq.FP8_E5M2)):
+        assert call(0, view(fa, 128, 256), view(fb, 64, 256), 128, 64, 256) == lpq.ERR_UNSUPPORTED, (fa, fb)
+    validated = (lpq.ERR_UNSUPPORTED, lpq.ERR_SHAPE, lpq.ERR_INVALID_ARG, lpq.ERR_ALIGN)
+    for fa, fb in ((lpq.MXFP8_E5M2, lpq.MXFP8), (lpq.MXFP8, lpq.MXFP8_E5M2), (lpq.MXFP4, lpq.MXFP4)):
+        # legal pairings pass validation and stop at the device check (no GPU here)
+        assert call(0, view(fa, 128, 256), view(fb, 64, 256), 128, 64, 256) not in validated, (fa, fb)
+    assert call(0, view(lpq.MXFP4, 128, 48), view(lpq.MXFP4, 64, 48), 128, 64, 48) == lpq.ERR_SHAPE
+    f4.sf_layout = lpq.SF_PLAIN
+    assert call(0, view(lpq.MXFP4, 128, 256), f4, 128, 64, 256) == lpq.ERR_INVALID_ARG  # plain scales
 
 
 def test_scale_update_and_selftest_validation():
@@ -109,6 +144,8 @@ def test_mma_peak_validation():
 def test_given_amax_validation():
     """LPQ_GIVEN_AMAX applies to current-scaled per-tensor FP8 and NVFP4 only."""
     assert _quantize_raw(None, 4, 32, lpq.MXFP8, lpq.ROWWISE | lpq.GIVEN_AMAX) == lpq.ERR_UNSUPPORTED
+    for fmt in (lpq.MXFP8_E5M2, lpq.MXFP4):
+        assert _quantize_raw(None, 4, 32, fmt, lpq.ROWWISE | lpq.GIVEN_AMAX) == lpq.ERR_UNSUPPORTED
     assert _quantize_raw(None, 4, 128, lpq.FP8_BLOCK_1x128, lpq.ROWWISE | lpq.GIVEN_AMAX) == lpq.ERR_UNSUPPORTED
     assert _quantize_raw(None, 4, 32, lpq.FP8_E4M3, lpq.ROWWISE | lpq.GIVEN_AMAX, scaling=1) == lpq.ERR_UNSUPPORTED
     assert _quantize_raw(None, 4, 32, lpq.NVFP4, lpq.ROWWISE | 32) == lpq.ERR_INVALID_ARG  # unknown bit

@@ -38,16 +38,18 @@ def check(a, b, M, N, K, out_fp32, layout=lpq.FPROP):
 @pytest.mark.parametrize("out_fp32", [True, False])
 @pytest.mark.parametrize("shape", SHAPES)
 @pytest.mark.parametrize("fmts", [(lpq.BF16, lpq.BF16), (lpq.FP8_E4M3, lpq.FP8_E4M3), (lpq.FP8_E5M2, lpq.FP8_E4M3),
-                                  (lpq.MXFP8, lpq.MXFP8), (lpq.NVFP4, lpq.NVFP4), (lpq.NVFP4, lpq.NVFP4_2D)])
+                                  (lpq.MXFP8, lpq.MXFP8), (lpq.MXFP8_E5M2, lpq.MXFP8),
+                                  (lpq.MXFP8_E5M2, lpq.MXFP8_E5M2), (lpq.MXFP4, lpq.MXFP4),
+                                  (lpq.NVFP4, lpq.NVFP4), (lpq.NVFP4, lpq.NVFP4_2D)])
 def test_gemm_parity(fmts, shape, out_fp32, path, monkeypatch):
     """Every kernel path: one CTA per 128 x 256 tile (NVFP4 scales stored into
     TMEM by scale warps, or copied by the MMA thread: single_cp), one CTA per
     128 x 128 tile with two accumulators (block-scaled kinds: single_bn128), and
     CTA pairs (cta_group::2) per 256 x 256 tile, whose bf16 output leaves
     through TMA tile stores (pair) or direct stores (pair_direct)."""
-    if path == "single_cp" and fmts[0] not in (lpq.NVFP4,):
-        pytest.skip("scale-copy variant exists for NVFP4 only")
-    if path == "single_bn128" and fmts[0] not in (lpq.NVFP4, lpq.MXFP8):
+    if path == "single_cp" and fmts[0] not in (lpq.NVFP4, lpq.MXFP4):
+        pytest.skip("scale-copy variant exists for the FP4 kinds only")
+    if path == "single_bn128" and fmts[0] not in (lpq.NVFP4, lpq.MXFP8, lpq.MXFP8_E5M2, lpq.MXFP4):
         pytest.skip("128-wide tiles exist for the block-scaled kinds only")
     monkeypatch.setenv("LPQ_GEMM_PAIR", "1" if path.startswith("pair") else "0")
     monkeypatch.setenv("LPQ_GEMM_DIRECT_STORE", "1" if path == "pair_direct" else "0")
@@ -81,7 +83,7 @@ def test_gemm_closed_form_all_ones():
     M, K, N = 256, 1024, 256
     x = torch.ones((M, K), dtype=torch.bfloat16, device="cuda")
     y = torch.ones((N, K), dtype=torch.bfloat16, device="cuda")
-    for fmt in (lpq.MXFP8, lpq.NVFP4, lpq.BF16):
+    for fmt in (lpq.MXFP8, lpq.MXFP8_E5M2, lpq.MXFP4, lpq.NVFP4, lpq.BF16):
         if fmt == lpq.BF16:
             a, b = lpq.Copy.of_bf16(x), lpq.Copy.of_bf16(y)
         else:
@@ -90,6 +92,8 @@ def test_gemm_closed_form_all_ones():
         torch.cuda.synchronize()
         ref, _ = o.gemm(oracle_operand(a), oracle_operand(b), 1, 1, K, pairs=np.array([[0, 0]]))
         assert float(ref[0]) == pytest.approx(K, rel=1e-6)
+        if fmt != lpq.NVFP4:
+            assert float(ref[0]) == K  # power-of-two scales: exact
         if fmt == lpq.NVFP4:  # the FP32 tensor scales 1/2688 are rounded: K up to a few ulps
             assert torch.allclose(c, torch.full_like(c, float(ref[0])), rtol=1e-6, atol=0), fmt
         else:
@@ -102,7 +106,7 @@ def test_gemm_single_nonzero_k():
     y = torch.zeros((N, K), dtype=torch.bfloat16, device="cuda")
     x[:, 77] = 3.0
     y[:, 77] = -2.0
-    for fmt in (lpq.MXFP8, lpq.FP8_E4M3, lpq.NVFP4, lpq.BF16):
+    for fmt in (lpq.MXFP8, lpq.MXFP8_E5M2, lpq.MXFP4, lpq.FP8_E4M3, lpq.NVFP4, lpq.BF16):
         if fmt == lpq.BF16:
             a, b = lpq.Copy.of_bf16(x), lpq.Copy.of_bf16(y)
         else:
@@ -113,7 +117,8 @@ def test_gemm_single_nonzero_k():
         assert torch.allclose(c, torch.full_like(c, float(ref[0])), rtol=1e-6), fmt
 
 
-@pytest.mark.parametrize("fmt", [lpq.MXFP8, lpq.NVFP4, lpq.FP8_E4M3, lpq.BF16, lpq.FP8_BLOCK_1x128])
+@pytest.mark.parametrize("fmt", [lpq.MXFP8, lpq.MXFP8_E5M2, lpq.MXFP4, lpq.NVFP4, lpq.FP8_E4M3, lpq.BF16,
+                                 lpq.FP8_BLOCK_1x128])
 def test_fprop_dgrad_wgrad_layouts(fmt):
     """The three GEMMs of a linear layer on the copies each one reads."""
     M, K, N = 256, 512, 384
@@ -135,6 +140,10 @@ def test_fprop_dgrad_wgrad_layouts(fmt):
         qx = lpq.quantize(X, fmt, both)
         qw = lpq.quantize(W, fmt, both)
         qd = lpq.quantize(dY, lpq.FP8_E5M2, both)
+    elif fmt == lpq.MXFP8_E5M2:  # MXFP8 with E5M2 gradients: dY in E5M2, X and W in E4M3
+        qx = lpq.quantize(X, lpq.MXFP8, both)
+        qw = lpq.quantize(W, lpq.MXFP8, both)
+        qd = lpq.quantize(dY, fmt, both)
     else:
         qx, qw, qd = (lpq.quantize(t, fmt, both) for t in (X, W, dY))
     check(qx.row, qw.row, M, N, K, True, lpq.FPROP)      # Y  [M, N]
@@ -142,7 +151,7 @@ def test_fprop_dgrad_wgrad_layouts(fmt):
     check(qd.col, qx.col, N, K, M, True, lpq.WGRAD)      # dW [N, K]
 
 
-@pytest.mark.parametrize("fmt", [lpq.NVFP4, lpq.MXFP8, lpq.FP8_E4M3, lpq.BF16])
+@pytest.mark.parametrize("fmt", [lpq.NVFP4, lpq.MXFP8, lpq.MXFP4, lpq.FP8_E4M3, lpq.BF16])
 def test_full_size_sampled(fmt):
     """QKV Fprop at the layer's size (15872 x 4096 x 12288): the first and last
     128 x 128 output tiles and 4096 uniformly sampled elements."""
@@ -186,6 +195,12 @@ def test_no_fallback_on_mixed_formats():
     with pytest.raises(lpq.LpqError) as e:
         lpq.gemm(lpq.FPROP, a, b)
     assert e.value.status == lpq.ERR_UNSUPPORTED
+    # MXFP4 pairs with MXFP4 only (not with NVFP4, nor with MXFP8)
+    c = lpq.quantize(x, lpq.MXFP4, lpq.ROWWISE).row
+    for a2, b2 in ((c, b), (b, c), (c, a)):
+        with pytest.raises(lpq.LpqError) as e:
+            lpq.gemm(lpq.FPROP, a2, b2)
+        assert e.value.status == lpq.ERR_UNSUPPORTED
 
 
 def test_bounded_wait_reports_timeout_and_context_survives():
@@ -210,7 +225,8 @@ def test_mma_peak_modes_run(kind, mode):
     assert 0 < rate < 1.2 * nominal
 
 
-@pytest.mark.parametrize("fmts", [(lpq.BF16, lpq.BF16), (lpq.FP8_E4M3, lpq.FP8_E4M3), (lpq.MXFP8, lpq.MXFP8)])
+@pytest.mark.parametrize("fmts", [(lpq.BF16, lpq.BF16), (lpq.FP8_E4M3, lpq.FP8_E4M3), (lpq.MXFP8, lpq.MXFP8),
+                                  (lpq.MXFP4, lpq.MXFP4)])
 def test_pair_gemm_ragged_n_direct_stores(fmts, monkeypatch):
     """N not a multiple of 8: no tensor map fits the output rows, so the pair
     kernel's epilogue stores directly (bf16 and FP32 outputs)."""

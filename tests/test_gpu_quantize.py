@@ -83,6 +83,62 @@ def test_mxfp8_gemm_layout_padding_is_zero():
     assert not buf[~used].any()
 
 
+MX_VARIANTS = {lpq.MXFP8_E5M2: (o.E5M2, 1e-3), lpq.MXFP4: (o.E2M1, 1.0)}  # element format, input std
+
+
+@pytest.mark.parametrize("layout", [lpq.SF_PLAIN, lpq.SF_GEMM])
+@pytest.mark.parametrize("shape", SHAPES_32)
+@pytest.mark.parametrize("fmt", [lpq.MXFP8_E5M2, lpq.MXFP4])
+def test_mx_variants(fmt, shape, layout):
+    """MXFP8 with E5M2 codes (gradients, std 1e-3 like dY) and MXFP4 (packed
+    E2M1): both copies, codes and E8M0 scales bit for bit."""
+    efmt, std = MX_VARIANTS[fmt]
+    x, bits = bf16_input(shape, std=std, seed=12, outlier_frac=0.001, outlier_scale=50)
+    q = lpq.quantize(x, fmt, BOTH, sf_layout=layout)
+    ref = o.mx(bits, efmt)
+    eq(codes(q.row), ref["row"])
+    eq(plain_scales(q.row), ref["row_sf"])
+    eq(codes(q.col), ref["col"])
+    eq(plain_scales(q.col), ref["col_sf"])
+
+
+@pytest.mark.parametrize("fmt", [lpq.MXFP8_E5M2, lpq.MXFP4])
+def test_mx_variants_special_values(fmt):
+    """Zeros (E8M0 code 0), a block whose max sits exactly on fmax * 2^e, a
+    tiny negative beside a large value (negative-zero code), and infinities
+    (saturated codes in a block of exponent 127)."""
+    efmt, _ = MX_VARIANTS[fmt]
+    z = torch.zeros((64, 128), dtype=torch.bfloat16, device="cuda")
+    fmax = {o.E5M2: 57344.0, o.E2M1: 6.0}[efmt]
+    z[1, 0:32] = 0.5
+    z[1, 5] = fmax / 4  # block max exactly fmax * 2^-2
+    z[7, 9] = -1e-30
+    z[7, 10] = 5.0
+    z[9, 40] = float("inf")
+    z[12, 70] = float("-inf")
+    bits = synth.host_bits(z)
+    q = lpq.quantize(z, fmt, BOTH)
+    ref = o.mx(bits, efmt)
+    for name in ("row", "col"):
+        eq(codes(getattr(q, name)), ref[name])
+        eq(plain_scales(getattr(q, name)), ref[name + "_sf"])
+    assert plain_scales(q.row)[1, 0] == 127 - 2
+    assert plain_scales(q.row)[0, 0] == 0
+
+
+def test_mxfp4_gemm_layout_padding_is_zero():
+    x, _ = bf16_input((160, 288), seed=3)
+    q = lpq.quantize(x, lpq.MXFP4, lpq.ROWWISE, sf_layout=lpq.SF_GEMM)
+    buf = q.row.scales.cpu().numpy().copy()
+    kt = 2 * ((288 + 255) // 256)
+    used = np.zeros(buf.size, bool)
+    r = np.arange(160)[:, None]
+    kb = np.arange(288 // 32)[None, :]
+    used[(((r >> 7) * kt + (kb >> 2)) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4 + (kb & 3)).ravel()] = True
+    assert buf.size == 2 * kt * 512
+    assert not buf[~used].any()
+
+
 @pytest.mark.parametrize("layout", [lpq.SF_PLAIN, lpq.SF_GEMM])
 @pytest.mark.parametrize("shape", SHAPES_16)
 @pytest.mark.parametrize("variant", ["rne", "rht", "sr", "rht_sr"])
@@ -199,6 +255,7 @@ def test_empty_input():
 
 
 @pytest.mark.parametrize("fmt,shape", [(lpq.MXFP8, (15872, 4096)), (lpq.NVFP4, (15872, 4096)),
+                                       (lpq.MXFP8_E5M2, (15872, 4096)), (lpq.MXFP4, (15872, 4096)),
                                        (lpq.FP8_E4M3, (15872, 4096)), (lpq.NVFP4_2D, (4096, 4096))])
 def test_full_size_whole_tensor(fmt, shape):
     """At the layer's full size, in the tensor-core scale layout the benchmark
@@ -216,6 +273,10 @@ def test_full_size_whole_tensor(fmt, shape):
     elif fmt == lpq.MXFP8:
         q = lpq.quantize(x, fmt, BOTH)
         ref = o.mxfp8(bits)
+        pairs = [("row", "row_sf"), ("col", "col_sf")]
+    elif fmt in MX_VARIANTS:
+        q = lpq.quantize(x, fmt, BOTH)
+        ref = o.mx(bits, MX_VARIANTS[fmt][0])
         pairs = [("row", "row_sf"), ("col", "col_sf")]
     else:
         q = lpq.quantize(x, fmt, BOTH)
