@@ -147,6 +147,46 @@ __device__ __forceinline__ float nv_ts_dec(const float* amax) {
   return finite_pos(a) ? __fdiv_rn(a, 2688.0f) : 1.0f;
 }
 
+// Column-wise NVFP4 copy of a 64 x 128 tile staged in shared memory (column
+// cl: 32 code bytes for the tile's 64 rows at col_stage + 32 cl, 4 block
+// scales at sf_stage + 4 cl): each column's codes leave as two 16-byte
+// stores (8-byte pieces when R % 32 != 0 or at a 16-row tail) and its scales
+// as one 4-byte store where the layout allows.  R and C are multiples of 16.
+__device__ __forceinline__ void store_col_staged(const QParams& p, const uint8_t* col_stage, const uint8_t* sf_stage,
+                                                 int64_t c_first, int64_t rt, int t) {
+  const int64_t R = p.R, C = p.C;
+  {
+    const int cl = t >> 1, h = t & 1;  // column, 32-row half
+    const int64_t c = c_first + cl, rr = rt + 32 * h;
+    if (c < C && rr < R) {
+      uint8_t* dst = p.col_codes + c * (R >> 1) + (rr >> 1);
+      const uint4 v16 = *reinterpret_cast<const uint4*>(col_stage + cl * 32 + 16 * h);
+      if (rr + 32 <= R && (R & 31) == 0) {
+        *reinterpret_cast<uint4*>(dst) = v16;  // 16-byte aligned: R / 2 and rr / 2 are multiples of 16
+      } else {
+        *reinterpret_cast<uint2*>(dst) = make_uint2(v16.x, v16.y);
+        if (rr + 16 < R) *reinterpret_cast<uint2*>(dst + 8) = make_uint2(v16.z, v16.w);
+      }
+    }
+  }
+  if (t < 128) {
+    const int64_t c = c_first + t;
+    const int64_t kb0 = rt >> 4, nkb = R >> 4;
+    if (c < C) {
+      const uint32_t sf4 = *reinterpret_cast<const uint32_t*>(sf_stage + 4 * t);
+      const int64_t off0 = p.col_gemm ? sf_gemm_offset(c, kb0, p.col_kt) : c * nkb + kb0;
+      if (kb0 + 4 <= nkb && (p.col_gemm || (nkb & 3) == 0)) {
+        *reinterpret_cast<uint32_t*>(p.col_sf + off0) = sf4;  // 4 consecutive, 4-byte aligned scales
+      } else {
+#pragma unroll
+        for (int b = 0; b < 4; ++b)
+          if (kb0 + b < nkb)
+            p.col_sf[p.col_gemm ? sf_gemm_offset(c, kb0 + b, p.col_kt) : c * nkb + kb0 + b] = (uint8_t)(sf4 >> (8 * b));
+      }
+    }
+  }
+}
+
 // NVO (NVFP4 options, compile-time so that the plain paths carry none of the
 // registers of the others): bit 0 stochastic rounding, bit 1 RHT of the
 // column-wise copy.
@@ -160,6 +200,9 @@ __global__ void __launch_bounds__(kThreads, KIND == QK_NV2D ? 5 : (KIND != QK_NV
   __shared__ float tile_f[32];
   __shared__ uint32_t tile_s[32];
   __shared__ float fb_tab[2][128];  // NVFP4: s_enc / dec(S) for the row and column copies
+  // NVFP4 column-wise copy staged per column (64 rows: 32 code bytes, 4 scales)
+  __shared__ __align__(16) uint8_t col_stage[KIND == QK_NV ? 128 * 32 : 16];
+  __shared__ __align__(4) uint8_t sf_stage[KIND == QK_NV ? 128 * 4 : 4];
 
   const int t = threadIdx.x;
   const int64_t r0 = (int64_t)blockIdx.y * TR, c0 = (int64_t)blockIdx.x * kTC;
@@ -474,6 +517,45 @@ __global__ void __launch_bounds__(kThreads, KIND == QK_NV2D ? 5 : (KIND != QK_NV
 
   // ---------------------------------------------------------------- column-wise copy
   if (!p.col_codes) return;
+  if constexpr (KIND == QK_NV) {
+    // Two adjacent columns per thread (each 4-byte shared load holds a row's
+    // values of both), one 16-row block: RHT, block scale and codes per
+    // column; the codes and scales are staged per column and leave as whole
+    // 32-byte column segments.  R is a multiple of 16.
+    const int cp = t & 63, rq = t >> 6;
+    const int64_t c = c0 + 2 * cp, rr = r0 + 16 * rq;
+    float f0[16], f1[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const uint32_t wv = *reinterpret_cast<const uint32_t*>(&tile[16 * rq + i][2 * cp]);
+      f0[i] = bf16_lo(wv);
+      f1[i] = bf16_hi(wv);
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      float* f = h ? f1 : f0;
+      if constexpr (kRHT) rht16(f, sgn);
+      float m = 0.f;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) m = absmax_acc(m, f[i]);
+      const uint32_t S = nv_block_scale(m, s_enc_col);
+      const float fb = fb_tab[1][S];
+      uint4 w[4] = {uint4{}, uint4{}, uint4{}, uint4{}};
+      if constexpr (kSR) {
+        const uint64_t g = (p.ctr_off + (uint64_t)((c + h) * R + rr)) >> 2;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) w[j] = keys.words(g + j, 1u);
+      }
+      const uint32_t a = nv_codes8(f, fb, kSR, w[0], w[1]);
+      const uint32_t b = nv_codes8(f + 8, fb, kSR, w[2], w[3]);
+      const int cl = 2 * cp + h;
+      *reinterpret_cast<uint2*>(col_stage + cl * 32 + rq * 8) = make_uint2(a, b);
+      sf_stage[cl * 4 + rq] = (uint8_t)S;
+    }
+    __syncthreads();
+    store_col_staged(p, col_stage, sf_stage, c0, r0, t);
+    return;
+  }
   const int cl = t & 127, rh = t >> 7;
   const int64_t c = c0 + cl, rbase = r0 + rh * 32;
   if (c >= C || rbase >= R) return;
@@ -519,33 +601,6 @@ __global__ void __launch_bounds__(kThreads, KIND == QK_NV2D ? 5 : (KIND != QK_NV
       const int64_t off = p.col_gemm ? sf_gemm_offset(c, kb, p.col_kt) : c * (R >> 5) + kb;
       p.col_sf[off] = (uint8_t)(e + 127);
     }
-  } else if constexpr (KIND == QK_NV) {
-#pragma unroll
-    for (int hb = 0; hb < 2; ++hb) {
-      if (hb * 16 >= nvalid) break;
-      float f[16];
-#pragma unroll
-      for (int i = 0; i < 16; ++i) f[i] = tile_val(tile[rh * 32 + hb * 16 + i], cl);
-      if constexpr (kRHT) rht16(f, sgn);
-      float m = 0.f;
-#pragma unroll
-      for (int i = 0; i < 16; ++i) m = absmax_acc(m, f[i]);
-      const uint32_t S = nv_block_scale(m, s_enc_col);
-      const float fb = fb_tab[1][S];
-      const int64_t rr = rbase + hb * 16;
-      uint4 w[4] = {uint4{}, uint4{}, uint4{}, uint4{}};
-      if constexpr (kSR) {
-        const uint64_t g = (p.ctr_off + (uint64_t)(c * R + rr)) >> 2;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) w[j] = keys.words(g + j, 1u);
-      }
-      const uint32_t a = nv_codes8(f, fb, kSR, w[0], w[1]);
-      const uint32_t b = nv_codes8(f + 8, fb, kSR, w[2], w[3]);
-      *reinterpret_cast<uint2*>(p.col_codes + c * (R >> 1) + (rr >> 1)) = make_uint2(a, b);
-      const int64_t kb = rr >> 4;
-      const int64_t off = p.col_gemm ? sf_gemm_offset(c, kb, p.col_kt) : c * (R >> 4) + kb;
-      p.col_sf[off] = (uint8_t)S;
-    }
   } else if constexpr (KIND == QK_BF16) {
     uint32_t w[16];
 #pragma unroll
@@ -556,6 +611,122 @@ __global__ void __launch_bounds__(kThreads, KIND == QK_NV2D ? 5 : (KIND != QK_NV
     for (int j = 0; j < 4; ++j)
       if (j * 8 < nvalid) *reinterpret_cast<uint4*>(dst + 8 * j) = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
   }
+}
+
+// ---------------------------------------------------------------- NVFP4 2D (16x16 weight tiles)
+// One CTA per 64 x 128 tile; warp w owns the 16 x 64 strip at rows
+// 16 (w / 2), columns 64 (w % 2): lane l loads 8 columns (8 (l % 8)) of rows
+// 4 (l / 8) .. +3, so each load instruction reads four 128-byte row segments.
+// A 16 x 16 tile lives in 8 lanes (lane bits 0, 3, 4), whose shuffle max is
+// the tile max; nothing goes through shared memory.  The codes are the same
+// for both copies (one scale per tile, element-wise encoding), so the
+// column-wise copy is the nibble transpose of the row-wise codes: within a
+// lane (4 rows x 8 columns) by byte permutes, then across the strip's four
+// row groups by shuffles; lane l stores columns 2 (l / 8) and 2 (l / 8) + 1
+// of its 8 as two 8-byte words (16 rows), gathered per column in shared memory.
+__device__ __forceinline__ uint32_t nib_lo4(uint32_t x) {  // low nibbles of 4 bytes -> 16 bits
+  uint32_t y = x & 0x0F0F0F0Fu;
+  y = (y | (y >> 4)) & 0x00FF00FFu;
+  return __byte_perm(y, 0u, 0x4420);
+}
+
+__global__ void __launch_bounds__(kThreads, 4) nv2d_kernel(const QParams p) {
+  __shared__ float fb_tab[128];  // s_enc / dec(S) for the 128 E4M3 codes
+  __shared__ __align__(16) uint8_t col_stage[128 * 32];  // column-wise codes: column, 64 rows
+  __shared__ __align__(4) uint8_t sf_stage[128 * 4];     // column-wise scales: column, 4 row blocks
+  const int t = threadIdx.x, w = t >> 5, l = t & 31;
+  const int chunk = l & 7, rsub = l >> 3;
+  const int64_t R = p.R, C = p.C;
+  const int64_t r0 = (int64_t)blockIdx.y * 64 + 16 * (w >> 1);                // the warp's 16 rows
+  const int64_t cw = (int64_t)blockIdx.x * 128 + 64 * (w & 1) + 8 * chunk;  // the lane's first column
+  // One weight amax: the tile scales use the row copy's encode scale (the
+  // column copy's when only it is requested).
+  const bool use_row = p.row_codes != nullptr;
+  const float s_enc = nv_s_enc(use_row ? p.amax_row : p.amax_col);
+  if (blockIdx.x == 0 && blockIdx.y == 0 && t == 0) {
+    if (p.row_ts) *p.row_ts = nv_ts_dec(p.amax_row);
+    if (p.col_ts) *p.col_ts = nv_ts_dec(p.amax_col);
+  }
+  nv_factor_table(fb_tab, s_enc, t);
+  __syncthreads();
+  // R and C are multiples of 16: a lane's rows and columns are all in range
+  // or all out (then it loads zeros and stores nothing).
+  const bool ok = cw < C && r0 < R;
+  uint4 v[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    v[i] = ok ? ld_stream(p.x + (r0 + 4 * rsub + i) * C + cw) : make_uint4(0u, 0u, 0u, 0u);
+  float m = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float f[8];
+    unpack8(v[i], f);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) m = absmax_acc(m, f[j]);
+  }
+  m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+  m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 8));
+  m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 16));
+  const uint32_t S = nv_block_scale(m, s_enc);
+  const float fb = fb_tab[S];
+  uint32_t q[4];  // codes of row 4 rsub + i: nibble j = column cw + j
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float f[8];
+    unpack8(v[i], f);
+    q[i] = nv_codes8(f, fb, false, uint4{}, uint4{});
+  }
+  if (p.row_codes && ok) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int64_t r = r0 + 4 * rsub + i;
+      *reinterpret_cast<uint32_t*>(p.row_codes + r * (C >> 1) + (cw >> 1)) = q[i];
+      if ((chunk & 1) == 0) {
+        const int64_t kb = cw >> 4;
+        p.row_sf[p.row_gemm ? sf_gemm_offset(r, kb, p.row_kt) : r * (C >> 4) + kb] = (uint8_t)S;
+      }
+    }
+  }
+  if (!p.col_codes) return;
+  // Byte b of q[i] holds columns 2b, 2b+1 of row i.  X[b] = byte b of q[0..3].
+  const uint32_t t01l = __byte_perm(q[0], q[1], 0x5140), t01h = __byte_perm(q[0], q[1], 0x7362);
+  const uint32_t t23l = __byte_perm(q[2], q[3], 0x5140), t23h = __byte_perm(q[2], q[3], 0x7362);
+  const uint32_t X[4] = {__byte_perm(t01l, t23l, 0x5410), __byte_perm(t01l, t23l, 0x7632),
+                         __byte_perm(t01h, t23h, 0x5410), __byte_perm(t01h, t23h, 0x7632)};
+  // H[k]: columns 2k (low 16 bits) and 2k+1 (high 16 bits), nibble i = row 4 rsub + i.
+  uint32_t H[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) H[k] = nib_lo4(X[k]) | (nib_lo4(X[k] >> 4) << 16);
+  // This lane stores columns 2 rsub, 2 rsub + 1: gather H[rsub] of the four row groups.
+  uint32_t G[4];  // G[g] = H[rsub] of row group g
+#pragma unroll
+  for (int g = 0; g < 4; ++g) G[g] = 0u;
+#pragma unroll
+  for (int d = 0; d < 4; ++d) {
+    const int k = rsub ^ d;  // what the partner (row group rsub ^ d) needs from this lane
+    const uint32_t send = k == 0 ? H[0] : k == 1 ? H[1] : k == 2 ? H[2] : H[3];
+    const uint32_t got = d == 0 ? send : __shfl_xor_sync(0xFFFFFFFFu, send, 8 * d);
+#pragma unroll
+    for (int g = 0; g < 4; ++g)
+      if (g == k) G[g] = got;
+  }
+  // The CTA's four row groups write their 8-byte column words and tile
+  // scales to shared memory; then each column's 32 code bytes (64 rows) leave
+  // as two 16-byte stores and its 4 scales as one 4-byte store where the
+  // layout allows (else in pieces).
+  const int rb = w >> 1;
+  if (ok) {
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const uint32_t sel = e ? 0x7632u : 0x5410u;
+      const int cl = 64 * (w & 1) + 8 * chunk + 2 * rsub + e;
+      *reinterpret_cast<uint2*>(col_stage + cl * 32 + rb * 8) =
+          make_uint2(__byte_perm(G[0], G[1], sel), __byte_perm(G[2], G[3], sel));
+      sf_stage[cl * 4 + rb] = (uint8_t)S;
+    }
+  }
+  __syncthreads();
+  store_col_staged(p, col_stage, sf_stage, (int64_t)blockIdx.x * 128, (int64_t)blockIdx.y * 64, t);
 }
 
 // ---------------------------------------------------------------- amax pass
@@ -683,6 +854,13 @@ lpq_status run_tile(const QParams& p, cudaStream_t s) {
   if (grid.y > 65535u) return set_error(LPQ_ERR_SHAPE, "too many rows (%lld) for one launch", (long long)p.R);
   quant_tile_kernel<KIND, kE5M2, NVO><<<grid, kThreads, 0, s>>>(p);
   return cuda_check(cudaGetLastError(), "quantize kernel launch");
+}
+
+lpq_status run_nv2d(const QParams& p, cudaStream_t s) {
+  dim3 grid((unsigned)((p.C + kTC - 1) / kTC), (unsigned)((p.R + 63) / 64));
+  if (grid.y > 65535u) return set_error(LPQ_ERR_SHAPE, "too many rows (%lld) for one launch", (long long)p.R);
+  nv2d_kernel<<<grid, kThreads, 0, s>>>(p);
+  return cuda_check(cudaGetLastError(), "NVFP4 2D kernel launch");
 }
 
 lpq_status run_amax(const uint16_t* x, int64_t R, int64_t C, float* o0, float* o1, float* rht_out,
@@ -836,7 +1014,7 @@ lpq_status launch_quantize(const void* xv, int64_t R, int64_t C, int32_t fmt, in
       }
       p.amax_row = rv ? rv->amax : nullptr;
       p.amax_col = cv ? cv->amax : nullptr;
-      if (fmt == LPQ_NVFP4_2D) return run_tile<QK_NV2D, false>(p, s);
+      if (fmt == LPQ_NVFP4_2D) return run_nv2d(p, s);
       switch ((p.sr ? 1 : 0) | (p.rht ? 2 : 0)) {
         case 0: return run_tile<QK_NV, false, 0>(p, s);
         case 1: return run_tile<QK_NV, false, 1>(p, s);
