@@ -185,6 +185,25 @@ __device__ __forceinline__ void rht16(float t[16], const float sgn[16]) {
   for (int j = 0; j < 16; ++j) t[j] = __fmul_rn(0.25f, t[j]);
 }
 
+// The same transform with the signs taken from a 16-bit mask (bit j set: -1)
+// by flipping sign bits: exact like the multiply, and without the 16
+// registers of the factors (for kernels limited by occupancy, not issue).
+__device__ __forceinline__ void rht16(float t[16], uint32_t signs) {
+#pragma unroll
+  for (int j = 0; j < 16; ++j) t[j] = __uint_as_float(__float_as_uint(t[j]) ^ ((signs << (31 - j)) & 0x80000000u));
+#pragma unroll
+  for (int h = 1; h < 16; h <<= 1)
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      if ((i & h) == 0) {
+        float a = t[i], b = t[i + h];
+        t[i] = __fadd_rn(a, b);
+        t[i + h] = __fsub_rn(a, b);
+      }
+#pragma unroll
+  for (int j = 0; j < 16; ++j) t[j] = __fmul_rn(0.25f, t[j]);
+}
+
 // Stochastic E2M1 rounding of y with random word r: between adjacent
 // magnitudes lo <= |y| <= hi, round up iff float(r >> 8) < ((|y| - lo) /
 // (hi - lo)) * 2^24.  Returned as the rounded value (a grid point with the

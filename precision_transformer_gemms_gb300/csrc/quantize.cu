@@ -4,6 +4,10 @@
 // each CTA reads a tile of the bf16 input once with 16-byte loads into
 // registers and shared memory; the row-wise copy is produced from registers
 // (block max by warp shuffles), the column-wise copy from the shared tile.
+// The 2D NVFP4 kernel needs no shared tile: its 16x16 maxima come from warp
+// shuffles and its column copy is a register transpose of the row codes.
+// Column-wise NVFP4 codes leave as whole 32-byte column segments staged in
+// shared memory.
 //
 // The arithmetic of every format follows these pages:
 //   FP8 E4M3/E5M2, per-tensor scaling, amax history: "Optimizing Transformer
@@ -27,7 +31,8 @@ namespace lpq {
 namespace {
 
 // QK_MX: MXFP8 (E4M3 codes, or E5M2 with kE5M2); QK_MX4: MXFP4 (packed E2M1).
-enum QKind { QK_FP8 = 0, QK_MX = 1, QK_NV = 2, QK_NV2D = 3, QK_BLK1 = 4, QK_BLK128 = 5, QK_BF16 = 6, QK_MX4 = 7 };
+// NVFP4 with 16x16 tiles has a kernel of its own (nv2d_kernel).
+enum QKind { QK_FP8 = 0, QK_MX = 1, QK_NV = 2, QK_BLK1 = 4, QK_BLK128 = 5, QK_BF16 = 6, QK_MX4 = 7 };
 
 struct QParams {
   const uint16_t* x;
@@ -191,14 +196,12 @@ __device__ __forceinline__ void store_col_staged(const QParams& p, const uint8_t
 // registers of the others): bit 0 stochastic rounding, bit 1 RHT of the
 // column-wise copy.
 template <int KIND, bool kE5M2, int NVO = 0>
-__global__ void __launch_bounds__(kThreads, KIND == QK_NV2D ? 5 : (KIND != QK_NV ? 1 : (NVO == 0 ? 6 : (NVO >= 2 ? 4 : 5)))) quant_tile_kernel(const QParams p) {
+__global__ void __launch_bounds__(kThreads, KIND != QK_NV ? 1 : (NVO == 0 ? 6 : (NVO == 3 ? 4 : 5))) quant_tile_kernel(const QParams p) {
   constexpr bool kSR = (NVO & 1) != 0, kRHT = (NVO & 2) != 0;
   constexpr int TR = (KIND == QK_BLK1 || KIND == QK_BLK128) ? 128 : 64;
   __shared__ __align__(16) uint16_t tile[TR][kTC];
   __shared__ float red[kThreads / 32];
   __shared__ float part[2][kTC];
-  __shared__ float tile_f[32];
-  __shared__ uint32_t tile_s[32];
   __shared__ float fb_tab[2][128];  // NVFP4: s_enc / dec(S) for the row and column copies
   // NVFP4 column-wise copy staged per column (64 rows: 32 code bytes, 4 scales)
   __shared__ __align__(16) uint8_t col_stage[KIND == QK_NV ? 128 * 32 : 16];
@@ -207,7 +210,7 @@ __global__ void __launch_bounds__(kThreads, KIND == QK_NV2D ? 5 : (KIND != QK_NV
   const int t = threadIdx.x;
   const int64_t r0 = (int64_t)blockIdx.y * TR, c0 = (int64_t)blockIdx.x * kTC;
   // The shared tile feeds the column-wise copy and the 2D / 128x128 scales.
-  const bool kNeedTile = p.col_codes != nullptr || KIND == QK_NV2D || KIND == QK_BLK128;
+  const bool kNeedTile = p.col_codes != nullptr || KIND == QK_BLK128;
   const int64_t R = p.R, C = p.C;
   constexpr float kFmax = kE5M2 ? 57344.0f : 448.0f;
 
@@ -227,15 +230,19 @@ __global__ void __launch_bounds__(kThreads, KIND == QK_NV2D ? 5 : (KIND != QK_NV
     }
   }
   float s_enc_row = 1.f, s_enc_col = 1.f;
-  float sgn[16];
-  if constexpr (KIND == QK_NV || KIND == QK_NV2D) {
+  float sgn[16];     // RHT sign factors (with stochastic rounding: multiplies on the FMA pipe)
+  uint32_t sgn_mask = 0;  // RHT signs as bits (without: fewer registers, more CTAs per SM)
+  if constexpr (KIND == QK_NV) {
     if (p.row_codes) s_enc_row = nv_s_enc(p.amax_row);
     if (p.col_codes) s_enc_col = nv_s_enc(p.amax_col);
     if (blockIdx.x == 0 && blockIdx.y == 0 && t == 0) {
       if (p.row_ts) *p.row_ts = nv_ts_dec(p.amax_row);
       if (p.col_ts) *p.col_ts = nv_ts_dec(p.amax_col);
     }
-    if constexpr (kRHT) rht_sign_factors(rht_signs(p.rht_seed), sgn);
+    if constexpr (kRHT) {
+      sgn_mask = rht_signs(p.rht_seed);
+      if constexpr (kSR) rht_sign_factors(sgn_mask, sgn);
+    }
     nv_factor_table(fb_tab[0], s_enc_row, t);
     nv_factor_table(fb_tab[1], s_enc_col, t - 128);
     __syncthreads();
@@ -373,81 +380,7 @@ __global__ void __launch_bounds__(kThreads, KIND == QK_NV2D ? 5 : (KIND != QK_NV
   if (!kNeedTile) return;
   __syncthreads();
 
-  // ---------------------------------------------------------------- 2D / 128x128 tiles
-  if constexpr (KIND == QK_NV2D) {
-    {
-      const int tid = t >> 3, sub = t & 7;  // 32 tiles of 16x16, 8 threads each
-      const int tr = tid >> 3, tc = tid & 7;
-      float m = 0.f;
-#pragma unroll
-      for (int rr = 0; rr < 2; ++rr)
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {  // 16-byte shared loads of 8 values
-          float f[8];
-          unpack8(*reinterpret_cast<const uint4*>(&tile[tr * 16 + sub * 2 + rr][tc * 16 + 8 * h]), f);
-#pragma unroll
-          for (int i = 0; i < 8; ++i) m = absmax_acc(m, f[i]);
-        }
-      m = warp_max_xor(m, 8);
-      if (sub == 0) {
-        const float s_enc = p.row_codes ? s_enc_row : s_enc_col;
-        const uint32_t S = nv_block_scale(m, s_enc);
-        tile_s[tid] = S;
-        tile_f[tid] = fb_tab[p.row_codes ? 0 : 1][S];
-      }
-    }
-    __syncthreads();
-    if (p.row_codes) {
-#pragma unroll
-      for (int it = 0; it < TR / 16; ++it) {
-        const int rl = it * 16 + lr;
-        const int64_t r = r0 + rl;
-        if (!(col_ok && r < R)) continue;
-        const int tid = (rl >> 4) * 8 + (lc >> 4);
-        float f[8];
-        unpack8(vbuf[it], f);  // this thread's own loaded values of the row
-        const uint32_t q = nv_codes8(f, tile_f[tid], false, uint4{}, uint4{});
-        *reinterpret_cast<uint32_t*>(p.row_codes + r * (C >> 1) + ((c0 + lc) >> 1)) = q;
-        if ((t & 1) == 0) {
-          const int64_t kb = (c0 + lc) >> 4;
-          const int64_t off = p.row_gemm ? sf_gemm_offset(r, kb, p.row_kt) : r * (C >> 4) + kb;
-          p.row_sf[off] = (uint8_t)tile_s[tid];
-        }
-      }
-    }
-    if (p.col_codes) {
-      // Two adjacent columns per thread, one 16-row block: each 4-byte shared
-      // load gives a row's values of both columns (both in the same 16x16 tile).
-      const int cp = t & 63, rq = t >> 6;
-      const int cl = 2 * cp;
-      const int64_t c = c0 + cl, rr = r0 + rq * 16;
-      if (c < C && rr < R) {
-        const int tid = rq * 8 + (cl >> 4);
-        float f0[16], f1[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const uint32_t w = *reinterpret_cast<const uint32_t*>(&tile[rq * 16 + i][cl]);
-          f0[i] = bf16_lo(w);
-          f1[i] = bf16_hi(w);
-        }
-        const float fb = tile_f[tid];
-        const int64_t kb = rr >> 4;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int64_t cc = c + h;
-          if (cc >= C) break;
-          const float* v = h ? f1 : f0;
-          const uint32_t a = nv_codes8(v, fb, false, uint4{}, uint4{});
-          const uint32_t b = nv_codes8(v + 8, fb, false, uint4{}, uint4{});
-          *reinterpret_cast<uint2*>(p.col_codes + cc * (R >> 1) + (rr >> 1)) = make_uint2(a, b);
-          const int64_t off = p.col_gemm ? sf_gemm_offset(cc, kb, p.col_kt) : cc * (R >> 4) + kb;
-          p.col_sf[off] = (uint8_t)tile_s[tid];
-        }
-      }
-    }
-    return;
-  }
-
+  // ---------------------------------------------------------------- 128x128 tiles
   if constexpr (KIND == QK_BLK128) {
     const float m = block_max(local_amax, red);
     const float s = finite_pos(m) ? __fdiv_rn(448.0f, m) : 1.0f;
@@ -534,7 +467,9 @@ __global__ void __launch_bounds__(kThreads, KIND == QK_NV2D ? 5 : (KIND != QK_NV
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       float* f = h ? f1 : f0;
-      if constexpr (kRHT) rht16(f, sgn);
+      if constexpr (kRHT) {
+        if constexpr (kSR) rht16(f, sgn); else rht16(f, sgn_mask);
+      }
       float m = 0.f;
 #pragma unroll
       for (int i = 0; i < 16; ++i) m = absmax_acc(m, f[i]);
