@@ -196,7 +196,7 @@ __device__ __forceinline__ void store_col_staged(const QParams& p, const uint8_t
 // registers of the others): bit 0 stochastic rounding, bit 1 RHT of the
 // column-wise copy.
 template <int KIND, bool kE5M2, int NVO = 0>
-__global__ void __launch_bounds__(kThreads, KIND != QK_NV ? 1 : (NVO == 0 ? 6 : (NVO == 3 ? 4 : 5))) quant_tile_kernel(const QParams p) {
+__global__ void __launch_bounds__(kThreads, KIND != QK_NV ? 1 : (NVO == 0 ? 6 : 5)) quant_tile_kernel(const QParams p) {
   constexpr bool kSR = (NVO & 1) != 0, kRHT = (NVO & 2) != 0;
   constexpr int TR = (KIND == QK_BLK1 || KIND == QK_BLK128) ? 128 : 64;
   __shared__ __align__(16) uint16_t tile[TR][kTC];
@@ -230,8 +230,7 @@ __global__ void __launch_bounds__(kThreads, KIND != QK_NV ? 1 : (NVO == 0 ? 6 : 
     }
   }
   float s_enc_row = 1.f, s_enc_col = 1.f;
-  float sgn[16];     // RHT sign factors (with stochastic rounding: multiplies on the FMA pipe)
-  uint32_t sgn_mask = 0;  // RHT signs as bits (without: fewer registers, more CTAs per SM)
+  uint32_t sgn_mask = 0;  // RHT signs as bits (flips of the sign bit; no registers of factors)
   if constexpr (KIND == QK_NV) {
     if (p.row_codes) s_enc_row = nv_s_enc(p.amax_row);
     if (p.col_codes) s_enc_col = nv_s_enc(p.amax_col);
@@ -239,10 +238,7 @@ __global__ void __launch_bounds__(kThreads, KIND != QK_NV ? 1 : (NVO == 0 ? 6 : 
       if (p.row_ts) *p.row_ts = nv_ts_dec(p.amax_row);
       if (p.col_ts) *p.col_ts = nv_ts_dec(p.amax_col);
     }
-    if constexpr (kRHT) {
-      sgn_mask = rht_signs(p.rht_seed);
-      if constexpr (kSR) rht_sign_factors(sgn_mask, sgn);
-    }
+    if constexpr (kRHT) sgn_mask = rht_signs(p.rht_seed);
     nv_factor_table(fb_tab[0], s_enc_row, t);
     nv_factor_table(fb_tab[1], s_enc_col, t - 128);
     __syncthreads();
@@ -467,9 +463,7 @@ __global__ void __launch_bounds__(kThreads, KIND != QK_NV ? 1 : (NVO == 0 ? 6 : 
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       float* f = h ? f1 : f0;
-      if constexpr (kRHT) {
-        if constexpr (kSR) rht16(f, sgn); else rht16(f, sgn_mask);
-      }
+      if constexpr (kRHT) rht16(f, sgn_mask);
       float m = 0.f;
 #pragma unroll
       for (int i = 0; i < 16; ++i) m = absmax_acc(m, f[i]);
