@@ -4,18 +4,22 @@
 // for low-precision training", autocast vs pre-quantize: the 12 GEMMs of a
 // layer, benchmarked separately per pass).
 //
-// One CTA computes a 128 x BN output tile.  Warp 0 (one lane) streams A/B
-// tiles into a shared-memory ring with TMA (128-byte swizzle) and the block
-// scale factors with bulk copies; warp 1 (one lane) moves scale factors into
-// TMEM (tcgen05.cp) and issues the tcgen05.mma instructions, accumulating in
-// FP32 in TMEM; all four warps then read the accumulator back with
-// tcgen05.ld, apply the per-tensor scale product and store bf16 or FP32.
+// Persistent, warp-specialized kernels.  Warp 0 (one lane) streams A/B tiles
+// into a shared-memory ring with TMA (128-byte swizzle) and the block scale
+// factors with bulk or TMA copies; warp 1 (one lane) issues the tcgen05.mma
+// instructions, accumulating in FP32 in TMEM; for the block-scaled kinds four
+// scale warps write each stage's scale factors into a TMEM slot with
+// tcgen05.st (or, LPQ_GEMM_SFCP=1, the MMA thread copies them with
+// tcgen05.cp); eight epilogue warps read the accumulator back with
+// tcgen05.ld, apply the per-tensor scale product and store bf16 or FP32.  The
+// default for M >= 256 is a CTA pair (cta_group::2) per 256 x 256 tile.
 //
 // Kinds: kind::f16 (bf16 x bf16), kind::f8f6f4 (per-tensor E4M3/E5M2),
-// kind::mxf8f6f4.block_scale (MXFP8: E4M3 with an E8M0 scale per 32 values,
-// "Faster training throughput in FP8 with NVIDIA NeMo", MXFP8) and
-// kind::mxf4nvf4.block_scale (NVFP4: E2M1 with an E4M3 scale per 16 values and
-// an FP32 tensor scale, "Accelerate LLM training with NVFP4 on Blackwell").
+// kind::mxf8f6f4.block_scale (MXFP8: E4M3 or E5M2 with an E8M0 scale per 32
+// values, "Faster training throughput in FP8 with NVIDIA NeMo", MXFP8),
+// kind::mxf4nvf4.block_scale.scale_vec::4X (NVFP4: E2M1 with an E4M3 scale per
+// 16 values and an FP32 tensor scale, "Accelerate LLM training with NVFP4 on
+// Blackwell") and scale_vec::2X (MXFP4: E2M1 with an E8M0 scale per 32).
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_bf16.h>
@@ -230,7 +234,7 @@ __global__ void __launch_bounds__(kThreadsGemm + (SFST ? 32 * kSfWarps : 0))
           tc_fence_after();
           const uint32_t alo = a0 + s * (CF::kA >> 4), blo = b0 + s * (CF::kB >> 4);
           const uint32_t falo = fa0 + s * (CF::kSfa >> 4), fblo = fb0 + s * (CF::kSfb >> 4);
-          if constexpr (KIND == kKindMXF8) {
+          if constexpr (KIND == kKindMXF8 && !SFST) {
             tmem_cp_sf(tmem_sfa, ((uint64_t)kHiSf << 32) | falo);
 #pragma unroll
             for (int i = 0; i < BN / 128; ++i) tmem_cp_sf(tmem_sfb + 4 * i, ((uint64_t)kHiSf << 32) | (fblo + i * 32));
@@ -242,7 +246,7 @@ __global__ void __launch_bounds__(kThreadsGemm + (SFST ? 32 * kSfWarps : 0))
             const uint32_t acc = (kt > 0 || j > 0) ? 1u : 0u;
             if constexpr (KIND == kKindF16 || KIND == kKindF8F6F4) {
               mma_ss<KIND>(tmem_d, ad, bd, g.idesc, acc);
-            } else if constexpr (KIND == kKindMXF8) {
+            } else if constexpr (KIND == kKindMXF8 && !SFST) {
               mma_bs<KIND>(tmem_d, ad, bd, g.idesc | ((uint32_t)j << 4) | ((uint32_t)j << 29), tmem_sfa, tmem_sfb, acc);
             } else if constexpr (SFST) {
               const int at = j * CF::kSfAtoms / 4;  // the MMA's scale atom
@@ -665,7 +669,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm + (SFST
           tc_fence_after();
           const uint32_t alo = a0 + s * (PC::kA >> 4), blo = b0 + s * (PC::kB >> 4);
           const uint32_t falo = fa0 + s * (PC::kSfa >> 4), fblo = fb0 + s * (PC::kSfb >> 4);
-          if constexpr (KIND == kKindMXF8) {
+          if constexpr (KIND == kKindMXF8 && !SFST) {
             tmem_cp_sf_pair(tmem_sfa, ((uint64_t)kHiSf << 32) | falo);
 #pragma unroll
             for (int i = 0; i < PC::kSfbGroups; ++i)
@@ -678,7 +682,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm + (SFST
             const uint32_t acc = (kt > 0 || j > 0) ? 1u : 0u;
             if constexpr (KIND == kKindF16 || KIND == kKindF8F6F4) {
               mma_pair<KIND>(tmem_d, ad, bd, g.idesc, acc);
-            } else if constexpr (KIND == kKindMXF8) {
+            } else if constexpr (KIND == kKindMXF8 && !SFST) {
               mma_pair_bs<KIND>(tmem_d, ad, bd, g.idesc | ((uint32_t)j << 4) | ((uint32_t)j << 29), tmem_sfa, tmem_sfb,
                                 acc);
             } else if constexpr (SFST) {
@@ -1215,20 +1219,26 @@ lpq_status launch_gemm(const lpq_qview* a, const lpq_qview* b, void* c, int32_t 
     g.sfa_kt = sf_kt_atoms(LPQ_MXFP8, k);
     g.sfb_kt = g.sfa_kt;
     g.sfb_groups = sf_row_groups(n);
+    // scale atoms into TMEM by the scale warps (tcgen05.st); LPQ_GEMM_SFCP=1:
+    // tcgen05.cp by the MMA thread
+    const bool cp = getenv_flag("LPQ_GEMM_SFCP");
     if (use_pair(kKindMXF8) && m >= 256) {
       CUtensorMap tsa, tsb;
       if ((st = make_map(&tb, b->codes, false, k, n, k, 128, kPairBN / 2)) != LPQ_OK) return st;
       if ((st = make_sf_map(&tsa, g.sfa, sf_row_groups(m) * g.sfa_kt, 1)) != LPQ_OK) return st;
       if ((st = make_sf_map(&tsb, g.sfb, g.sfb_groups * g.sfb_kt, 1)) != LPQ_OK) return st;
       g.idesc = (g.idesc & ~(31u << 24)) | (16u << 24);
-      return run_pair<kKindMXF8, true>(ta, tb, tsa, tsb, g, s);
+      if (cp) return run_pair<kKindMXF8, true>(ta, tb, tsa, tsb, g, s);
+      return run_pair<kKindMXF8, true, true>(ta, tb, tsa, tsb, g, s);
     }
     if (nv_bn == 128) {
       if ((st = make_map(&tb, b->codes, false, k, n, k, 128, 128)) != LPQ_OK) return st;
       g.idesc = idesc_block_scaled(af, bf, 1, 128);
-      return run<kKindMXF8, 128, 2>(ta, tb, g, s);
+      if (cp) return run<kKindMXF8, 128, 2>(ta, tb, g, s);
+      return run<kKindMXF8, 128, 2, true>(ta, tb, g, s);
     }
-    return run<kKindMXF8, BN, 1>(ta, tb, g, s);
+    if (cp) return run<kKindMXF8, BN, 1>(ta, tb, g, s);
+    return run<kKindMXF8, BN, 1, true>(ta, tb, g, s);
   }
   if (fa == LPQ_MXFP4) {
     // packed E2M1 (format 1) with an E8M0 scale per 32 values: two scales per
@@ -1274,25 +1284,23 @@ lpq_status launch_gemm(const lpq_qview* a, const lpq_qview* b, void* c, int32_t 
     g.sfb_groups = sf_row_groups(n);
     g.alpha_a = a->tensor_scale;
     g.alpha_b = b->tensor_scale;
+    const bool cp = getenv_flag("LPQ_GEMM_SFCP");  // scale copies by the MMA thread (tcgen05.cp)
     if (use_pair(kKindNVF4) && m >= 256) {
       CUtensorMap tsa, tsb;
       if ((st = make_map(&tb, b->codes, false, k / 2, n, k / 2, 128, kPairBN / 2)) != LPQ_OK) return st;
       if ((st = make_sf_map(&tsa, g.sfa, sf_row_groups(m) * g.sfa_kt, 4)) != LPQ_OK) return st;
       if ((st = make_sf_map(&tsb, g.sfb, g.sfb_groups * g.sfb_kt, 4)) != LPQ_OK) return st;
       g.idesc = (g.idesc & ~(31u << 24)) | (16u << 24);
-      const char* e = getenv("LPQ_GEMM_SFCP");
-      if (e && e[0] == '1') return run_pair<kKindNVF4, true>(ta, tb, tsa, tsb, g, s);
+      if (cp) return run_pair<kKindNVF4, true>(ta, tb, tsa, tsb, g, s);
       return run_pair<kKindNVF4, true, true>(ta, tb, tsa, tsb, g, s);
     }
     if (nv_bn == 128) {
       if ((st = make_map(&tb, b->codes, false, k / 2, n, k / 2, 128, 128)) != LPQ_OK) return st;
       g.idesc = idesc_block_scaled(1, 1, 0, 128);
-      const char* e = getenv("LPQ_GEMM_SFCP");
-      if (e && e[0] == '1') return run<kKindNVF4, 128, 2>(ta, tb, g, s);
+      if (cp) return run<kKindNVF4, 128, 2>(ta, tb, g, s);
       return run<kKindNVF4, 128, 2, true>(ta, tb, g, s);
     }
-    const char* e = getenv("LPQ_GEMM_SFCP");  // =1: scale copies by the MMA thread (tcgen05.cp)
-    if (e && e[0] == '1') return run<kKindNVF4, BN, 1>(ta, tb, g, s);
+    if (cp) return run<kKindNVF4, BN, 1>(ta, tb, g, s);
     return run<kKindNVF4, BN, 1, true>(ta, tb, g, s);
   }
   if (fa == LPQ_FP8_BLOCK_1x128 || fa == LPQ_FP8_BLOCK_128x128) {

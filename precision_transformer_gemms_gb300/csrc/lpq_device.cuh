@@ -443,11 +443,12 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32
       "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31]) : "memory");
 }
 
-// Store N (8, 16 or 32) consecutive 32-bit columns.
+// Store N (4, 8, 16 or 32) consecutive 32-bit columns.
 template <int N>
 __device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const uint32_t (&v)[N]) {
-  static_assert(N == 8 || N == 16 || N == 32, "8, 16 or 32 columns");
-  if constexpr (N == 8) tmem_st8(taddr, v);
+  static_assert(N == 4 || N == 8 || N == 16 || N == 32, "4, 8, 16 or 32 columns");
+  if constexpr (N == 4) tmem_st4(taddr, v[0], v[1], v[2], v[3]);
+  else if constexpr (N == 8) tmem_st8(taddr, v);
   else if constexpr (N == 16) tmem_st16(taddr, v);
   else tmem_st32(taddr, v);
 }

@@ -42,13 +42,13 @@ def check(a, b, M, N, K, out_fp32, layout=lpq.FPROP):
                                   (lpq.MXFP8_E5M2, lpq.MXFP8_E5M2), (lpq.MXFP4, lpq.MXFP4),
                                   (lpq.NVFP4, lpq.NVFP4), (lpq.NVFP4, lpq.NVFP4_2D)])
 def test_gemm_parity(fmts, shape, out_fp32, path, monkeypatch):
-    """Every kernel path: one CTA per 128 x 256 tile (NVFP4 scales stored into
+    """Every kernel path: one CTA per 128 x 256 tile (block scales stored into
     TMEM by scale warps, or copied by the MMA thread: single_cp), one CTA per
     128 x 128 tile with two accumulators (block-scaled kinds: single_bn128), and
     CTA pairs (cta_group::2) per 256 x 256 tile, whose bf16 output leaves
     through TMA tile stores (pair) or direct stores (pair_direct)."""
-    if path == "single_cp" and fmts[0] not in (lpq.NVFP4, lpq.MXFP4):
-        pytest.skip("scale-copy variant exists for the FP4 kinds only")
+    if path == "single_cp" and fmts[0] not in (lpq.NVFP4, lpq.MXFP4, lpq.MXFP8, lpq.MXFP8_E5M2):
+        pytest.skip("scale-copy variant exists for the block-scaled kinds only")
     if path == "single_bn128" and fmts[0] not in (lpq.NVFP4, lpq.MXFP8, lpq.MXFP8_E5M2, lpq.MXFP4):
         pytest.skip("128-wide tiles exist for the block-scaled kinds only")
     monkeypatch.setenv("LPQ_GEMM_PAIR", "1" if path.startswith("pair") else "0")
