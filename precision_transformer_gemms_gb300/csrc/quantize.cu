@@ -194,9 +194,11 @@ __device__ __forceinline__ void store_col_staged(const QParams& p, const uint8_t
 
 // NVO (NVFP4 options, compile-time so that the plain paths carry none of the
 // registers of the others): bit 0 stochastic rounding, bit 1 RHT of the
-// column-wise copy.
+// column-wise copy.  CTAs per SM: six for the plain path (40 registers),
+// four for stochastic rounding alone (64 registers, no spills; faster than
+// five with spills), five with the RHT (47-48 registers).
 template <int KIND, bool kE5M2, int NVO = 0>
-__global__ void __launch_bounds__(kThreads, KIND != QK_NV ? 1 : (NVO == 0 ? 6 : 5)) quant_tile_kernel(const QParams p) {
+__global__ void __launch_bounds__(kThreads, KIND != QK_NV ? 1 : (NVO == 0 ? 6 : (NVO == 1 ? 4 : 5))) quant_tile_kernel(const QParams p) {
   constexpr bool kSR = (NVO & 1) != 0, kRHT = (NVO & 2) != 0;
   constexpr int TR = (KIND == QK_BLK1 || KIND == QK_BLK128) ? 128 : 64;
   __shared__ __align__(16) uint16_t tile[TR][kTC];
