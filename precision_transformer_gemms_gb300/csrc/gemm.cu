@@ -347,8 +347,10 @@ __global__ void __launch_bounds__(kThreadsGemm + (SFST ? 32 * kSfWarps : 0))
           tmem_ld32(tbase + (uint32_t)(cc * 32), v);
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            __nv_bfloat162 h = __floats2bfloat162_rn(__fmul_rn(__uint_as_float(v[2 * i]), alpha),
-                                                     __fmul_rn(__uint_as_float(v[2 * i + 1]), alpha));
+            // one packed two-wide multiply (each half rounded like __fmul_rn), one packed convert
+            const float2 y = __fmul2_rn(make_float2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])),
+                                        make_float2(alpha, alpha));
+            __nv_bfloat162 h = __floats2bfloat162_rn(y.x, y.y);
             pk[cc * 16 + i] = *reinterpret_cast<uint32_t*>(&h);
           }
         }
@@ -780,8 +782,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm + (SFST
           tmem_ld32(tbase + (uint32_t)(cc * 32), v);
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            __nv_bfloat162 h = __floats2bfloat162_rn(__fmul_rn(__uint_as_float(v[2 * i]), alpha),
-                                                     __fmul_rn(__uint_as_float(v[2 * i + 1]), alpha));
+            // one packed two-wide multiply (each half rounded like __fmul_rn), one packed convert
+            const float2 y = __fmul2_rn(make_float2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])),
+                                        make_float2(alpha, alpha));
+            __nv_bfloat162 h = __floats2bfloat162_rn(y.x, y.y);
             pk[cc * 16 + i] = *reinterpret_cast<uint32_t*>(&h);
           }
         }
