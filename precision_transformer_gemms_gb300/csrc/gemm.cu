@@ -82,7 +82,7 @@ struct Cfg {
 constexpr int kGroupM = 16;  // tiles along M that share a band of B tiles (L2 reuse)
 constexpr int kEpiWarps = 8;  // two per TMEM lane quarter, each owning half of the tile's columns
 constexpr int kThreadsGemm = 64 + 32 * kEpiWarps;
-constexpr int kSfWarps = 4;  // scale-store warps of the NVFP4 kernel, one per TMEM lane quarter
+constexpr int kSfWarps = 4;  // scale-store warps of the block-scaled kernels, one per TMEM lane quarter
 
 struct GemmArgs {
   const uint8_t* sfa;  // tensor-core scale layout of A (block-scaled kinds)
@@ -274,46 +274,47 @@ __global__ void __launch_bounds__(kThreadsGemm + (SFST ? 32 * kSfWarps : 0))
     }
   } else if (SFST && warp >= 2 + kEpiWarps) {
     if constexpr (SFST) {  // only kernels with scale warps carry this code
-    // ------------------------------------------------------------ scale warps (NVFP4)
-    // Per k-step: once the stage's previous MMAs are done (its TMEM scale slot
-    // is free), this warp's lane quarter of the step's 12 scale atoms goes
-    // from shared memory into the slot with tcgen05.st (replicated in every
-    // quarter), and the warp arrives on the stage's full barrier.
-    const int q = warp & 3;
-    const uint32_t lanes = (uint32_t)(q * 32) << 16;
-    uint32_t s = 0, ph = 0;
-    bool ok = true;
-    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-      for (int kt = 0; kt < g.num_k; ++kt) {
-        if (!(ok = mbar_wait_bounded(&sfd[s], ph, abort_flag, &g_device_error))) break;
-        if (!(ok = mbar_wait_bounded(&empty[s], ph ^ 1u, abort_flag, &g_device_error))) break;  // slot free
-        __syncwarp();
-        tc_fence_after();
-        constexpr int NA = CF::kSfAtoms, G = BN / 128;
-        const uint4* fa = reinterpret_cast<const uint4*>(sSfa + s * CF::kSfa) + lane;  // atom j line `lane`
-        const uint4* fb = reinterpret_cast<const uint4*>(sSfb + s * CF::kSfb) + lane;
-        uint32_t va[4 * NA], vb[4 * NA * G];
+      // ------------------------------------------------------------ scale warps (block-scaled kinds)
+      // Per k-step: once the stage's previous MMAs are done (its TMEM scale slot
+      // is free), this warp's lane quarter of the step's scale atoms (per 128
+      // rows: 1 MXFP8, 2 MXFP4, 4 NVFP4) goes from shared memory into the slot
+      // with tcgen05.st (replicated in every quarter), and the warp arrives on
+      // the stage's full barrier.
+      const int q = warp & 3;
+      const uint32_t lanes = (uint32_t)(q * 32) << 16;
+      uint32_t s = 0, ph = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        for (int kt = 0; kt < g.num_k; ++kt) {
+          if (!(ok = mbar_wait_bounded(&sfd[s], ph, abort_flag, &g_device_error))) break;
+          if (!(ok = mbar_wait_bounded(&empty[s], ph ^ 1u, abort_flag, &g_device_error))) break;  // slot free
+          __syncwarp();
+          tc_fence_after();
+          constexpr int NA = CF::kSfAtoms, G = BN / 128;
+          const uint4* fa = reinterpret_cast<const uint4*>(sSfa + s * CF::kSfa) + lane;  // atom j line `lane`
+          const uint4* fb = reinterpret_cast<const uint4*>(sSfb + s * CF::kSfb) + lane;
+          uint32_t va[4 * NA], vb[4 * NA * G];
 #pragma unroll
-        for (int j = 0; j < NA; ++j) {
-          const uint4 x = fa[j * 32];
-          va[4 * j] = x.x; va[4 * j + 1] = x.y; va[4 * j + 2] = x.z; va[4 * j + 3] = x.w;
+          for (int j = 0; j < NA; ++j) {
+            const uint4 x = fa[j * 32];
+            va[4 * j] = x.x; va[4 * j + 1] = x.y; va[4 * j + 2] = x.z; va[4 * j + 3] = x.w;
 #pragma unroll
-          for (int i = 0; i < G; ++i) {
-            const uint4 y = fb[(i * NA + j) * 32];
-            const int c = 4 * G * j + 4 * i;
-            vb[c] = y.x; vb[c + 1] = y.y; vb[c + 2] = y.z; vb[c + 3] = y.w;
+            for (int i = 0; i < G; ++i) {
+              const uint4 y = fb[(i * NA + j) * 32];
+              const int c = 4 * G * j + 4 * i;
+              vb[c] = y.x; vb[c + 1] = y.y; vb[c + 2] = y.z; vb[c + 3] = y.w;
+            }
           }
+          const uint32_t base = tmem_base + NACC * BN + s * (CF::kSfaCols + CF::kSfbCols) + lanes;
+          tmem_st_cols(base, va);
+          tmem_st_cols(base + CF::kSfaCols, vb);
+          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&full[s]);
+          if (++s == (uint32_t)S) { s = 0; ph ^= 1u; }
         }
-        const uint32_t base = tmem_base + NACC * BN + s * (CF::kSfaCols + CF::kSfbCols) + lanes;
-        tmem_st_cols(base, va);
-        tmem_st_cols(base + CF::kSfaCols, vb);
-        tmem_wait_st();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&full[s]);
-        if (++s == (uint32_t)S) { s = 0; ph ^= 1u; }
       }
-    }
     }  // SFST
   } else if (warp >= 2) {
     // ------------------------------------------------------------ epilogue
@@ -713,46 +714,46 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm + (SFST
     }
   } else if (run && SFST && warp >= 2 + kEpiWarps) {
     if constexpr (SFST) {  // only kernels with scale warps carry this code
-    // scale warps: this CTA's lane quarter of the step's scale atoms (its own A
-    // rows, all 256 B rows) from shared memory into the TMEM slot; both CTAs'
-    // scale warps report to the even CTA's slot barrier
-    const int q = warp & 3;
-    const uint32_t lanes = (uint32_t)(q * 32) << 16;
-    uint32_t s = 0, ph = 0;
-    bool ok = true;
-    for (int t = pair; t < total && ok; t += npairs) {
-      for (int kt = 0; kt < g.num_k; ++kt) {
-        if (!(ok = mbar_wait_bounded(&sfd[s], ph, abort_flag, &g_device_error))) break;  // own scale atoms
-        if (!(ok = mbar_wait_bounded(&empty[s], ph ^ 1u, abort_flag, &g_device_error))) break;  // slot free
-        __syncwarp();
-        tc_fence_after();
-        constexpr int NA = PC::kSfAtoms, G = PC::kSfbGroups;
-        const uint4* fa = reinterpret_cast<const uint4*>(sSfa + s * PC::kSfa) + lane;
-        const uint4* fb = reinterpret_cast<const uint4*>(sSfb + s * PC::kSfb) + lane;
-        uint32_t va[4 * NA], vb[4 * NA * G];
+      // scale warps: this CTA's lane quarter of the step's scale atoms (its own A
+      // rows, all 256 B rows) from shared memory into the TMEM slot; both CTAs'
+      // scale warps report to the even CTA's slot barrier
+      const int q = warp & 3;
+      const uint32_t lanes = (uint32_t)(q * 32) << 16;
+      uint32_t s = 0, ph = 0;
+      bool ok = true;
+      for (int t = pair; t < total && ok; t += npairs) {
+        for (int kt = 0; kt < g.num_k; ++kt) {
+          if (!(ok = mbar_wait_bounded(&sfd[s], ph, abort_flag, &g_device_error))) break;  // own scale atoms
+          if (!(ok = mbar_wait_bounded(&empty[s], ph ^ 1u, abort_flag, &g_device_error))) break;  // slot free
+          __syncwarp();
+          tc_fence_after();
+          constexpr int NA = PC::kSfAtoms, G = PC::kSfbGroups;
+          const uint4* fa = reinterpret_cast<const uint4*>(sSfa + s * PC::kSfa) + lane;
+          const uint4* fb = reinterpret_cast<const uint4*>(sSfb + s * PC::kSfb) + lane;
+          uint32_t va[4 * NA], vb[4 * NA * G];
 #pragma unroll
-        for (int j = 0; j < NA; ++j) {
-          const uint4 x = fa[j * 32];
-          va[4 * j] = x.x; va[4 * j + 1] = x.y; va[4 * j + 2] = x.z; va[4 * j + 3] = x.w;
+          for (int j = 0; j < NA; ++j) {
+            const uint4 x = fa[j * 32];
+            va[4 * j] = x.x; va[4 * j + 1] = x.y; va[4 * j + 2] = x.z; va[4 * j + 3] = x.w;
 #pragma unroll
-          for (int i = 0; i < G; ++i) {
-            const uint4 y = fb[(i * NA + j) * 32];
-            const int c = 4 * G * j + 4 * i;
-            vb[c] = y.x; vb[c + 1] = y.y; vb[c + 2] = y.z; vb[c + 3] = y.w;
+            for (int i = 0; i < G; ++i) {
+              const uint4 y = fb[(i * NA + j) * 32];
+              const int c = 4 * G * j + 4 * i;
+              vb[c] = y.x; vb[c + 1] = y.y; vb[c + 2] = y.z; vb[c + 3] = y.w;
+            }
           }
+          const uint32_t base = tmem_sfa + s * (PC::kSfaCols + PC::kSfbCols) + lanes;
+          tmem_st_cols(base, va);
+          tmem_st_cols(base + PC::kSfaCols, vb);
+          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) {
+            if (leader) mbar_arrive(&full[s]); else mbar_arrive_remote_relaxed(full_leader + 8 * s);
+          }
+          if (++s == (uint32_t)S) { s = 0; ph ^= 1u; }
         }
-        const uint32_t base = tmem_sfa + s * (PC::kSfaCols + PC::kSfbCols) + lanes;
-        tmem_st_cols(base, va);
-        tmem_st_cols(base + PC::kSfaCols, vb);
-        tmem_wait_st();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) {
-          if (leader) mbar_arrive(&full[s]); else mbar_arrive_remote_relaxed(full_leader + 8 * s);
-        }
-        if (++s == (uint32_t)S) { s = 0; ph ^= 1u; }
       }
-    }
     }  // SFST
   } else if (run && warp >= 2) {
     constexpr int HALF = kPairBN / 2;
