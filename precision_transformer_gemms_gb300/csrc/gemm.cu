@@ -951,25 +951,46 @@ struct BlockArgs {
 
 constexpr int kBlkBN = 128;
 constexpr int kBlkStages = 6;
+constexpr int kBlkBufs = 4;   // TMEM partial buffers (4 x 128 columns): the MMA warp runs up to 3 slices ahead
+constexpr int kBlkAhead = 2;  // slices ahead that the epilogue fetches its factors
 constexpr int kBlkStage = kBM * kKBytes + kBlkBN * kKBytes;
-constexpr int kBlkSmem = kBlkStages * kBlkStage + 1024 + 512 + kBlkBN * 4;
 constexpr int kBlkEpiWarps = 8;  // two per TMEM lane quarter, 64 columns each
+constexpr int kBlkSbRing = kBlkAhead + 1;  // per-warp ring of 1x128 B factors (64 per slice)
+constexpr int kBlkSmem = kBlkStages * kBlkStage + 1024 + 512 + kBlkEpiWarps * kBlkSbRing * 64 * 4;
 constexpr int kBlkThreads = 64 + 32 * kBlkEpiWarps;
+
+// Factor of slice kt for this thread's row (1x128 A: one per row; 128x128: one
+// per 128-row block) and the two 1x128 B factors of its lane (columns
+// 2 lane, 2 lane + 1 of the warp's 64); zeros past the matrix.
+__device__ __forceinline__ float blk_a_factor(const BlockArgs& g, int64_t KB, int64_t row, int mt, int kt) {
+  if (kt >= g.num_k) return 0.f;
+  if (g.a_rows == 1) return row < g.M ? g.sa[(int64_t)kt * g.M + row] : 0.f;
+  return g.sa[(int64_t)mt * KB + kt];
+}
+__device__ __forceinline__ float2 blk_b_factors(const BlockArgs& g, int64_t KB, int64_t ncol, int nt, int kt) {
+  if (kt >= g.num_k) return make_float2(0.f, 0.f);
+  if (g.b_rows == 1) {
+    const float* p = g.sb + (int64_t)kt * g.N;
+    return make_float2(ncol < g.N ? p[ncol] : 0.f, ncol + 1 < g.N ? p[ncol + 1] : 0.f);
+  }
+  const float f = g.sb[(int64_t)(nt * kBlkBN / 128) * KB + kt];
+  return make_float2(f, f);
+}
 
 __global__ void __launch_bounds__(kBlkThreads, 1)
     block_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                       const BlockArgs g) {
-  constexpr int S = kBlkStages, BN = kBlkBN, HALF = BN / 2;
+  constexpr int S = kBlkStages, BN = kBlkBN, HALF = BN / 2, NB = kBlkBufs;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
   uint8_t* sB = sA + S * kBM * kKBytes;
-  float* s_sb = reinterpret_cast<float*>(sB + S * BN * kKBytes);  // per-slice B factors (1x128 B)
-  uint64_t* full = reinterpret_cast<uint64_t*>(s_sb + BN);
+  float* s_sb = reinterpret_cast<float*>(sB + S * BN * kKBytes);  // [warp][ring][64] 1x128 B factors
+  uint64_t* full = reinterpret_cast<uint64_t*>(s_sb + kBlkEpiWarps * kBlkSbRing * 64);
   uint64_t* empty = full + S;
-  uint64_t* acc_full = empty + S;   // [2]
-  uint64_t* acc_empty = acc_full + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
+  uint64_t* acc_full = empty + S;   // [NB]
+  uint64_t* acc_empty = acc_full + NB;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + NB);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -980,7 +1001,7 @@ __global__ void __launch_bounds__(kBlkThreads, 1)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    for (int a = 0; a < 2; ++a) {
+    for (int a = 0; a < NB; ++a) {
       mbar_init(&acc_full[a], 1);
       mbar_init(&acc_empty[a], kBlkEpiWarps);
     }
@@ -989,7 +1010,7 @@ __global__ void __launch_bounds__(kBlkThreads, 1)
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
   }
-  if (warp == 1) tmem_alloc(tmem_slot, 256);
+  if (warp == 1) tmem_alloc(tmem_slot, NB * BN);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -1011,6 +1032,8 @@ __global__ void __launch_bounds__(kBlkThreads, 1)
           tma_load_2d(sB + s * BN * kKBytes, &tmB, kt * kKBytes, nt * BN, &full[s]);
         }
       }
+      // After an abort, let the loads still in flight land before the CTA exits.
+      if (!ok) drain_stages(full, S, it > (uint32_t)S ? it - S : 0u, it);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -1021,7 +1044,7 @@ __global__ void __launch_bounds__(kBlkThreads, 1)
       bool ok = true;
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
         for (int kt = 0; kt < g.num_k; ++kt, ++slice) {
-          const uint32_t a = slice & 1u, aph = (slice >> 1) & 1u;
+          const uint32_t a = slice % NB, aph = (slice / NB) & 1u;
           if (!(ok = mbar_wait_bounded(&acc_empty[a], aph ^ 1u, abort_flag, &g_device_error))) break;
           if (!(ok = mbar_wait_bounded(&full[s], ph, abort_flag, &g_device_error))) break;
           tc_fence_after();
@@ -1037,10 +1060,14 @@ __global__ void __launch_bounds__(kBlkThreads, 1)
       }
     }
   } else {
+    // Epilogue: per 128-deep slice, acc += partial * fa[row] * fb[col] in FP32
+    // registers.  The factors of slice kt + kBlkAhead are loaded while slice kt
+    // is processed; the warp's 64 B factors of a slice go through a ring in the
+    // warp's own shared memory (written by its lanes, read by all of them).
     const int ew = warp - 2;          // 0..7
     const int q = warp & 3;           // TMEM lane quarter
     const int half = ew >> 2;         // column half of the tile
-    const int et = threadIdx.x - 64;  // 0..255
+    float* my_sb = s_sb + ew * kBlkSbRing * 64;
     const bool vec_ok = g.c_fp32 ? (g.N % 4 == 0) : (g.N % 8 == 0);
     uint32_t slice = 0;
     bool ok = true;
@@ -1049,24 +1076,34 @@ __global__ void __launch_bounds__(kBlkThreads, 1)
       tile_coords(t, g.tiles_m, g.tiles_n, mt, nt);
       const int64_t row = (int64_t)mt * kBM + q * 32 + lane;
       const int64_t n0 = (int64_t)nt * BN;
+      const int64_t ncol = n0 + half * HALF + 2 * lane;  // this lane's two B-factor columns
       float acc[HALF];
 #pragma unroll
       for (int i = 0; i < HALF; ++i) acc[i] = 0.f;
+      // factors of the first kBlkAhead slices
+      float fa_ring[kBlkAhead];
+      float2 fb_ring[kBlkAhead];
+#pragma unroll
+      for (int d = 0; d < kBlkAhead; ++d) {
+        fa_ring[d] = blk_a_factor(g, KB, row, mt, d);
+        fb_ring[d] = blk_b_factors(g, KB, ncol, nt, d);
+      }
       for (int kt = 0; kt < g.num_k; ++kt, ++slice) {
-        const uint32_t a = slice & 1u, aph = (slice >> 1) & 1u;
-        // this slice's factors: A per row (or per 128-row block), B per column (or block)
-        float fa;
-        if (g.a_rows == 1) fa = row < g.M ? g.sa[(int64_t)kt * g.M + row] : 0.f;
-        else fa = g.sa[(int64_t)mt * KB + kt];
-        if (g.b_rows == 1) {
-          asm volatile("bar.sync 1, %0;" ::"n"(32 * kBlkEpiWarps) : "memory");
-          if (et < BN) {
-            const int64_t n = n0 + et;
-            s_sb[et] = n < g.N ? g.sb[(int64_t)kt * g.N + n] : 0.f;
-          }
-          asm volatile("bar.sync 1, %0;" ::"n"(32 * kBlkEpiWarps) : "memory");
+        const uint32_t a = slice % NB, aph = (slice / NB) & 1u;
+        const float fa = fa_ring[0];
+        const float2 fbv = fb_ring[0];
+#pragma unroll
+        for (int d = 0; d + 1 < kBlkAhead; ++d) {
+          fa_ring[d] = fa_ring[d + 1];
+          fb_ring[d] = fb_ring[d + 1];
         }
-        const float fb_blk = g.b_rows == 1 ? 0.f : g.sb[(n0 / 128) * KB + kt];
+        fa_ring[kBlkAhead - 1] = blk_a_factor(g, KB, row, mt, kt + kBlkAhead);
+        fb_ring[kBlkAhead - 1] = blk_b_factors(g, KB, ncol, nt, kt + kBlkAhead);
+        float* sbs = my_sb + (kt % kBlkSbRing) * 64;
+        if (g.b_rows == 1) {
+          *reinterpret_cast<float2*>(sbs + 2 * lane) = fbv;
+          __syncwarp();
+        }
         if (!(ok = mbar_wait_bounded(&acc_full[a], aph, abort_flag, &g_device_error))) break;
         __syncwarp();
         tc_fence_after();
@@ -1082,10 +1119,17 @@ __global__ void __launch_bounds__(kBlkThreads, 1)
           }
           if (g.b_rows == 1) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
-              acc[32 * cc + i] = fmaf(__uint_as_float(v[i]), fa * s_sb[half * HALF + 32 * cc + i], acc[32 * cc + i]);
+            for (int i4 = 0; i4 < 8; ++i4) {
+              const float4 f4 = *reinterpret_cast<const float4*>(sbs + 32 * cc + 4 * i4);  // broadcast
+              const float f[4] = {f4.x, f4.y, f4.z, f4.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int i = 4 * i4 + e;
+                acc[32 * cc + i] = fmaf(__uint_as_float(v[i]), fa * f[e], acc[32 * cc + i]);
+              }
+            }
           } else {
-            const float f = fa * fb_blk;
+            const float f = fa * fbv.x;
 #pragma unroll
             for (int i = 0; i < 32; ++i) acc[32 * cc + i] = fmaf(__uint_as_float(v[i]), f, acc[32 * cc + i]);
           }
@@ -1131,7 +1175,7 @@ __global__ void __launch_bounds__(kBlkThreads, 1)
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, 256);
+    tmem_dealloc(tmem_base, NB * BN);
   }
 }
 
