@@ -631,7 +631,7 @@ def run_lpq(args, rank, world, local):
         wall = time.perf_counter() - t0
         cpu = {"value": layer.flops / sec / 1e12, "unit": "TFLOP/s", "cores": o.num_threads(), "kind": "oracle",
                "sample": "per GEMM 32x256 outputs of the FP64 oracle GEMM on NVFP4 operands plus the NVFP4 "
-                         "quantization of those operand rows, projected to the full layer (quantize share %.0f%%)"
+                         "quantization of those operand rows, projected to the full layer (quantize share %.2f%%)"
                          % (100 * info["quant_s"] / sec),
                "wall_s": wall}
 

@@ -230,6 +230,26 @@ __device__ __forceinline__ float sr_e2m1_value(float y, uint32_t r) {
   return __uint_as_float(__float_as_uint(v) | (__float_as_uint(c) & 0x80000000u));
 }
 
+// The same rounding for two values at once, its six floating-point steps as
+// packed two-wide operations (each half rounded exactly like the scalar step).
+__device__ __forceinline__ float2 sr_e2m1_value2(float2 y, uint32_t r0, uint32_t r1) {
+  const float c0 = fmaxf(fminf(y.x, 6.0f), -6.0f), c1 = fmaxf(fminf(y.y, 6.0f), -6.0f);
+  const uint32_t e0 = __float_as_uint(fmaxf(fabsf(c0), 1.0f)) & 0x7F800000u;
+  const uint32_t e1 = __float_as_uint(fmaxf(fabsf(c1), 1.0f)) & 0x7F800000u;
+  const float2 d = __fmul2_rn(make_float2(__uint_as_float(e0), __uint_as_float(e1)), make_float2(0.5f, 0.5f));
+  const float2 q = __fmul2_rn(make_float2(fabsf(c0), fabsf(c1)),
+                              make_float2(__uint_as_float(0x7F800000u - e0), __uint_as_float(0x7F800000u - e1)));
+  const float2 fl = make_float2(floorf(q.x), floorf(q.y));
+  const float2 fr = __fadd2_rn(q, make_float2(-fl.x, -fl.y));  // q - fl, exact
+  const float2 diff = __ffma2_rn(fr, make_float2(16777216.0f, 16777216.0f),
+                                 make_float2(-(float)(r0 >> 8), -(float)(r1 >> 8)));
+  const float2 up = make_float2(__saturatef(__fmul_rn(diff.x, 1.70141183e38f)),
+                                __saturatef(__fmul_rn(diff.y, 1.70141183e38f)));
+  const float2 v = __fmul2_rn(__fadd2_rn(fl, up), d);
+  return make_float2(__uint_as_float(__float_as_uint(v.x) | (__float_as_uint(c0) & 0x80000000u)),
+                     __uint_as_float(__float_as_uint(v.y) | (__float_as_uint(c1) & 0x80000000u)));
+}
+
 // ------------------------------------------------------------------ warp helpers
 __device__ __forceinline__ float warp_max_xor(float v, int width_lanes) {
   for (int o = 1; o < width_lanes; o <<= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));

@@ -111,19 +111,22 @@ __device__ __forceinline__ void nv_factor_table(float* tab, float s_enc, int t) 
 // i).  f == 0 marks a block whose scale decoded to 0: all codes +0.
 __device__ __forceinline__ uint32_t nv_codes8(const float v[8], float f, bool sr, uint4 w0, uint4 w1) {
   if (f == 0.f) return 0u;
+  uint32_t out = 0;
+  if (sr) {  // y = v * f and the rounding two values at a time (packed two-wide operations)
+    const uint32_t w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 yy = __fmul2_rn(make_float2(v[2 * i], v[2 * i + 1]), make_float2(f, f));
+      const float2 r = sr_e2m1_value2(yy, w[2 * i], w[2 * i + 1]);
+      out |= cvt_e2m1x2(r.x, r.y) << (8 * i);
+    }
+    return out;
+  }
   float y[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) y[i] = __fmul_rn(v[i], f);
-  uint32_t out = 0;
-  if (sr) {
-    const uint32_t w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
-      out |= cvt_e2m1x2(sr_e2m1_value(y[2 * i], w[2 * i]), sr_e2m1_value(y[2 * i + 1], w[2 * i + 1])) << (8 * i);
-  } else {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) out |= cvt_e2m1x2(y[2 * i], y[2 * i + 1]) << (8 * i);
-  }
+  for (int i = 0; i < 4; ++i) out |= cvt_e2m1x2(y[2 * i], y[2 * i + 1]) << (8 * i);
   return out;
 }
 
