@@ -186,22 +186,36 @@ __device__ __forceinline__ void rht16(float t[16], const float sgn[16]) {
 }
 
 // The same transform with the signs taken from a 16-bit mask (bit j set: -1)
-// by flipping sign bits: exact like the multiply, and without the 16
-// registers of the factors (for kernels limited by occupancy, not issue).
+// by flipping sign bits (exact like the multiply, without the 16 registers of
+// the factors), the butterflies and the final scaling as packed two-wide
+// operations: the quantizers' column-wise RHT.
 __device__ __forceinline__ void rht16(float t[16], uint32_t signs) {
 #pragma unroll
   for (int j = 0; j < 16; ++j) t[j] = __uint_as_float(__float_as_uint(t[j]) ^ ((signs << (31 - j)) & 0x80000000u));
+  // Butterflies two at a time with packed two-wide operations, each half
+  // rounded like the scalar step: (a, b) -> (a + b, a - b), the difference as
+  // fma(b, -1, a) (the product is exact).
 #pragma unroll
-  for (int h = 1; h < 16; h <<= 1)
+  for (int h = 1; h < 16; h <<= 1) {
+    int idx[8], n = 0;
 #pragma unroll
     for (int i = 0; i < 16; ++i)
-      if ((i & h) == 0) {
-        float a = t[i], b = t[i + h];
-        t[i] = __fadd_rn(a, b);
-        t[i + h] = __fsub_rn(a, b);
-      }
+      if ((i & h) == 0) idx[n++] = i;
 #pragma unroll
-  for (int j = 0; j < 16; ++j) t[j] = __fmul_rn(0.25f, t[j]);
+    for (int p = 0; p < 8; p += 2) {
+      const int i0 = idx[p], i1 = idx[p + 1];
+      const float2 a = make_float2(t[i0], t[i1]), b = make_float2(t[i0 + h], t[i1 + h]);
+      const float2 sum = __fadd2_rn(a, b);
+      const float2 dif = __ffma2_rn(b, make_float2(-1.0f, -1.0f), a);
+      t[i0] = sum.x; t[i1] = sum.y;
+      t[i0 + h] = dif.x; t[i1 + h] = dif.y;
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < 16; j += 2) {
+    const float2 r = __fmul2_rn(make_float2(t[j], t[j + 1]), make_float2(0.25f, 0.25f));
+    t[j] = r.x; t[j + 1] = r.y;
+  }
 }
 
 // Stochastic E2M1 rounding of y with random word r: between adjacent
