@@ -604,7 +604,10 @@ def run_lpq(args, rank, world, local):
                     ev.record(st)
                     ev_out[k].append(ev)
 
-        for w in range(2):
+        # warm-up: every buffer of both sets touched, and the host link past its slow first
+        # copies of a fresh process (LPQ_E2E_WARMUP overrides the count)
+        e2e_warm = int(os.environ.get("LPQ_E2E_WARMUP", str(max(3, args.warmup))))
+        for w in range(e2e_warm):
             e2e_step(w)
         torch.cuda.synchronize()
         barrier(world)
