@@ -605,10 +605,16 @@ def run_lpq(args, rank, world, local):
                     ev_out[k].append(ev)
 
         # warm-up: every buffer of both sets touched, and the host link past its slow first
-        # copies of a fresh process (LPQ_E2E_WARMUP overrides the count)
+        # copies on a fresh box: at least max(3, W) steps and at least one second of steps
+        # (LPQ_E2E_WARMUP overrides the step count)
         e2e_warm = int(os.environ.get("LPQ_E2E_WARMUP", str(max(3, args.warmup))))
-        for w in range(e2e_warm):
+        t_w = time.perf_counter()
+        w = 0
+        while w < e2e_warm or (time.perf_counter() - t_w < 1.0 and w < 200):
             e2e_step(w)
+            w += 1
+            if w >= e2e_warm:
+                torch.cuda.synchronize()
         torch.cuda.synchronize()
         barrier(world)
         t0 = time.perf_counter()
