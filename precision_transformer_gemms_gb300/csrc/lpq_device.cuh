@@ -150,12 +150,6 @@ struct PhiloxKeys {
   }
 };
 
-// 4 random words for elements j = 4g .. 4g+3 of copy `copy_id`.
-__device__ __forceinline__ uint4 sr_words(uint64_t seed, uint64_t g, uint32_t copy_id) {
-  return philox4x32_10(make_uint4((uint32_t)g, (uint32_t)(g >> 32), copy_id, 0u), (uint32_t)seed,
-                       (uint32_t)(seed >> 32));
-}
-
 __device__ __forceinline__ uint32_t rht_signs(uint32_t rht_seed) {
   return philox4x32_10(make_uint4(0u, 0u, 2u, 0u), rht_seed, 0u).x & 0xFFFFu;
 }
@@ -229,23 +223,8 @@ __device__ __forceinline__ void rht16(float t[16], uint32_t signs) {
 // threshold of the definition, and the up/down decision is the saturated
 // product of the difference thr - float(r >> 8) (its sign exact) scaled by
 // 2^127 (1 when positive, else 0).
-__device__ __forceinline__ float sr_e2m1_value(float y, uint32_t r) {
-  const float c = fmaxf(fminf(y, 6.0f), -6.0f);
-  const uint32_t e = __float_as_uint(fmaxf(fabsf(c), 1.0f)) & 0x7F800000u;  // 2^k, k = 0, 1, 2
-  const float d = __fmul_rn(__uint_as_float(e), 0.5f);                        // spacing 2^(k-1)
-  const float q = __fmul_rn(fabsf(c), __uint_as_float(0x7F800000u - e));      // |y| / d, exact
-  const float fl = floorf(q);
-  // (q - fl) * 2^24 - float(r >> 8) in one rounding: the product is exact, so
-  // the sign is that of thr - float(r >> 8), and a positive value is at least
-  // 2^-124 (thr >= 2^-124 when r >> 8 is 0, else an ulp of thr >= 1).
-  const float diff = __fmaf_rn(__fsub_rn(q, fl), 16777216.0f, -(float)(r >> 8));
-  const float up = __saturatef(__fmul_rn(diff, 1.70141183e38f));  // * 2^127: >= 8 when positive
-  const float v = __fmul_rn(__fadd_rn(fl, up), d);
-  return __uint_as_float(__float_as_uint(v) | (__float_as_uint(c) & 0x80000000u));
-}
-
-// The same rounding for two values at once, its six floating-point steps as
-// packed two-wide operations (each half rounded exactly like the scalar step).
+// Two values at a time: the six floating-point steps run as packed two-wide
+// operations, each half rounded exactly like the scalar operation.
 __device__ __forceinline__ float2 sr_e2m1_value2(float2 y, uint32_t r0, uint32_t r1) {
   const float c0 = fmaxf(fminf(y.x, 6.0f), -6.0f), c1 = fmaxf(fminf(y.y, 6.0f), -6.0f);
   const uint32_t e0 = __float_as_uint(fmaxf(fabsf(c0), 1.0f)) & 0x7F800000u;
@@ -515,9 +494,6 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
   uint32_t r;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
   return r;
-}
-__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 // Relaxed remote arrival, for hand-overs of TMEM whose accesses by the
 // arriving side are already complete (tcgen05.wait::st / wait::ld), with no
