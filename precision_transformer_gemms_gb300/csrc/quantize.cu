@@ -122,11 +122,11 @@ __device__ __forceinline__ uint32_t nv_codes8(const float v[8], float f, bool sr
     }
     return out;
   }
-  float y[8];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) y[i] = __fmul_rn(v[i], f);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) out |= cvt_e2m1x2(y[2 * i], y[2 * i + 1]) << (8 * i);
+  for (int i = 0; i < 4; ++i) {  // y = v * f two at a time (packed), RNE encode
+    const float2 yy = __fmul2_rn(make_float2(v[2 * i], v[2 * i + 1]), make_float2(f, f));
+    out |= cvt_e2m1x2(yy.x, yy.y) << (8 * i);
+  }
   return out;
 }
 
