@@ -515,49 +515,9 @@ def run_lpq(args, rank, world, local):
             "peak_source": peak_src, "algorithmic_bytes_per_launch": algo_bytes / len(layer.shapes)}
     hbm = peaks["hbm_gbs"] if peaks else 6800.0
 
-    # recipe sweep (fewer steps each)
-    recipes = {}
-    if not args.no_sweep:
-        sweep = sweep_recipes(args)
-        k = max(3, args.steps // 4)
-        for r in sweep:
-            layer.prequantize(r)
-            res = {}
-            for mode in ("autocast", "prequant"):
-                ac = mode == "autocast" or r == "fp8_delayed"
-                if r == "bf16":
-                    ac = False
-                ms, _ = time_steps(layer, r, ac, k, 2, world)
-                res[f"{mode}_ms_per_layer"] = ms
-                res[f"{mode}_tflops"] = layer.flops / (ms * 1e-3) / 1e12
-            if r != "bf16":
-                import torch
-                for w in range(2):
-                    layer.fused_step(r, w)
-                torch.cuda.synchronize()
-                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                e0.record()
-                for s_ in range(k):
-                    layer.fused_step(r, 10 + s_)
-                e1.record()
-                torch.cuda.synchronize()
-                res["fused_ms_per_layer"] = e0.elapsed_time(e1) / k
-                res["fused_tflops"] = layer.flops / (res["fused_ms_per_layer"] * 1e-3) / 1e12
-            recipes[r] = res
-            # free this recipe's buffers before the next one
-            for key in [k_ for k_ in layer.bufs if k_[0] == r and r != recipe]:
-                del layer.bufs[key]
-            torch.cuda.empty_cache()
-        if "bf16" in recipes:
-            # BF16 does the same work in both modes: the faster run is the baseline
-            b = min(recipes["bf16"]["prequant_ms_per_layer"], recipes["bf16"]["autocast_ms_per_layer"])
-            recipes["bf16"]["baseline_ms_per_layer"] = b
-            for r, res in recipes.items():
-                for mode in ("autocast", "prequant", "fused"):
-                    if f"{mode}_ms_per_layer" in res:
-                        res[f"{mode}_speedup_vs_bf16"] = b / res[f"{mode}_ms_per_layer"]
-
-    # e2e: every step copies its bf16 inputs from pinned host memory and its
+    # e2e (right after the headline, before the recipe sweep: after the sweep's tens of
+    # seconds the host link was seen to run slower): every step copies its bf16 inputs
+    # from pinned host memory and its
     # outputs back to pinned host memory.  Copies run on their own streams,
     # double-buffered (inputs of step s+1 and outputs of step s-1 move while
     # step s computes); events order each buffer's reuse.
@@ -633,6 +593,48 @@ def run_lpq(args, rank, world, local):
                "copies": f"pinned host <-> device on {nlanes} copy streams per direction, double-buffered against "
                          "the compute stream"}
         del host_in, host_out, inp_sets, out_sets
+
+    # recipe sweep (fewer steps each)
+    recipes = {}
+    if not args.no_sweep:
+        sweep = sweep_recipes(args)
+        k = max(3, args.steps // 4)
+        for r in sweep:
+            layer.prequantize(r)
+            res = {}
+            for mode in ("autocast", "prequant"):
+                ac = mode == "autocast" or r == "fp8_delayed"
+                if r == "bf16":
+                    ac = False
+                ms, _ = time_steps(layer, r, ac, k, 2, world)
+                res[f"{mode}_ms_per_layer"] = ms
+                res[f"{mode}_tflops"] = layer.flops / (ms * 1e-3) / 1e12
+            if r != "bf16":
+                import torch
+                for w in range(2):
+                    layer.fused_step(r, w)
+                torch.cuda.synchronize()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                for s_ in range(k):
+                    layer.fused_step(r, 10 + s_)
+                e1.record()
+                torch.cuda.synchronize()
+                res["fused_ms_per_layer"] = e0.elapsed_time(e1) / k
+                res["fused_tflops"] = layer.flops / (res["fused_ms_per_layer"] * 1e-3) / 1e12
+            recipes[r] = res
+            # free this recipe's buffers before the next one
+            for key in [k_ for k_ in layer.bufs if k_[0] == r and r != recipe]:
+                del layer.bufs[key]
+            torch.cuda.empty_cache()
+        if "bf16" in recipes:
+            # BF16 does the same work in both modes: the faster run is the baseline
+            b = min(recipes["bf16"]["prequant_ms_per_layer"], recipes["bf16"]["autocast_ms_per_layer"])
+            recipes["bf16"]["baseline_ms_per_layer"] = b
+            for r, res in recipes.items():
+                for mode in ("autocast", "prequant", "fused"):
+                    if f"{mode}_ms_per_layer" in res:
+                        res[f"{mode}_speedup_vs_bf16"] = b / res[f"{mode}_ms_per_layer"]
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
