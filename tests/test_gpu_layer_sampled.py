@@ -7,7 +7,8 @@ dequantized operands, |C - C_ref| <= 1e-3 sum_k |a b| (+ half a bf16 ulp of C).
 NVFP4 follows the layer recipe: 1D 16-value blocks for X and dY, 16x16 tiles for
 W, the random Hadamard transform on the Wgrad operands (the column-wise copies
 of X and dY) and stochastic rounding of dY; MXFP8 quantizes every tensor with
-E4M3 codes and E8M0 scales per 32 values."""
+E4M3 codes and E8M0 scales per 32 values (the E5M2 variant gives dY E5M2
+codes); MXFP4 every tensor with packed E2M1 codes and E8M0 scales per 32."""
 import numpy as np
 import pytest
 import torch
@@ -37,6 +38,10 @@ def quantize_copy(t, recipe, role, colwise, seed):
     flags = lpq.COLWISE if colwise else lpq.ROWWISE
     if recipe == "mxfp8":
         q = lpq.quantize(t, lpq.MXFP8, flags)
+    elif recipe == "mxfp8_e5m2":  # E5M2 codes for the gradients, E4M3 for X and W
+        q = lpq.quantize(t, lpq.MXFP8_E5M2 if role == "dY" else lpq.MXFP8, flags)
+    elif recipe == "mxfp4":
+        q = lpq.quantize(t, lpq.MXFP4, flags)
     elif role == "W":
         q = lpq.quantize(t, lpq.NVFP4_2D, flags)
     else:
@@ -48,7 +53,7 @@ def quantize_copy(t, recipe, role, colwise, seed):
     return q.col if colwise else q.row
 
 
-@pytest.mark.parametrize("recipe", ["nvfp4", "mxfp8"])
+@pytest.mark.parametrize("recipe", ["nvfp4", "mxfp8", "mxfp8_e5m2", "mxfp4"])
 @pytest.mark.parametrize("index", range(12))
 def test_layer_gemm_sampled(recipe, index):
     name, layout, M, K, N = layer_shapes()[index]
