@@ -247,6 +247,38 @@ def test_nonfinite_inputs_follow_the_oracle():
     eq(codes(q.row), ref["row"])
 
 
+def test_nvfp4_nonfinite_inputs_follow_the_oracle():
+    """NaN and infinities in an NVFP4 input: the amax skips NaN, an infinite
+    amax gives tensor scale 1, NaN values encode as +6 and infinities
+    saturate; the RHT spreads a NaN over its 16-value run.  Row-wise with
+    stochastic rounding, column-wise with RHT (+ SR), and the 2D copies."""
+    x, _ = bf16_input((64, 128), seed=19)
+    x[1, 2] = float("nan")
+    x[4, 6] = float("inf")
+    x[40, 70] = float("-inf")
+    bits = synth.host_bits(x)
+    for flags, ref_flags in [(BOTH, o.NV_ROW | o.NV_COL),
+                             (BOTH | lpq.STOCHASTIC, o.NV_ROW | o.NV_COL | o.NV_SR),
+                             (BOTH | lpq.RHT_COLWISE, o.NV_ROW | o.NV_COL | o.NV_RHT),
+                             (BOTH | lpq.RHT_COLWISE | lpq.STOCHASTIC, o.NV_ROW | o.NV_COL | o.NV_RHT | o.NV_SR)]:
+        q = lpq.quantize(x, lpq.NVFP4, flags, seed=3, rht_seed=7)
+        ref = o.nvfp4(bits, ref_flags, seed=3, rht_seed=7)
+        for name in ("row", "col"):
+            eq(codes(getattr(q, name)), ref[name])
+            eq(plain_scales(getattr(q, name)), ref[name + "_sf"])
+    x2 = x.clone()
+    x2[4, 6] = 1.0
+    x2[40, 70] = -2.0  # only the NaN: a finite amax
+    bits2 = synth.host_bits(x2)
+    for t, b in ((x, bits), (x2, bits2)):
+        q = lpq.quantize(t, lpq.NVFP4_2D, BOTH)
+        ref = o.nvfp4(b, o.NV_ROW | o.NV_COL | o.NV_2D)
+        for name in ("row", "col"):
+            eq(codes(getattr(q, name)), ref[name])
+            eq(plain_scales(getattr(q, name)), ref[name + "_sf"])
+        assert scalar(q.row.tensor_scale) == np.float32(ref["row_ts"])
+
+
 def test_empty_input():
     x = torch.empty((0, 128), dtype=torch.bfloat16, device="cuda")
     q = lpq.quantize(x, lpq.NVFP4, lpq.ROWWISE)
