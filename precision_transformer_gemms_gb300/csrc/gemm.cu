@@ -490,13 +490,15 @@ lpq_status run(const CUtensorMap& ta, const CUtensorMap& tb, GemmArgs g, cudaStr
 // 256 x 256 output tile: each CTA loads its own 128 rows of A and its own 128
 // rows of B (each SM streams half the B bytes of the single-CTA kernel), the
 // even CTA issues the pair MMAs, and each CTA's TMEM holds the accumulator
-// rows of its half.  Every load is a TMA tile load that signals the even
+// rows of its half.  Every A/B load is a TMA tile load that signals the even
 // CTA's full barrier; MMA completion is multicast to both CTAs.  For the
 // block-scaled kinds each CTA also loads the scale atoms of its A rows and of
 // all 256 B rows of the tile (each CTA's accumulator spans every column, so
 // each TMEM needs every column's scales; kSfbFull = false, each CTA holding
-// only its own 128 B rows, does not match the pair MMA), which the pair
-// copies (tcgen05.cp.cta_group::2) move into each CTA's TMEM.
+// only its own 128 B rows, does not match the pair MMA).  With scale warps
+// (SFST, the default) each CTA's four scale warps write them into the
+// stage's TMEM slot with tcgen05.st and report to the even CTA's full
+// barrier; otherwise the pair copies (tcgen05.cp.cta_group::2) move them.
 constexpr int kPairBN = 256;
 
 template <int KIND, bool kSfbFull, bool SFST = false>
