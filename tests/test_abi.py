@@ -149,3 +149,20 @@ def test_given_amax_validation():
     assert _quantize_raw(None, 4, 128, lpq.FP8_BLOCK_1x128, lpq.ROWWISE | lpq.GIVEN_AMAX) == lpq.ERR_UNSUPPORTED
     assert _quantize_raw(None, 4, 32, lpq.FP8_E4M3, lpq.ROWWISE | lpq.GIVEN_AMAX, scaling=1) == lpq.ERR_UNSUPPORTED
     assert _quantize_raw(None, 4, 32, lpq.NVFP4, lpq.ROWWISE | 32) == lpq.ERR_INVALID_ARG  # unknown bit
+
+
+def test_binding_constants_match_the_header():
+    """Every LPQ_* enum value the header declares has the same value in the
+    Python binding (LPQ_X <-> lpq.X), and the binding's format names cover
+    every format."""
+    text = open(os.path.join(ROOT, "include", "lpq.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    values = {name: int(v) for name, v in re.findall(r"\bLPQ_([A-Z0-9_a-z]+)\s*=\s*(\d+)", text)}
+    assert len(values) >= 30
+    for name, v in values.items():
+        assert hasattr(lpq, name), name
+        assert getattr(lpq, name) == v, (name, getattr(lpq, name), v)
+    formats = [n for n in ("BF16", "FP8_E4M3", "FP8_E5M2", "MXFP8", "NVFP4", "NVFP4_2D", "FP8_BLOCK_1x128",
+                           "FP8_BLOCK_128x128", "MXFP8_E5M2", "MXFP4")]
+    assert sorted(getattr(lpq, n) for n in formats) == list(range(len(formats)))
+    assert set(lpq.FORMAT_NAMES) == set(range(len(formats)))
