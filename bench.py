@@ -70,7 +70,6 @@ def parse():
     p.add_argument("-o", "--output", default=None, help="write the per-GEMM table as JSON here")
     p.add_argument("--workload", choices=["layer", "ksweep", "drift", "report"], default="layer",
                    help="layer: the contract line; ksweep / drift: the K-sweep and the FP8 drift runs")
-    p.add_argument("--verify", action="store_true", help="drift: compare every step with the oracle")
     p.add_argument("--mma-peaks", action="store_true",
                    help="only measure the dense tcgen05 rates (shared-memory-resident operands) and exit")
     return p.parse_args()
@@ -759,9 +758,9 @@ def run_drift(args):
     """Per-tensor FP8 current vs delayed scaling on the attention-output GEMMs
     (M = 15872, 4096 x 4096 weight) over 20 steps whose activation std drifts
     1 -> 4 (gradients std 1e-3); Fprop + Dgrad + Wgrad each step, autocast.
-    Reports per step the ms, the amax and the scale in use; with --verify
-    every step's codes are compared with the oracle."""
-    import numpy as np
+    Reports per step the ms, the amax, the scale in use and how many
+    activations exceed the E4M3 range at that scale (a device-side count).
+    Every step's codes are compared with the oracle in the GPU tests."""
     import torch
     from precision_transformer_gemms_gb300 import lpq, synth
     torch.cuda.set_device(0)
@@ -777,13 +776,11 @@ def run_drift(args):
         outs = [torch.empty((M, N), dtype=torch.bfloat16, device="cuda"),
                 torch.empty((M, K), dtype=torch.bfloat16, device="cuda"),
                 torch.empty((N, K), dtype=torch.bfloat16, device="cuda")]
-        steps, ref_state = [], None
-        if args.verify:
-            import oracle as o
-            ref_state = o.DelayedState(16)
+        steps = []
         for t in range(20):
             X = synth.bf16_normal((M, K), synth.drift_std(t), 10 * t, "cuda")
             dY = synth.bf16_normal((M, N), synth.GRAD_STD, 10 * t + 2, "cuda")
+            x_scale = st["X"].scale.clone() if sc else None  # the scale this step's X is quantized with
             torch.cuda.synchronize()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record()
@@ -798,16 +795,10 @@ def run_drift(args):
             torch.cuda.synchronize()
             rec = {"ms": e0.elapsed_time(e1), "x_amax": float(bufs["X"].row.amax.item()),
                    "x_scale_inv": float(bufs["X"].row.tensor_scale.item())}
-            if args.verify:
-                import oracle as o
-                bits = synth.host_bits(X)
-                scale = None if sc == lpq.SCALING_CURRENT else float(ref_state.scale[0])
-                ref = o.fp8_pertensor(bits, o.E4M3, scale=scale)
-                rec["bit_exact"] = bool(np.array_equal(bufs["X"].row.codes_matrix().cpu().numpy(), ref["row"]) and
-                                        np.array_equal(bufs["X"].col.codes_matrix().cpu().numpy(), ref["col"]))
-                rec["saturated"] = ref["saturated"]
-                if scale is not None:
-                    ref_state.update(ref["amax"], 448.0)
+            # diagnostic (outside the timed region): |X * scale| > 448 in fp32, the scale being
+            # 448 / amax (current) or the delayed state's scale before this step's update
+            scale = x_scale if sc else 448.0 / bufs["X"].row.amax
+            rec["saturated"] = int(((X.float() * scale).abs() > 448.0).sum().item())
             steps.append(rec)
         res[scaling] = {"steps": steps, "mean_ms": statistics.mean(s["ms"] for s in steps[2:])}
         del bufs, outs
