@@ -436,7 +436,9 @@ void orc_mxfp8(const uint16_t* x, int64_t R, int64_t C, uint8_t* row_codes, uint
 
 // MX quantization of any element format (E4M3 and E5M2: 1 byte per code, E2M1:
 // packed): row-wise codes [R, C (/2)] + E8M0 [R, C/32]; column-wise copy the
-// transpose re-blocked along R.  fmt = E4M3 is orc_mxfp8.
+// transpose re-blocked along R.  fmt = E4M3 is orc_mxfp8 ([NeMo] MXFP8); E5M2
+// is the gradient variant ([FP8]: E5M2 for backward gradients); E2M1 is MXFP4
+// ([NVFP4] technical deep dive: the 32-value blocks NVFP4 narrows to 16).
 void orc_mx(const uint16_t* x, int64_t R, int64_t C, int fmt, uint8_t* row_codes, uint8_t* row_sf,
             uint8_t* col_codes, uint8_t* col_sf) {
   if (row_codes)
