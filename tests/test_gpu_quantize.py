@@ -319,3 +319,34 @@ def test_full_size_whole_tensor(fmt, shape):
         eq(codes(copy), ref[cname])
         if sname:
             eq(plain_scales(copy), ref[sname])
+
+
+def test_delayed_state_checkpoint_resume():
+    """The delayed-scaling state is raw arrays (history, position, scale,
+    1/scale): 10 steps, a save to host memory, a restore into a fresh state
+    and 10 more steps give the same codes, amaxes and state, bit for bit, as
+    20 uninterrupted steps."""
+    def run(state, t0, t1):
+        out = []
+        for t in range(t0, t1):
+            x, _ = bf16_input((128, 256), std=synth.drift_std(t), seed=10 * t)
+            q = lpq.quantize(x, lpq.FP8_E4M3, BOTH, scaling=lpq.SCALING_DELAYED, state=state)
+            lpq.scale_update(state, q.row.amax, 448.0)
+            out.append((codes(q.row), codes(q.col), scalar(q.row.amax), scalar(q.row.tensor_scale)))
+        return out
+
+    whole = lpq.DelayedState(16)
+    ref = run(whole, 0, 20)
+    first = lpq.DelayedState(16)
+    part = run(first, 0, 10)
+    saved = {k: getattr(first, k).cpu().numpy().copy() for k in ("hist", "pos", "scale", "scale_inv")}
+    resumed = lpq.DelayedState(16)
+    for k, v in saved.items():
+        getattr(resumed, k).copy_(torch.from_numpy(v))
+    part += run(resumed, 10, 20)
+    for t, (a, b) in enumerate(zip(ref, part)):
+        eq(a[0], b[0])
+        eq(a[1], b[1])
+        assert a[2:] == b[2:], t
+    for k in ("hist", "pos", "scale", "scale_inv"):
+        eq(getattr(whole, k).cpu().numpy(), getattr(resumed, k).cpu().numpy())
