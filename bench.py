@@ -568,12 +568,12 @@ def run_lpq(args, rank, world, local):
                     ev_out[k].append(ev)
 
         # warm-up: every buffer of both sets touched, and the host link past its slow first
-        # copies on a fresh box: at least max(3, W) steps and at least one second of steps
-        # (LPQ_E2E_WARMUP overrides the step count)
+        # copies on a fresh box (seen to last more than half a second): at least max(3, W)
+        # steps and at least three seconds of steps (LPQ_E2E_WARMUP overrides the count)
         e2e_warm = int(os.environ.get("LPQ_E2E_WARMUP", str(max(3, args.warmup))))
         t_w = time.perf_counter()
         w = 0
-        while w < e2e_warm or (time.perf_counter() - t_w < 1.0 and w < 200):
+        while w < e2e_warm or (time.perf_counter() - t_w < 3.0 and w < 200):
             e2e_step(w)
             w += 1
             if w >= e2e_warm:
