@@ -509,8 +509,7 @@ def run_lpq(args, rank, world, local):
                if default_layer and autocast else None)
     roof = {"bound": "tensor", "achieved": gemm_achieved, "peak": peak, "unit": "TFLOP/s",
             "frac": gemm_achieved / peak, "traffic": traffic,
-            "kernel": ("gemm_kernel" if os.environ.get("LPQ_GEMM_PAIR", "1")[:1] == "0" else "gemm_pair_kernel")
-            + f" ({recipe})",
+            "kernel": f"gemm_pair_kernel ({recipe})",
             "peak_source": peak_src, "algorithmic_bytes_per_launch": algo_bytes / len(layer.shapes)}
     hbm = peaks["hbm_gbs"] if peaks else 6800.0
 
@@ -695,6 +694,10 @@ def run_mma_peaks(args):
             out[kind + "_scale_copies_interleaved"] = lpq.mma_peak(kind, iters=iters, with_scale_copies=3)
             out[kind + "_scales_stored_by_warps"] = lpq.mma_peak(kind, iters=iters, with_scale_copies=4)
             out[kind + "_scale_copies_by_other_warp"] = lpq.mma_peak(kind, iters=iters, with_scale_copies=5)
+        # CTA pairs (cta_group::2, 256 x 256 MMAs): the shape the product GEMM issues
+        out[kind + "_pair"] = lpq.mma_peak(kind, iters=iters, with_scale_copies=6)
+        if kind in ("mxfp8", "nvfp4"):
+            out[kind + "_pair_scales_stored_by_warps"] = lpq.mma_peak(kind, iters=iters, with_scale_copies=7)
     out["clocks"] = clocks.stop()
     out["unit"] = "TFLOP/s"
     print(json.dumps(out), flush=True)

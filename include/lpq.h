@@ -217,6 +217,36 @@ typedef enum { LPQ_FPROP = 0, LPQ_DGRAD = 1, LPQ_WGRAD = 2 } lpq_layout;
 lpq_status lpq_gemm(int32_t layout, const lpq_qview *a, const lpq_qview *b, void *c, int32_t c_is_fp32,
                     int64_t m, int64_t n, int64_t k, lpq_stream_t stream);
 
+/* Kernel-path options of lpq_gemm_ex.  They choose between kernels that
+ * compute the same result (every path passes the same parity tests); they
+ * never change the format, the precision or the arithmetic, and nothing else
+ * (no environment variable, no global setting) selects a path.  All-zero is
+ * the default path that lpq_gemm takes.
+ *   single_cta    0: CTA pairs (cta_group::2, 256 x 256 output tiles) when
+ *                 m >= 256, one CTA per 128 x 256 tile otherwise; 1: always
+ *                 one CTA per tile.
+ *   tile_n        single-CTA block-scaled kinds: 0 or 256 (128 x 256 tiles,
+ *                 one TMEM accumulator) or 128 (128 x 128 tiles, two
+ *                 accumulators).  Ignored elsewhere.
+ *   scale_copies  block-scaled kinds: 0 = the scale factors are written into
+ *                 TMEM by four scale warps (tcgen05.st); 1 = copied by the
+ *                 MMA-issuing thread (tcgen05.cp).
+ *   direct_store  CTA-pair kernel, bf16 output: 0 = TMA tile stores through
+ *                 shared memory (when n % 8 == 0); 1 = stores from registers.
+ *   reserved      must be 0.
+ * Values outside these sets give LPQ_ERR_INVALID_ARG. */
+typedef struct {
+  int32_t single_cta;
+  int32_t tile_n;
+  int32_t scale_copies;
+  int32_t direct_store;
+  int32_t reserved[4];
+} lpq_gemm_opts;
+
+/* lpq_gemm with explicit kernel-path options (NULL = all defaults). */
+lpq_status lpq_gemm_ex(int32_t layout, const lpq_qview *a, const lpq_qview *b, void *c, int32_t c_is_fp32,
+                       int64_t m, int64_t n, int64_t k, const lpq_gemm_opts *opts, lpq_stream_t stream);
+
 /* Transformer configuration ([TE] "model configuration and training input"). */
 typedef struct {
   int64_t hidden, intermediate, heads, layers, micro_batch, seq;
@@ -259,8 +289,13 @@ lpq_status lpq_selftest_wait(uint64_t limit_ns, lpq_stream_t stream);
  * right before it, 4 = the scale columns rewritten by four other warps with
  * tcgen05.st while the MMAs run, 5 = the step's copies issued by a thread of
  * another warp while the MMAs run (4 and 5: NVFP4 only, unsynchronised with
- * the MMAs, throughput only).  Other values give LPQ_ERR_INVALID_ARG.
- * FLOPs = SMs * iters * 4 * 2 * 128 * 256 * K;
+ * the MMAs, throughput only), 6 = CTA pairs (cta_group::2: clusters of two
+ * CTAs, each pair issuing four 256 x 256 MMAs per k-step, each SM holding
+ * 128 rows of A and of B, the shape of the product GEMM; any kind), 7 = CTA
+ * pairs with the scale columns rewritten by four warps per CTA with
+ * tcgen05.st while the MMAs run (kinds 2, 3).  Other values give
+ * LPQ_ERR_INVALID_ARG.  Modes 6 and 7 launch SMs rounded down to even CTAs.
+ * FLOPs = CTAs * iters * 4 * 2 * 128 * 256 * K;
  * the caller times the launch with events on `stream`. */
 lpq_status lpq_mma_peak(int32_t kind, int32_t iters, int32_t with_scale_copies, lpq_stream_t stream);
 

@@ -8,6 +8,8 @@
 #include <string.h>
 
 #include <mutex>
+#include <set>
+#include <utility>
 
 #include "lpq_internal.h"
 
@@ -98,6 +100,42 @@ lpq_status set_error(lpq_status st, const char* fmt, ...) {
 lpq_status cuda_check(cudaError_t e, const char* what) {
   if (e == cudaSuccess) return LPQ_OK;
   return set_error(LPQ_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+namespace {
+std::mutex g_dev_mu;
+std::set<int>* g_sms_known = nullptr;  // devices whose SM count is cached
+int g_sms_of[256];
+std::set<std::pair<int, const void*>>* g_smem_set = nullptr;  // (device, kernel) pairs already raised
+}  // namespace
+
+int device_sms() {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  std::lock_guard<std::mutex> lock(g_dev_mu);
+  if (!g_sms_known) g_sms_known = new std::set<int>();
+  if (dev >= 0 && dev < 256 && g_sms_known->count(dev)) return g_sms_of[dev];
+  int n = 0;
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  if (n <= 0) n = 148;
+  if (dev >= 0 && dev < 256) {
+    g_sms_of[dev] = n;
+    g_sms_known->insert(dev);
+  }
+  return n;
+}
+
+lpq_status set_smem_attr(const void* kernel, int bytes) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_check(e, "cudaGetDevice");
+  std::lock_guard<std::mutex> lock(g_dev_mu);
+  if (!g_smem_set) g_smem_set = new std::set<std::pair<int, const void*>>();
+  if (g_smem_set->count({dev, kernel})) return LPQ_OK;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess) return cuda_check(e, "cudaFuncSetAttribute(max dynamic shared memory)");
+  g_smem_set->insert({dev, kernel});
+  return LPQ_OK;
 }
 
 }  // namespace lpq
@@ -195,7 +233,19 @@ lpq_status lpq_scale_update(const lpq_delayed_state* state, const float* amax, f
 
 lpq_status lpq_gemm(int32_t layout, const lpq_qview* a, const lpq_qview* b, void* c, int32_t c_is_fp32, int64_t m,
                     int64_t n, int64_t k, lpq_stream_t stream) {
+  return lpq_gemm_ex(layout, a, b, c, c_is_fp32, m, n, k, nullptr, stream);
+}
+
+lpq_status lpq_gemm_ex(int32_t layout, const lpq_qview* a, const lpq_qview* b, void* c, int32_t c_is_fp32, int64_t m,
+                       int64_t n, int64_t k, const lpq_gemm_opts* opts, lpq_stream_t stream) {
   if (!a || !b) return set_error(LPQ_ERR_INVALID_ARG, "NULL operand");
+  if (opts) {
+    if (opts->single_cta < 0 || opts->single_cta > 1 || opts->scale_copies < 0 || opts->scale_copies > 1 ||
+        opts->direct_store < 0 || opts->direct_store > 1 || !(opts->tile_n == 0 || opts->tile_n == 128 || opts->tile_n == 256))
+      return set_error(LPQ_ERR_INVALID_ARG, "lpq_gemm_opts: single_cta, scale_copies, direct_store 0/1; tile_n 0, 128 or 256");
+    for (int i = 0; i < 4; ++i)
+      if (opts->reserved[i]) return set_error(LPQ_ERR_INVALID_ARG, "lpq_gemm_opts.reserved must be 0");
+  }
   if (layout < LPQ_FPROP || layout > LPQ_WGRAD) return set_error(LPQ_ERR_INVALID_ARG, "layout %d", layout);
   if (m < 0 || n < 0 || k < 0) return set_error(LPQ_ERR_SHAPE, "negative dimension");
   if (a->rows != m || a->cols != k) return set_error(LPQ_ERR_SHAPE, "a is %lld x %lld, expected m x k = %lld x %lld",
@@ -239,7 +289,7 @@ lpq_status lpq_gemm(int32_t layout, const lpq_qview* a, const lpq_qview* b, void
   }
   lpq_status st = check_arch();
   if (st != LPQ_OK) return st;
-  return launch_gemm(a, b, c, c_is_fp32, m, n, k, reinterpret_cast<cudaStream_t>(stream));
+  return launch_gemm(a, b, c, c_is_fp32, m, n, k, opts, reinterpret_cast<cudaStream_t>(stream));
 }
 
 lpq_status lpq_layer_shapes(const lpq_transformer_cfg* cfg, lpq_gemm_shape out[12], int32_t* count) {
@@ -283,8 +333,10 @@ lpq_status lpq_selftest_wait(uint64_t limit_ns, lpq_stream_t stream) {
 lpq_status lpq_mma_peak(int32_t kind, int32_t iters, int32_t with_scale_copies, lpq_stream_t stream) {
   if (kind < 0 || kind > 3) return set_error(LPQ_ERR_INVALID_ARG, "kind %d", kind);
   if (iters < 1 || iters > (1 << 24)) return set_error(LPQ_ERR_INVALID_ARG, "iters %d", iters);
-  if (with_scale_copies < 0 || with_scale_copies > 5 || (with_scale_copies > 1 && kind != 3))
-    return set_error(LPQ_ERR_INVALID_ARG, "with_scale_copies %d for kind %d", with_scale_copies, kind);
+  const bool ok_mode = (with_scale_copies >= 0 && with_scale_copies <= 1) ||
+                       (with_scale_copies >= 2 && with_scale_copies <= 5 && kind == 3) || with_scale_copies == 6 ||
+                       (with_scale_copies == 7 && (kind == 2 || kind == 3));
+  if (!ok_mode) return set_error(LPQ_ERR_INVALID_ARG, "with_scale_copies %d for kind %d", with_scale_copies, kind);
   lpq_status st = check_arch();
   if (st != LPQ_OK) return st;
   return launch_mma_peak(kind, iters, with_scale_copies, reinterpret_cast<cudaStream_t>(stream));

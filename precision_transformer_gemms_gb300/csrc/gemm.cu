@@ -9,8 +9,8 @@
 // factors with bulk or TMA copies; warp 1 (one lane) issues the tcgen05.mma
 // instructions, accumulating in FP32 in TMEM; for the block-scaled kinds four
 // scale warps write each stage's scale factors into a TMEM slot with
-// tcgen05.st (or, LPQ_GEMM_SFCP=1, the MMA thread copies them with
-// tcgen05.cp); eight epilogue warps read the accumulator back with
+// tcgen05.st (or, with lpq_gemm_opts.scale_copies, the MMA thread copies them
+// with tcgen05.cp); eight epilogue warps read the accumulator back with
 // tcgen05.ld, apply the per-tensor scale product and store bf16 or FP32.  The
 // default for M >= 256 is a CTA pair (cta_group::2) per 256 x 256 tile.
 //
@@ -452,35 +452,17 @@ uint32_t idesc_block_scaled(uint32_t afmt, uint32_t bfmt, uint32_t e8m0, int n) 
   return (afmt << 7) | (bfmt << 10) | ((uint32_t)(n >> 3) << 17) | (e8m0 << 23) | ((uint32_t)(kBM >> 4) << 24);
 }
 
-int g_sms = 0;
-
-// An environment switch set to something other than "0" (read per call).
-bool getenv_flag(const char* name) {
-  const char* e = getenv(name);
-  return e && e[0] && e[0] != '0';
-}
-
 template <int KIND, int BN, int NACC, bool SFST = false>
 lpq_status run(const CUtensorMap& ta, const CUtensorMap& tb, GemmArgs g, cudaStream_t s) {
   using CF = Cfg<KIND, BN, NACC, SFST>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<KIND, BN, NACC, SFST>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         CF::kSmem);
-    if (e != cudaSuccess) return cuda_check(e, "cudaFuncSetAttribute(gemm smem)");
-    attr_set = true;
-  }
-  if (g_sms == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&g_sms, cudaDevAttrMultiProcessorCount, dev);
-    if (g_sms <= 0) g_sms = 148;
-  }
+  lpq_status st = set_smem_attr(reinterpret_cast<const void*>(gemm_kernel<KIND, BN, NACC, SFST>), CF::kSmem);
+  if (st != LPQ_OK) return st;
+  const int sms = device_sms();
   const int64_t tm = (g.M + kBM - 1) / kBM, tn = (g.N + BN - 1) / BN;
   if (tm * tn > (int64_t)1 << 30) return set_error(LPQ_ERR_SHAPE, "too many output tiles");
   g.tiles_m = (int)tm;
   g.tiles_n = (int)tn;
-  const int grid = (int)std::min<int64_t>(tm * tn, g_sms);
+  const int grid = (int)std::min<int64_t>(tm * tn, sms);
   gemm_kernel<KIND, BN, NACC, SFST><<<grid, kThreadsGemm + (SFST ? 32 * kSfWarps : 0), CF::kSmem, s>>>(ta, tb, g);
   return cuda_check(cudaGetLastError(), "gemm kernel launch");
 }
@@ -891,32 +873,21 @@ lpq_status make_sf_map(CUtensorMap* map, const void* base, int64_t total_atoms, 
 
 template <int KIND, bool kSfbFull, bool SFST = false>
 lpq_status run_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tsa, const CUtensorMap& tsb,
-                    GemmArgs g, cudaStream_t s) {
+                    GemmArgs g, bool direct_store, cudaStream_t s) {
   using PC = PairCfg<KIND, kSfbFull, SFST>;
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_pair_kernel<KIND, kSfbFull, SFST>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, PC::kSmem);
-    if (e != cudaSuccess) return cuda_check(e, "cudaFuncSetAttribute(pair gemm)");
-    attr = true;
-  }
-  if (g_sms == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&g_sms, cudaDevAttrMultiProcessorCount, dev);
-    if (g_sms <= 0) g_sms = 148;
-  }
+  lpq_status st = set_smem_attr(reinterpret_cast<const void*>(gemm_pair_kernel<KIND, kSfbFull, SFST>), PC::kSmem);
+  if (st != LPQ_OK) return st;
+  const int sms = device_sms();
   const int64_t tm = (g.M + 255) / 256, tn = (g.N + kPairBN - 1) / kPairBN;
   g.tiles_m = (int)tm;
   g.tiles_n = (int)tn;
-  const int pairs = (int)std::min<int64_t>(tm * tn, g_sms / 2);
+  const int pairs = (int)std::min<int64_t>(tm * tn, sms / 2);
   // bf16 C leaves through TMA tile stores (32 x 64 boxes) when its row pitch
   // allows a tensor map (N % 8 == 0); otherwise the epilogue stores directly.
   CUtensorMap tc = ta;
   g.c_tma = 0;
-  if (!g.c_fp32 && g.N % 8 == 0 && !getenv_flag("LPQ_GEMM_DIRECT_STORE")) {
-    lpq_status st = make_map(&tc, g.c, true, g.N, g.M, g.N * 2, 64, 32);
-    if (st != LPQ_OK) return st;
+  if (!g.c_fp32 && g.N % 8 == 0 && !direct_store) {
+    if ((st = make_map(&tc, g.c, true, g.N, g.M, g.N * 2, 64, 32)) != LPQ_OK) return st;
     g.c_tma = 1;
   }
   gemm_pair_kernel<KIND, kSfbFull, SFST>
@@ -924,14 +895,6 @@ lpq_status run_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensor
   return cuda_check(cudaGetLastError(), "pair gemm launch");
 }
 
-// Kernel path per GEMM: the CTA-pair kernel (256 x 256 tiles) for every kind
-// when M >= 256 (each SM streams half the B bytes of a single-CTA tile).
-// LPQ_GEMM_PAIR=0 forces single CTAs; read on every call so both paths can be
-// exercised.
-bool use_pair(int /*kind*/) {
-  const char* e = getenv("LPQ_GEMM_PAIR");
-  return !(e && e[0] == '0');
-}
 // Sub-channel FP8 GEMM ("Faster training throughput in FP8 with NVIDIA NeMo",
 // sub-channel scaling: 1x128 activation and 128x128 weight blocks with FP32
 // factors).  Every 128-deep K slice is one pipeline stage: the MMA warp
@@ -1182,38 +1145,21 @@ __global__ void __launch_bounds__(kBlkThreads, 1)
 }
 
 lpq_status run_block_gemm(const CUtensorMap& ta, const CUtensorMap& tb, BlockArgs g, cudaStream_t s) {
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(block_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kBlkSmem);
-    if (e != cudaSuccess) return cuda_check(e, "cudaFuncSetAttribute(block gemm)");
-    attr = true;
-  }
-  if (g_sms == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&g_sms, cudaDevAttrMultiProcessorCount, dev);
-    if (g_sms <= 0) g_sms = 148;
-  }
+  lpq_status st = set_smem_attr(reinterpret_cast<const void*>(block_gemm_kernel), kBlkSmem);
+  if (st != LPQ_OK) return st;
+  const int sms = device_sms();
   const int64_t tm = (g.M + kBM - 1) / kBM, tn = (g.N + kBlkBN - 1) / kBlkBN;
   g.tiles_m = (int)tm;
   g.tiles_n = (int)tn;
-  const int grid = (int)std::min<int64_t>(tm * tn, g_sms);
+  const int grid = (int)std::min<int64_t>(tm * tn, sms);
   block_gemm_kernel<<<grid, kBlkThreads, kBlkSmem, s>>>(ta, tb, g);
   return cuda_check(cudaGetLastError(), "block gemm launch");
-}
-
-// Output-tile width of the single-CTA block-scaled GEMMs: 256 (one TMEM
-// accumulator) or 128 (two accumulators, epilogue overlapped); LPQ_GEMM_BN=128
-// selects the latter, read on every call like the other path switches.
-int lpq_gemm_config_bn() {
-  const char* e = getenv("LPQ_GEMM_BN");
-  return (e && atoi(e) == 128) ? 128 : 256;
 }
 
 }  // namespace
 
 lpq_status launch_gemm(const lpq_qview* a, const lpq_qview* b, void* c, int32_t c_is_fp32, int64_t m, int64_t n,
-                       int64_t k, cudaStream_t s) {
+                       int64_t k, const lpq_gemm_opts* opts, cudaStream_t s) {
   if (m == 0 || n == 0) return LPQ_OK;
   const int32_t fa = a->fmt, fb = b->fmt;
   GemmArgs g{};
@@ -1230,17 +1176,23 @@ lpq_status launch_gemm(const lpq_qview* a, const lpq_qview* b, void* c, int32_t 
   CUtensorMap ta, tb;
   lpq_status st;
   constexpr int BN = 256;
-  const int nv_bn = lpq_gemm_config_bn();
+  // Kernel path (lpq_gemm_opts; NULL = the defaults): CTA pairs per 256 x 256
+  // tile whenever M >= 256, else one CTA per 128 x 256 tile; block-scaled
+  // scales written into TMEM by the scale warps; bf16 C through TMA stores.
+  const bool pair_ok = !(opts && opts->single_cta) && m >= 256;
+  const int nv_bn = (opts && opts->tile_n == 128) ? 128 : 256;
+  const bool cp = opts && opts->scale_copies;
+  const bool direct = opts && opts->direct_store;
   if (fa == LPQ_BF16) {
     g.num_k = (int)((k * 2 + kKBytes - 1) / kKBytes);
     if ((st = make_map(&ta, a->codes, true, k, m, k * 2, 64, kBM)) != LPQ_OK) return st;
     if ((st = make_map(&tb, b->codes, true, k, n, k * 2, 64, BN)) != LPQ_OK) return st;
     g.idesc = idesc_dense(1, 1, BN);  // BF16 x BF16 -> F32
-    if (use_pair(kKindF16) && m >= 256) {
+    if (pair_ok) {
       if ((st = make_map(&ta, a->codes, true, k, m, k * 2, 64, kBM)) != LPQ_OK) return st;
       if ((st = make_map(&tb, b->codes, true, k, n, k * 2, 64, kPairBN / 2)) != LPQ_OK) return st;
       g.idesc = idesc_dense(1, 1, kPairBN) & ~(31u << 24) | (16u << 24);  // M = 256
-      return run_pair<kKindF16, true>(ta, tb, ta, tb, g, s);
+      return run_pair<kKindF16, true>(ta, tb, ta, tb, g, direct, s);
     }
     return run<kKindF16, BN, 2>(ta, tb, g, s);
   }
@@ -1251,10 +1203,10 @@ lpq_status launch_gemm(const lpq_qview* a, const lpq_qview* b, void* c, int32_t 
     g.idesc = idesc_dense(fa == LPQ_FP8_E5M2 ? 1 : 0, fb == LPQ_FP8_E5M2 ? 1 : 0, BN);
     g.alpha_a = a->tensor_scale;
     g.alpha_b = b->tensor_scale;
-    if (use_pair(kKindF8F6F4) && m >= 256) {
+    if (pair_ok) {
       if ((st = make_map(&tb, b->codes, false, k, n, k, 128, kPairBN / 2)) != LPQ_OK) return st;
       g.idesc = (g.idesc & ~(31u << 24)) | (16u << 24);  // M = 256
-      return run_pair<kKindF8F6F4, true>(ta, tb, ta, tb, g, s);
+      return run_pair<kKindF8F6F4, true>(ta, tb, ta, tb, g, direct, s);
     }
     return run<kKindF8F6F4, BN, 2>(ta, tb, g, s);
   }
@@ -1270,17 +1222,16 @@ lpq_status launch_gemm(const lpq_qview* a, const lpq_qview* b, void* c, int32_t 
     g.sfa_kt = sf_kt_atoms(LPQ_MXFP8, k);
     g.sfb_kt = g.sfa_kt;
     g.sfb_groups = sf_row_groups(n);
-    // scale atoms into TMEM by the scale warps (tcgen05.st); LPQ_GEMM_SFCP=1:
+    // scale atoms into TMEM by the scale warps (tcgen05.st), or (scale_copies)
     // tcgen05.cp by the MMA thread
-    const bool cp = getenv_flag("LPQ_GEMM_SFCP");
-    if (use_pair(kKindMXF8) && m >= 256) {
+    if (pair_ok) {
       CUtensorMap tsa, tsb;
       if ((st = make_map(&tb, b->codes, false, k, n, k, 128, kPairBN / 2)) != LPQ_OK) return st;
       if ((st = make_sf_map(&tsa, g.sfa, sf_row_groups(m) * g.sfa_kt, 1)) != LPQ_OK) return st;
       if ((st = make_sf_map(&tsb, g.sfb, g.sfb_groups * g.sfb_kt, 1)) != LPQ_OK) return st;
       g.idesc = (g.idesc & ~(31u << 24)) | (16u << 24);
-      if (cp) return run_pair<kKindMXF8, true>(ta, tb, tsa, tsb, g, s);
-      return run_pair<kKindMXF8, true, true>(ta, tb, tsa, tsb, g, s);
+      if (cp) return run_pair<kKindMXF8, true>(ta, tb, tsa, tsb, g, direct, s);
+      return run_pair<kKindMXF8, true, true>(ta, tb, tsa, tsb, g, direct, s);
     }
     if (nv_bn == 128) {
       if ((st = make_map(&tb, b->codes, false, k, n, k, 128, 128)) != LPQ_OK) return st;
@@ -1294,7 +1245,7 @@ lpq_status launch_gemm(const lpq_qview* a, const lpq_qview* b, void* c, int32_t 
   if (fa == LPQ_MXFP4) {
     // packed E2M1 (format 1) with an E8M0 scale per 32 values: two scales per
     // K = 64 MMA, two atoms per 256-value k-step; the scale warps write them
-    // into TMEM as for NVFP4 (LPQ_GEMM_SFCP=1: tcgen05.cp by the MMA thread)
+    // into TMEM as for NVFP4 (scale_copies: tcgen05.cp by the MMA thread)
     g.num_k = (int)((k / 2 + kKBytes - 1) / kKBytes);
     if ((st = make_map(&ta, a->codes, false, k / 2, m, k / 2, 128, kBM)) != LPQ_OK) return st;
     if ((st = make_map(&tb, b->codes, false, k / 2, n, k / 2, 128, BN)) != LPQ_OK) return st;
@@ -1304,15 +1255,14 @@ lpq_status launch_gemm(const lpq_qview* a, const lpq_qview* b, void* c, int32_t 
     g.sfa_kt = sf_kt_atoms(LPQ_MXFP4, k);
     g.sfb_kt = g.sfa_kt;
     g.sfb_groups = sf_row_groups(n);
-    const bool cp = getenv_flag("LPQ_GEMM_SFCP");
-    if (use_pair(kKindMXF4) && m >= 256) {
+    if (pair_ok) {
       CUtensorMap tsa, tsb;
       if ((st = make_map(&tb, b->codes, false, k / 2, n, k / 2, 128, kPairBN / 2)) != LPQ_OK) return st;
       if ((st = make_sf_map(&tsa, g.sfa, sf_row_groups(m) * g.sfa_kt, 2)) != LPQ_OK) return st;
       if ((st = make_sf_map(&tsb, g.sfb, g.sfb_groups * g.sfb_kt, 2)) != LPQ_OK) return st;
       g.idesc = (g.idesc & ~(31u << 24)) | (16u << 24);
-      if (cp) return run_pair<kKindMXF4, true>(ta, tb, tsa, tsb, g, s);
-      return run_pair<kKindMXF4, true, true>(ta, tb, tsa, tsb, g, s);
+      if (cp) return run_pair<kKindMXF4, true>(ta, tb, tsa, tsb, g, direct, s);
+      return run_pair<kKindMXF4, true, true>(ta, tb, tsa, tsb, g, direct, s);
     }
     if (nv_bn == 128) {
       if ((st = make_map(&tb, b->codes, false, k / 2, n, k / 2, 128, 128)) != LPQ_OK) return st;
@@ -1335,15 +1285,14 @@ lpq_status launch_gemm(const lpq_qview* a, const lpq_qview* b, void* c, int32_t 
     g.sfb_groups = sf_row_groups(n);
     g.alpha_a = a->tensor_scale;
     g.alpha_b = b->tensor_scale;
-    const bool cp = getenv_flag("LPQ_GEMM_SFCP");  // scale copies by the MMA thread (tcgen05.cp)
-    if (use_pair(kKindNVF4) && m >= 256) {
+    if (pair_ok) {
       CUtensorMap tsa, tsb;
       if ((st = make_map(&tb, b->codes, false, k / 2, n, k / 2, 128, kPairBN / 2)) != LPQ_OK) return st;
       if ((st = make_sf_map(&tsa, g.sfa, sf_row_groups(m) * g.sfa_kt, 4)) != LPQ_OK) return st;
       if ((st = make_sf_map(&tsb, g.sfb, g.sfb_groups * g.sfb_kt, 4)) != LPQ_OK) return st;
       g.idesc = (g.idesc & ~(31u << 24)) | (16u << 24);
-      if (cp) return run_pair<kKindNVF4, true>(ta, tb, tsa, tsb, g, s);
-      return run_pair<kKindNVF4, true, true>(ta, tb, tsa, tsb, g, s);
+      if (cp) return run_pair<kKindNVF4, true>(ta, tb, tsa, tsb, g, direct, s);
+      return run_pair<kKindNVF4, true, true>(ta, tb, tsa, tsb, g, direct, s);
     }
     if (nv_bn == 128) {
       if ((st = make_map(&tb, b->codes, false, k / 2, n, k / 2, 128, 128)) != LPQ_OK) return st;
@@ -1488,25 +1437,123 @@ __global__ void __launch_bounds__(256, 1) mma_peak_kernel(int iters, uint32_t id
   }
 }
 
+// The same rate measurement on CTA pairs (cta_group::2), the shape the
+// product GEMM issues: each cluster of two CTAs runs `iters` k-steps of four
+// 256 x 256 pair MMAs (each SM holds 128 rows of A and 128 rows of B in shared
+// memory, as in gemm_pair_kernel).  MODE 7 (block-scaled kinds) has four warps
+// per CTA rewrite the scale columns with tcgen05.st while the MMAs run
+// (unsynchronised; a rate probe).
+template <int KIND, int MODE>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1) mma_peak_pair_kernel(int iters, uint32_t idesc) {
+  using PC = PairCfg<KIND, true, false>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = sA + PC::kA;
+  uint8_t* sSf = sB + PC::kB;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sSf + PC::kSfa + PC::kSfb);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 1);
+  int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+  const int warp = threadIdx.x >> 5;
+  const bool leader = cluster_ctarank() == 0;
+  for (int i = threadIdx.x; i < (PC::kA + PC::kB + PC::kSfa + PC::kSfb) / 16; i += blockDim.x)
+    reinterpret_cast<uint4*>(smem)[i] = make_uint4(0, 0, 0, 0);
+  if (threadIdx.x == 0) {
+    mbar_init(bar, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  fence_proxy_async_smem();
+  if (warp == 1) tmem_alloc_pair(tmem_slot, 512);
+  tc_fence_before();
+  cluster_sync_all();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+  const uint32_t tsfa = tbase + kPairBN, tsfb = tsfa + PC::kSfaCols;
+  if (MODE == 7 && warp >= 4) {
+    if constexpr (MODE == 7 && PC::kSfAtoms > 0) {
+      uint32_t va[PC::kSfaCols], vb[PC::kSfbCols];
+#pragma unroll
+      for (int i = 0; i < PC::kSfaCols; ++i) va[i] = 0x38383838u;
+#pragma unroll
+      for (int i = 0; i < PC::kSfbCols; ++i) vb[i] = 0x38383838u;
+      const uint32_t lanes = (uint32_t)((warp & 3) * 32) << 16;
+      for (int it = 0; it < iters; ++it) {
+        tmem_st_cols(tsfa + lanes, va);
+        tmem_st_cols(tsfb + lanes, vb);
+        tmem_wait_st();
+      }
+    }
+  }
+  if (threadIdx.x == 0) {
+    if (leader) {
+      const uint32_t kHiSw = (uint32_t)(smem_desc(0, 16, 1024, 2) >> 32);
+      const uint32_t alo = (uint32_t)smem_desc(smem_u32(sA), 16, 1024, 2);
+      const uint32_t blo = (uint32_t)smem_desc(smem_u32(sB), 16, 1024, 2);
+      for (int it = 0; it < iters; ++it) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint64_t ad = ((uint64_t)kHiSw << 32) | (alo + 2 * j);
+          const uint64_t bd = ((uint64_t)kHiSw << 32) | (blo + 2 * j);
+          const uint32_t acc = (it > 0 || j > 0) ? 1u : 0u;
+          if constexpr (KIND == kKindF16 || KIND == kKindF8F6F4) {
+            mma_pair<KIND>(tbase, ad, bd, idesc, acc);
+          } else {
+            const int at = j * PC::kSfAtoms / 4;
+            mma_pair_bs<KIND>(tbase, ad, bd, idesc | sf_select<KIND>(j), tsfa + 4 * at, tsfb + 8 * at, acc);
+          }
+        }
+      }
+      tc_commit_pair(bar, 0x3);
+    }
+    mbar_wait_bounded(bar, 0, abort_flag, &g_device_error);
+  }
+  tc_fence_before();
+  cluster_sync_all();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tbase, 512);
+  }
+}
+
+template <int KIND, int MODE>
+lpq_status run_peak_pair(int iters, uint32_t idesc, cudaStream_t s) {
+  using PC = PairCfg<KIND, true, false>;
+  const int smem = PC::kA + PC::kB + PC::kSfa + PC::kSfb + 1024 + 256;
+  lpq_status st = set_smem_attr(reinterpret_cast<const void*>(mma_peak_pair_kernel<KIND, MODE>), smem);
+  if (st != LPQ_OK) return st;
+  const int sms = device_sms();
+  mma_peak_pair_kernel<KIND, MODE><<<sms & ~1, 256, smem, s>>>(iters, (idesc & ~(31u << 24)) | (16u << 24));
+  return cuda_check(cudaGetLastError(), "pair peak kernel launch");
+}
+
 template <int KIND, int MODE>
 lpq_status run_peak(int iters, uint32_t idesc, cudaStream_t s) {
   using CF = Cfg<KIND, 256, 1>;
   const int smem = CF::kA + CF::kB + CF::kSfa + CF::kSfb + 1024 + 256;
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(mma_peak_kernel<KIND, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return cuda_check(e, "cudaFuncSetAttribute(peak)");
-    attr = true;
-  }
-  int dev = 0, sms = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  lpq_status st = set_smem_attr(reinterpret_cast<const void*>(mma_peak_kernel<KIND, MODE>), smem);
+  if (st != LPQ_OK) return st;
+  const int sms = device_sms();
   mma_peak_kernel<KIND, MODE><<<sms, MODE >= 4 ? 256 : 128, smem, s>>>(iters, idesc);
   return cuda_check(cudaGetLastError(), "peak kernel launch");
 }
 
 lpq_status launch_mma_peak(int32_t kind, int32_t iters, int32_t with_sf, cudaStream_t s) {
   const uint32_t mx = idesc_block_scaled(0, 0, 1, 256), nv = idesc_block_scaled(1, 1, 0, 256);
+  if (with_sf == 6) {  // CTA pairs, no scale traffic
+    switch (kind) {
+      case kKindF16: return run_peak_pair<kKindF16, 6>(iters, idesc_dense(1, 1, 256), s);
+      case kKindF8F6F4: return run_peak_pair<kKindF8F6F4, 6>(iters, idesc_dense(0, 0, 256), s);
+      case kKindMXF8: return run_peak_pair<kKindMXF8, 6>(iters, mx, s);
+      case kKindNVF4: return run_peak_pair<kKindNVF4, 6>(iters, nv, s);
+    }
+    return set_error(LPQ_ERR_INVALID_ARG, "kind %d", kind);
+  }
+  if (with_sf == 7) {  // CTA pairs, scale columns rewritten by four warps per CTA
+    if (kind == kKindMXF8) return run_peak_pair<kKindMXF8, 7>(iters, mx, s);
+    if (kind == kKindNVF4) return run_peak_pair<kKindNVF4, 7>(iters, nv, s);
+    return set_error(LPQ_ERR_INVALID_ARG, "mode 7 is for the block-scaled kinds");
+  }
   switch (kind) {
     case kKindF16: return run_peak<kKindF16, 0>(iters, idesc_dense(1, 1, 256), s);
     case kKindF8F6F4: return run_peak<kKindF8F6F4, 0>(iters, idesc_dense(0, 0, 256), s);

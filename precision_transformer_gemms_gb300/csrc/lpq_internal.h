@@ -18,6 +18,13 @@ enum { kKindF16 = 0, kKindF8F6F4 = 1, kKindMXF8 = 2, kKindNVF4 = 3, kKindMXF4 = 
 lpq_status set_error(lpq_status st, const char* fmt, ...);
 lpq_status cuda_check(cudaError_t e, const char* what);
 
+// Per-device launch settings (capi.cu), safe to call from several threads:
+// the current device's SM count, and raising a kernel's dynamic shared-memory
+// limit once per (device, kernel) -- cudaFuncSetAttribute acts on the current
+// device only, so a second GPU in the same process needs its own call.
+int device_sms();
+lpq_status set_smem_attr(const void* kernel, int bytes);
+
 // Scale-factor geometry of the tensor-core layout.
 // Atoms (4 scales of 128 rows) per 128-row group: one per 128 columns for
 // MXFP8, two per 256 columns for MXFP4 (a 256-value k-step of packed E2M1
@@ -38,7 +45,7 @@ lpq_status launch_scale_update(const lpq_delayed_state* state, const float* amax
 
 // GEMM launcher (gemm.cu).  Operands validated.
 lpq_status launch_gemm(const lpq_qview* a, const lpq_qview* b, void* c, int32_t c_is_fp32, int64_t m,
-                       int64_t n, int64_t k, cudaStream_t stream);
+                       int64_t n, int64_t k, const lpq_gemm_opts* opts, cudaStream_t stream);
 
 // Device error word (gemm.cu owns it).
 lpq_status read_and_clear_device_error(cudaStream_t stream, int32_t* code);

@@ -770,18 +770,6 @@ __global__ void scale_update_kernel(float* hist, int32_t* pos, float* scale, flo
   }
 }
 
-int g_num_sms = 0;
-
-int num_sms() {
-  if (g_num_sms == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
-    if (g_num_sms <= 0) g_num_sms = 148;
-  }
-  return g_num_sms;
-}
-
 template <int KIND, bool kE5M2, int NVO = 0>
 lpq_status run_tile(const QParams& p, cudaStream_t s) {
   constexpr int TR = (KIND == QK_BLK1 || KIND == QK_BLK128) ? 128 : 64;
@@ -802,7 +790,7 @@ lpq_status run_amax(const uint16_t* x, int64_t R, int64_t C, float* o0, float* o
                     uint32_t rht_seed, cudaStream_t s) {
   const int64_t units = rht_out ? (R / 16) * (C / 8) : R * (C / 8);
   int64_t blocks = (units + kThreads - 1) / kThreads;
-  const int64_t cap = (int64_t)num_sms() * 8;
+  const int64_t cap = (int64_t)device_sms() * 8;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
   if (rht_out)

@@ -52,6 +52,23 @@ class DelayedStateC(ctypes.Structure):
                 ("scale_inv", ctypes.c_void_p), ("len", ctypes.c_int32)]
 
 
+class GemmOpts(ctypes.Structure):
+    """Kernel-path options of lpq_gemm_ex (all zero: the default path)."""
+    _fields_ = [("single_cta", ctypes.c_int32), ("tile_n", ctypes.c_int32), ("scale_copies", ctypes.c_int32),
+                ("direct_store", ctypes.c_int32), ("reserved", ctypes.c_int32 * 4)]
+
+
+# Named kernel paths of the GEMM (every one computes the same result).
+GEMM_PATHS = {
+    "default": GemmOpts(),
+    "pair": GemmOpts(),                               # CTA pairs where m >= 256 (the default)
+    "pair_direct": GemmOpts(direct_store=1),          # CTA pairs, bf16 C stored from registers
+    "single": GemmOpts(single_cta=1),                 # one CTA per 128 x 256 tile
+    "single_cp": GemmOpts(single_cta=1, scale_copies=1),  # scale factors copied by the MMA thread
+    "single_bn128": GemmOpts(single_cta=1, tile_n=128),   # one CTA per 128 x 128 tile
+}
+
+
 class TransformerCfg(ctypes.Structure):
     _fields_ = [("hidden", ctypes.c_int64), ("intermediate", ctypes.c_int64), ("heads", ctypes.c_int64),
                 ("layers", ctypes.c_int64), ("micro_batch", ctypes.c_int64), ("seq", ctypes.c_int64)]
@@ -81,6 +98,8 @@ def lib():
                                    ctypes.POINTER(QTensorC), P]
         L.lpq_scale_update.argtypes = [ctypes.POINTER(DelayedStateC), P, F, P]
         L.lpq_gemm.argtypes = [I32, ctypes.POINTER(QView), ctypes.POINTER(QView), P, I32, I64, I64, I64, P]
+        L.lpq_gemm_ex.argtypes = [I32, ctypes.POINTER(QView), ctypes.POINTER(QView), P, I32, I64, I64, I64,
+                                  ctypes.POINTER(GemmOpts), P]
         L.lpq_layer_shapes.argtypes = [ctypes.POINTER(TransformerCfg), ctypes.POINTER(GemmShape),
                                        ctypes.POINTER(I32)]
         L.lpq_last_error.restype = ctypes.c_char_p
@@ -88,7 +107,7 @@ def lib():
         L.lpq_selftest_wait.argtypes = [U64, P]
         L.lpq_mma_peak.argtypes = [I32, I32, I32, P]
         L.lpq_version.restype = I32
-        for name in ("lpq_copy_bytes", "lpq_quantize", "lpq_scale_update", "lpq_gemm", "lpq_layer_shapes",
+        for name in ("lpq_copy_bytes", "lpq_quantize", "lpq_scale_update", "lpq_gemm", "lpq_gemm_ex", "lpq_layer_shapes",
                      "lpq_device_status", "lpq_selftest_wait", "lpq_mma_peak"):
             getattr(L, name).restype = I32
         _lib = L
@@ -217,14 +236,21 @@ def scale_update(state, amax, fmax, stream=None):
     _check(lib().lpq_scale_update(ctypes.byref(state.c()), _ptr(amax), float(fmax), _stream(stream)))
 
 
-def gemm(layout, a, b, c=None, out_fp32=False, stream=None):
-    """lpq_gemm: C[m, n] = sum_k deq(a)[m, k] deq(b)[n, k]; a, b are Copy objects."""
+def gemm(layout, a, b, c=None, out_fp32=False, stream=None, path=None):
+    """lpq_gemm: C[m, n] = sum_k deq(a)[m, k] deq(b)[n, k]; a, b are Copy objects.
+    `path` (a GEMM_PATHS name or a GemmOpts) selects a kernel path through
+    lpq_gemm_ex; None is lpq_gemm's default."""
     m, k, n = a.rows, a.cols, b.rows
     if c is None:
         c = torch.empty((m, n), dtype=torch.float32 if out_fp32 else torch.bfloat16, device=a.codes.device)
     va, vb = a.view(), b.view()
-    _check(lib().lpq_gemm(layout, ctypes.byref(va), ctypes.byref(vb), _ptr(c), int(out_fp32), m, n, k,
-                          _stream(stream)))
+    if path is None:
+        _check(lib().lpq_gemm(layout, ctypes.byref(va), ctypes.byref(vb), _ptr(c), int(out_fp32), m, n, k,
+                              _stream(stream)))
+    else:
+        opts = GEMM_PATHS[path] if isinstance(path, str) else path
+        _check(lib().lpq_gemm_ex(layout, ctypes.byref(va), ctypes.byref(vb), _ptr(c), int(out_fp32), m, n, k,
+                                 ctypes.byref(opts), _stream(stream)))
     return c
 
 
@@ -243,14 +269,18 @@ MMA_K = {0: 16, 1: 32, 2: 32, 3: 64}
 
 
 def mma_peak(kind, iters=20000, with_scale_copies=True, stream=None):
-    """Dense tcgen05 rate in TFLOP/s for `kind` (see lpq_mma_peak)."""
+    """Dense tcgen05 rate in TFLOP/s for `kind` (see lpq_mma_peak; modes 6 and
+    7 run on CTA pairs)."""
     k = MMA_KINDS[kind] if isinstance(kind, str) else kind
+    mode = int(with_scale_copies)
+    st = stream if stream is not None else torch.cuda.current_stream()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    _check(lib().lpq_mma_peak(k, 64, int(with_scale_copies), _stream(stream)))  # warm-up
-    e0.record()
-    _check(lib().lpq_mma_peak(k, iters, int(with_scale_copies), _stream(stream)))  # mode 0..5
-    e1.record()
+    _check(lib().lpq_mma_peak(k, 64, mode, _stream(st)))  # warm-up
+    e0.record(st)
+    _check(lib().lpq_mma_peak(k, iters, mode, _stream(st)))  # mode 0..7
+    e1.record(st)
     torch.cuda.synchronize()
     sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
-    flops = sms * iters * 4 * 2 * 128 * 256 * MMA_K[k]
+    ctas = sms & ~1 if mode >= 6 else sms
+    flops = ctas * iters * 4 * 2 * 128 * 256 * MMA_K[k]
     return flops / (e0.elapsed_time(e1) * 1e-3) / 1e12

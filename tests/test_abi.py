@@ -137,8 +137,28 @@ def test_mma_peak_validation():
     L = lpq.lib()
     assert L.lpq_mma_peak(4, 10, 0, None) == lpq.ERR_INVALID_ARG     # no such kind
     assert L.lpq_mma_peak(3, 0, 0, None) == lpq.ERR_INVALID_ARG      # iters
-    assert L.lpq_mma_peak(3, 10, 6, None) == lpq.ERR_INVALID_ARG     # no such mode
+    assert L.lpq_mma_peak(3, 10, 8, None) == lpq.ERR_INVALID_ARG     # no such mode
     assert L.lpq_mma_peak(2, 10, 4, None) == lpq.ERR_INVALID_ARG     # modes 2..5 are NVFP4 only
+    assert L.lpq_mma_peak(0, 10, 7, None) == lpq.ERR_INVALID_ARG     # mode 7 is for the block-scaled kinds
+    assert L.lpq_mma_peak(1, 10, -1, None) == lpq.ERR_INVALID_ARG
+
+
+def test_gemm_options_validation():
+    """lpq_gemm_ex checks its kernel-path options before anything else; the
+    default options (all zero, or NULL) validate like lpq_gemm."""
+    L = lpq.lib()
+    v = lambda rows, cols: lpq.QView(16, 16, 16, 16, rows, cols, lpq.MXFP8, lpq.SF_GEMM, 0, 0)
+    a, b = v(128, 256), v(64, 256)
+    bad = [lpq.GemmOpts(single_cta=2), lpq.GemmOpts(tile_n=64), lpq.GemmOpts(scale_copies=-1),
+           lpq.GemmOpts(direct_store=3), lpq.GemmOpts(reserved=(ctypes.c_int32 * 4)(0, 1, 0, 0))]
+    for opts in bad:
+        assert L.lpq_gemm_ex(0, ctypes.byref(a), ctypes.byref(b), 16, 0, 128, 64, 256, ctypes.byref(opts),
+                             None) == lpq.ERR_INVALID_ARG
+    validated = (lpq.ERR_UNSUPPORTED, lpq.ERR_SHAPE, lpq.ERR_INVALID_ARG, lpq.ERR_ALIGN)
+    for name, opts in lpq.GEMM_PATHS.items():  # legal options pass validation and stop at the device check
+        assert L.lpq_gemm_ex(0, ctypes.byref(a), ctypes.byref(b), 16, 0, 128, 64, 256, ctypes.byref(opts),
+                             None) not in validated, name
+    assert L.lpq_gemm_ex(0, ctypes.byref(a), ctypes.byref(b), 16, 0, 128, 64, 256, None, None) not in validated
 
 
 def test_given_amax_validation():

@@ -25,8 +25,8 @@ def quantize_pair(fmt_a, fmt_b, M, K, N, seed=0):
     return qa.row, qb.row
 
 
-def check(a, b, M, N, K, out_fp32, layout=lpq.FPROP):
-    c = lpq.gemm(layout, a, b, out_fp32=out_fp32)
+def check(a, b, M, N, K, out_fp32, layout=lpq.FPROP, path=None):
+    c = lpq.gemm(layout, a, b, out_fp32=out_fp32, path=path)
     torch.cuda.synchronize()
     assert lpq.device_status() == 0
     ref, bound = o.gemm(oracle_operand(a), oracle_operand(b), M, N, K)
@@ -41,7 +41,7 @@ def check(a, b, M, N, K, out_fp32, layout=lpq.FPROP):
                                   (lpq.MXFP8, lpq.MXFP8), (lpq.MXFP8_E5M2, lpq.MXFP8),
                                   (lpq.MXFP8_E5M2, lpq.MXFP8_E5M2), (lpq.MXFP4, lpq.MXFP4),
                                   (lpq.NVFP4, lpq.NVFP4), (lpq.NVFP4, lpq.NVFP4_2D)])
-def test_gemm_parity(fmts, shape, out_fp32, path, monkeypatch):
+def test_gemm_parity(fmts, shape, out_fp32, path):
     """Every kernel path: one CTA per 128 x 256 tile (block scales stored into
     TMEM by scale warps, or copied by the MMA thread: single_cp), one CTA per
     128 x 128 tile with two accumulators (block-scaled kinds: single_bn128), and
@@ -51,15 +51,11 @@ def test_gemm_parity(fmts, shape, out_fp32, path, monkeypatch):
         pytest.skip("scale-copy variant exists for the block-scaled kinds only")
     if path == "single_bn128" and fmts[0] not in (lpq.NVFP4, lpq.MXFP8, lpq.MXFP8_E5M2, lpq.MXFP4):
         pytest.skip("128-wide tiles exist for the block-scaled kinds only")
-    monkeypatch.setenv("LPQ_GEMM_PAIR", "1" if path.startswith("pair") else "0")
-    monkeypatch.setenv("LPQ_GEMM_DIRECT_STORE", "1" if path == "pair_direct" else "0")
-    monkeypatch.setenv("LPQ_GEMM_SFCP", "1" if path == "single_cp" else "0")
-    monkeypatch.setenv("LPQ_GEMM_BN", "128" if path == "single_bn128" else "256")
     M, K, N = shape
     if fmts[1] == lpq.NVFP4_2D and N % 16:
         pytest.skip("2D weight tiles need N % 16 == 0")
     a, b = quantize_pair(*fmts, M, K, N)
-    check(a, b, M, N, K, out_fp32)
+    check(a, b, M, N, K, out_fp32, path=path)
 
 
 BLOCK_SHAPES = [(4, 128, 16), (256, 512, 384), (300, 640, 200), (520, 1024, 776)]
@@ -214,7 +210,9 @@ def test_bounded_wait_reports_timeout_and_context_survives():
 
 
 @pytest.mark.parametrize("kind,mode", [("bf16", 0), ("fp8", 0), ("mxfp8", 0), ("mxfp8", 1), ("nvfp4", 0), ("nvfp4", 1),
-                                       ("nvfp4", 2), ("nvfp4", 3), ("nvfp4", 4), ("nvfp4", 5)])
+                                       ("nvfp4", 2), ("nvfp4", 3), ("nvfp4", 4), ("nvfp4", 5),
+                                       ("bf16", 6), ("fp8", 6), ("mxfp8", 6), ("nvfp4", 6), ("mxfp8", 7),
+                                       ("nvfp4", 7)])
 def test_mma_peak_modes_run(kind, mode):
     """Every rate-probe mode runs to completion with a clean device status and
     a rate below the nominal dense peak of its kind (x1.2 for clock slack)."""
@@ -227,11 +225,10 @@ def test_mma_peak_modes_run(kind, mode):
 
 @pytest.mark.parametrize("fmts", [(lpq.BF16, lpq.BF16), (lpq.FP8_E4M3, lpq.FP8_E4M3), (lpq.MXFP8, lpq.MXFP8),
                                   (lpq.MXFP4, lpq.MXFP4)])
-def test_pair_gemm_ragged_n_direct_stores(fmts, monkeypatch):
+def test_pair_gemm_ragged_n_direct_stores(fmts):
     """N not a multiple of 8: no tensor map fits the output rows, so the pair
     kernel's epilogue stores directly (bf16 and FP32 outputs)."""
-    monkeypatch.setenv("LPQ_GEMM_PAIR", "1")
     M, K, N = 512, 256, 100
     a, b = quantize_pair(*fmts, M, K, N, seed=11)
     for out_fp32 in (False, True):
-        check(a, b, M, N, K, out_fp32)
+        check(a, b, M, N, K, out_fp32, path="pair")
