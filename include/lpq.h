@@ -72,6 +72,11 @@ typedef enum {
   LPQ_MXFP4 = 9               /* packed E2M1 codes, one E8M0 scale per 32 values [NVFP4] */
 } lpq_format;
 
+/* Per-tensor FP8 scaling.  Every scale that is a quotient of a format maximum
+ * by an amax (fmax / amax, NVFP4's 2688 / amax and s_enc / dec(S), the
+ * sub-channel 448 / block max) is clamped to the largest finite float when it
+ * overflows (an amax below about fmax / 3.4e38), so zeros stay +0 and every
+ * dequantization factor stays positive. */
 typedef enum { LPQ_SCALING_CURRENT = 0, LPQ_SCALING_DELAYED = 1 } lpq_scaling;
 
 /* lpq_quantize flags */
@@ -105,7 +110,8 @@ enum {
  *                FP8, the FP32 tensor scale for NVFP4; NULL otherwise.
  *   amax         one FP32: max |value| of this copy's input values (after the
  *                Hadamard transform for an RHT copy).  Required for per-tensor
- *                FP8 and NVFP4 (lpq_quantize writes it), optional otherwise.
+ *                FP8 and NVFP4 (lpq_quantize writes it), optional for the MX
+ *                formats (written when non-NULL), unused by the others.
  *   rows, cols   dimensions of this copy (the column-wise copy of an
  *                [R, C] tensor is [C, R]).
  *   colwise      1 for a column-wise copy, 0 for a row-wise copy.        */
@@ -188,8 +194,11 @@ lpq_status lpq_quantize(const void *x, int64_t rows, int64_t cols, int32_t fmt, 
                         const lpq_delayed_state *state, lpq_qtensor *out, lpq_stream_t stream);
 
 /* Delayed-scaling update (one CTA): history[pos] = *amax; pos = (pos+1) % len;
- * m = max(history); scale = fmax / m if m > 0 and finite (else unchanged);
- * scale_inv = 1 / scale.  fmax is 448 (E4M3) or 57344 (E5M2). */
+ * m = max(history); scale = fmax / m if m > 0 and finite (else unchanged),
+ * clamped to the largest finite float if the quotient overflows;
+ * scale_inv = 1 / scale.  fmax is 448 (E4M3) or 57344 (E5M2).  pos should be
+ * in [0, len); a value outside is taken modulo len (no write leaves the
+ * history). */
 lpq_status lpq_scale_update(const lpq_delayed_state *state, const float *amax, float fmax,
                             lpq_stream_t stream);
 

@@ -268,6 +268,14 @@ float fmt_max(int fmt) { return (float)decode(fmt, (uint8_t)max_code(fmt)); }
 // Value 2^k as a float for k in [-127, 127] (2^-127 is a subnormal).
 float pow2f(int k) { return (float)std::ldexp(1.0, k); }
 
+// A scale that is the quotient of a format maximum by an amax (fmax / amax,
+// 2688 / A, 448 / block max) overflows the float range when the amax is below
+// about fmax / 3.4e38 (bf16 holds such values).  Reading: the quotient is then
+// clamped to the largest finite float.  The pages give no rule for this case;
+// an infinite scale would turn zero elements into NaN codes and the
+// dequantization factor 1 / scale into 0.
+float finite_scale(float q) { return q > 3.40282347e38f ? 3.40282347e38f : q; }
+
 // MXFP8 block exponent for block amax a ([NeMo] MXFP8: power-of-two E8M0
 // scale per 32 values).  Reading: the smallest e with 448 * 2^e >= a, i.e.
 // ceil(log2(a / 448)), so no element of the block saturates; taken from the
@@ -329,7 +337,8 @@ float orc_amax_bf16(const uint16_t* x, int64_t n) { return amax_bf16(x, n); }
 
 // ---------------------------------------------------------------- per-tensor FP8
 // Current scaling ([FP8] per-tensor dynamic scaling; [NeMo] current scaling):
-// scale = fmax / amax (fp32, RN), or 1 when amax is 0 or not finite; codes =
+// scale = fmax / amax (fp32, RN; clamped to the largest finite float if it
+// overflows), or 1 when amax is 0 or not finite; codes =
 // RNE-saturated encode of x * scale; scale_inv = 1 / scale.  Reading: no
 // margin and no power-of-two rounding of the scale (the pages state neither).
 // The column-wise copy ([C, R]) is the transpose of the same codes.
@@ -343,7 +352,7 @@ int64_t orc_fp8_pertensor(const uint16_t* x, int64_t R, int64_t C, int fmt, cons
   float amax = amax_bf16(x, R * C);
   float scale;
   if (scale_in) scale = *scale_in;
-  else scale = (amax > 0.f && std::isfinite(amax)) ? fmax / amax : 1.0f;
+  else scale = (amax > 0.f && std::isfinite(amax)) ? finite_scale(fmax / amax) : 1.0f;
   std::atomic<int64_t> sat{0};
   parallel_for(R, [&](int64_t lo, int64_t hi) {
     int64_t local = 0;
@@ -365,15 +374,17 @@ int64_t orc_fp8_pertensor(const uint16_t* x, int64_t R, int64_t C, int fmt, cons
 
 // Delayed-scaling state update ([FP8] amax history; [NeMo] per-tensor delayed
 // scaling).  Reading: the amax of this step goes into a ring of `len` entries
-// at `pos`; pos advances modulo len; the next scale is fmax / max(ring) when
-// that max is positive and finite, else the scale is kept; scale_inv = 1/scale.
+// at `pos`; pos advances modulo len; the next scale is fmax / max(ring)
+// (clamped to the largest finite float) when that max is positive and finite,
+// else the scale is kept; scale_inv = 1/scale.
 void orc_scale_update(float* hist, int32_t len, int32_t* pos, float* scale, float* scale_inv,
                       float amax, float fmax) {
-  hist[*pos] = amax;
-  *pos = (*pos + 1) % len;
+  int32_t slot = ((*pos % len) + len) % len;  // a position outside [0, len) is taken modulo len
+  hist[slot] = amax;
+  *pos = (slot + 1) % len;
   float m = 0.f;
   for (int i = 0; i < len; ++i) m = std::max(m, hist[i]);
-  if (m > 0.f && std::isfinite(m)) *scale = fmax / m;
+  if (m > 0.f && std::isfinite(m)) *scale = finite_scale(fmax / m);
   *scale_inv = 1.0f / *scale;
 }
 
@@ -458,6 +469,8 @@ int orc_mx_exponent_fmt(float a, int fmt) { return mx_exponent_fmt(a, fmt); }
 //   per block: d = (blockmax / 6) * s_enc, S = E4M3 RNE-sat encode of d;
 //   if S decodes to 0 all codes of the block are +0, else
 //   y = v * (s_enc / dec(S)) and the code is E2M1 (RNE-sat, or stochastic).
+// Both quotients (s_enc and s_enc / dec(S)) are clamped to the largest finite
+// float when they overflow, which only a tiny A (below about 4e-33) can cause.
 // Reading: the constant 2688, the operation order and ts_dec = A / 2688 are
 // choices; the pages give only "E4M3 per 16 values plus an FP32 per-tensor
 // scale".  tile2d selects one scale per 16x16 tile (weights, [TE] "2D block
@@ -482,7 +495,7 @@ static void nvfp4_copy(const std::vector<float>& v, int64_t rows, int64_t cols, 
     for (float p : part) A = std::max(A, p);
   }
   bool ok = A > 0.f && std::isfinite(A);
-  float s_enc = ok ? 2688.0f / A : 1.0f;
+  float s_enc = ok ? finite_scale(2688.0f / A) : 1.0f;
   float ts_dec = ok ? A / 2688.0f : 1.0f;
   int64_t nb = cols / 16;
   auto block_scale = [&](float bmax) {
@@ -515,7 +528,7 @@ static void nvfp4_copy(const std::vector<float>& v, int64_t rows, int64_t cols, 
         if (Sd == 0.f) {
           for (int i = 0; i < 16; ++i) q[i] = 0;
         } else {
-          float f = s_enc / Sd;
+          float f = finite_scale(s_enc / Sd);
           for (int i = 0; i < 16; ++i) {
             float y = blk[i] * f;
             if (sr) {
@@ -612,7 +625,7 @@ static void fp8_block_copy(const std::function<float(int64_t, int64_t)>& v, int6
         float m = 0.f;
         for (int64_t r = r0; r < r1; ++r)
           for (int i = 0; i < 128; ++i) m = std::max(m, std::fabs(v(r, b * 128 + i)));
-        float scale = (m > 0.f && std::isfinite(m)) ? 448.0f / m : 1.0f;
+        float scale = (m > 0.f && std::isfinite(m)) ? finite_scale(448.0f / m) : 1.0f;
         for (int64_t r = r0; r < r1; ++r)
           for (int i = 0; i < 128; ++i) codes[r * cols + b * 128 + i] = encode(E4M3, v(r, b * 128 + i) * scale);
         sinv[rb * nb + b] = 1.0f / scale;

@@ -90,6 +90,13 @@ __device__ __forceinline__ float block_max(float v, float* red) {
   return m;
 }
 
+// fmax / amax-style scale quotient, clamped to the largest finite float when
+// it overflows (an amax below about fmax / 3.4e38): an infinite scale would
+// turn zero elements into NaN codes and 1 / scale into 0.
+__device__ __forceinline__ float scale_quotient(float fmax, float a) {
+  return fminf(__fdiv_rn(fmax, a), 3.40282347e38f);
+}
+
 // NVFP4 block scale (E4M3 code) for block max `bmax` and encode scale s_enc.
 __device__ __forceinline__ uint32_t nv_block_scale(float bmax, float s_enc) {
   float d = __fmul_rn(div6_rn(bmax), s_enc);
@@ -98,12 +105,13 @@ __device__ __forceinline__ uint32_t nv_block_scale(float bmax, float s_enc) {
 
 // Per-CTA table of the encode factors s_enc / dec(S) for the 128 E4M3 codes S
 // a block scale can take (0 for S = 0, whose block is all zeros; the NaN code
-// is never produced by the saturating conversion): the per-block division
-// becomes a shared-memory lookup with the same values.
+// is never produced by the saturating conversion; clamped to the largest
+// finite float like every scale quotient): the per-block division becomes a
+// shared-memory lookup with the same values.
 __device__ __forceinline__ void nv_factor_table(float* tab, float s_enc, int t) {
   if (t >= 0 && t < 128) {
     const float Sd = t < 127 ? e4m3_value((uint32_t)t) : 0.f;
-    tab[t] = Sd == 0.f ? 0.f : __fdiv_rn(s_enc, Sd);
+    tab[t] = Sd == 0.f ? 0.f : scale_quotient(s_enc, Sd);
   }
 }
 
@@ -148,7 +156,7 @@ __device__ __forceinline__ int mx_block_exponent(float m) {
 
 __device__ __forceinline__ float nv_s_enc(const float* amax) {
   float a = *amax;
-  return finite_pos(a) ? __fdiv_rn(2688.0f, a) : 1.0f;
+  return finite_pos(a) ? scale_quotient(2688.0f, a) : 1.0f;
 }
 __device__ __forceinline__ float nv_ts_dec(const float* amax) {
   float a = *amax;
@@ -226,7 +234,7 @@ __global__ void __launch_bounds__(kThreads, KIND != QK_NV ? 1 : (NVO == 0 ? 6 : 
       scale = *p.delayed_scale;
     } else {
       float a = *p.amax_row;
-      scale = finite_pos(a) ? __fdiv_rn(kFmax, a) : 1.0f;
+      scale = finite_pos(a) ? scale_quotient(kFmax, a) : 1.0f;
     }
     if (blockIdx.x == 0 && blockIdx.y == 0 && t == 0) {
       float sinv = __fdiv_rn(1.0f, scale);
@@ -353,7 +361,7 @@ __global__ void __launch_bounds__(kThreads, KIND != QK_NV ? 1 : (NVO == 0 ? 6 : 
 #pragma unroll
       for (int i = 0; i < 8; ++i) m = absmax_acc(m, f[i]);
       m = warp_max_xor(m, 16);
-      const float s = finite_pos(m) ? __fdiv_rn(448.0f, m) : 1.0f;
+      const float s = finite_pos(m) ? scale_quotient(448.0f, m) : 1.0f;
       uint2 q = fp8_codes8<false>(f, s);
       if (ok) {
         *reinterpret_cast<uint2*>(p.row_codes + r * C + c0 + lc) = q;
@@ -384,7 +392,7 @@ __global__ void __launch_bounds__(kThreads, KIND != QK_NV ? 1 : (NVO == 0 ? 6 : 
   // ---------------------------------------------------------------- 128x128 tiles
   if constexpr (KIND == QK_BLK128) {
     const float m = block_max(local_amax, red);
-    const float s = finite_pos(m) ? __fdiv_rn(448.0f, m) : 1.0f;
+    const float s = finite_pos(m) ? scale_quotient(448.0f, m) : 1.0f;
     const float sinv = __fdiv_rn(1.0f, s);
     const int64_t nrb = (R + 127) >> 7, ncb = C >> 7;
     if (t == 0) {
@@ -430,7 +438,7 @@ __global__ void __launch_bounds__(kThreads, KIND != QK_NV ? 1 : (NVO == 0 ? 6 : 
     part[rh][cl] = m;
     __syncthreads();
     m = fmaxf(part[0][cl], part[1][cl]);
-    const float s = finite_pos(m) ? __fdiv_rn(448.0f, m) : 1.0f;
+    const float s = finite_pos(m) ? scale_quotient(448.0f, m) : 1.0f;
     if (c < C && rbase < R) {
 #pragma unroll
       for (int q4 = 0; q4 < 4; ++q4) {
@@ -737,7 +745,7 @@ __global__ void given_amax_scales_kernel(int nvfp4, float fmax, const float* ama
     if (nvfp4) {
       *ts[i] = finite_pos(a) ? __fdiv_rn(a, 2688.0f) : 1.0f;
     } else {
-      const float scale = finite_pos(a) ? __fdiv_rn(fmax, a) : 1.0f;
+      const float scale = finite_pos(a) ? scale_quotient(fmax, a) : 1.0f;
       *ts[i] = __fdiv_rn(1.0f, scale);
     }
   }
@@ -750,7 +758,9 @@ __global__ void scale_update_kernel(float* hist, int32_t* pos, float* scale, flo
   __shared__ int32_t slot;
   const int t = threadIdx.x;
   if (t == 0) {
-    slot = *pos;
+    // A position outside [0, len) (a corrupted or foreign checkpoint) is taken
+    // modulo len, so the ring write stays inside the history.
+    slot = ((*pos % len) + len) % len;
     hist[slot] = *amax;
     *pos = (slot + 1) % len;
   }
@@ -764,7 +774,7 @@ __global__ void scale_update_kernel(float* hist, int32_t* pos, float* scale, flo
     float mm = 0.f;
     for (int i = 0; i < (int)(blockDim.x >> 5); ++i) mm = fmaxf(mm, red[i]);
     float s = *scale;
-    if (finite_pos(mm)) s = __fdiv_rn(fmax, mm);
+    if (finite_pos(mm)) s = scale_quotient(fmax, mm);
     *scale = s;
     *scale_inv = __fdiv_rn(1.0f, s);
   }
@@ -917,9 +927,14 @@ lpq_status launch_quantize(const void* xv, int64_t R, int64_t C, int32_t fmt, in
     case LPQ_MXFP8:
     case LPQ_MXFP8_E5M2:
     case LPQ_MXFP4:
-      if (rv && rv->amax) {  // optional amax output
-        if ((st = zero_f32(rv->amax, s)) != LPQ_OK) return st;
-        if ((st = run_amax(p.x, R, C, rv->amax, cv ? cv->amax : nullptr, nullptr, 0, s)) != LPQ_OK) return st;
+      {  // optional amax outputs: whichever views ask for one get max |x|
+        float* a0 = rv ? rv->amax : nullptr;
+        float* a1 = cv ? cv->amax : nullptr;
+        if (!a0) { a0 = a1; a1 = nullptr; }
+        if (a0) {
+          if ((st = zero_f32(a0, s)) != LPQ_OK || (st = zero_f32(a1, s)) != LPQ_OK) return st;
+          if ((st = run_amax(p.x, R, C, a0, a1, nullptr, 0, s)) != LPQ_OK) return st;
+        }
       }
       if (fmt == LPQ_MXFP4) return run_tile<QK_MX4, false>(p, s);
       return fmt == LPQ_MXFP8_E5M2 ? run_tile<QK_MX, true>(p, s) : run_tile<QK_MX, false>(p, s);

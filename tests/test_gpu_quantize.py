@@ -279,6 +279,81 @@ def test_nvfp4_nonfinite_inputs_follow_the_oracle():
         assert scalar(q.row.tensor_scale) == np.float32(ref["row_ts"])
 
 
+def test_tiny_amax_scales_follow_the_oracle():
+    """Tensors whose amax is below fmax / FLT_MAX (2^-123, and a block max at
+    the smallest bf16 subnormal 2^-133): every scale quotient that overflows
+    is clamped to the largest finite float on both sides, so zeros stay +0 and
+    the dequantization factors stay positive.  Per-tensor FP8 (current and
+    delayed, after a scale update with that amax), NVFP4 (plain, RHT, SR, 2D),
+    and sub-channel FP8, bit-exact against the oracle."""
+    z = torch.zeros((64, 128), dtype=torch.bfloat16, device="cuda")
+    z[1, 5], z[2, 7], z[33, 16], z[40, 100] = 2.0 ** -123, -(2.0 ** -123), 2.0 ** -133, 2.0 ** -130
+    bits = synth.host_bits(z)
+    for fmt, of in ((lpq.FP8_E4M3, o.E4M3), (lpq.FP8_E5M2, o.E5M2)):
+        q = lpq.quantize(z, fmt, BOTH)
+        ref = o.fp8_pertensor(bits, of)
+        eq(codes(q.row), ref["row"])
+        eq(codes(q.col), ref["col"])
+        assert scalar(q.row.tensor_scale) == np.float32(ref["scale_inv"]) > 0
+        st, st_ref = lpq.DelayedState(16), o.DelayedState(16)
+        lpq.scale_update(st, q.row.amax, lpq.FMAX[fmt])
+        st_ref.update(ref["amax"], o.FMAX[of])
+        assert scalar(st.scale) == st_ref.scale[0] and scalar(st.scale_inv) == st_ref.scale_inv[0]
+        q = lpq.quantize(z, fmt, BOTH, scaling=lpq.SCALING_DELAYED, state=st)
+        eq(codes(q.row), o.fp8_pertensor(bits, of, scale=float(st_ref.scale[0]))["row"])
+    for flags, ref_flags in [(BOTH, o.NV_ROW | o.NV_COL),
+                             (BOTH | lpq.RHT_COLWISE | lpq.STOCHASTIC, o.NV_ROW | o.NV_COL | o.NV_RHT | o.NV_SR)]:
+        q = lpq.quantize(z, lpq.NVFP4, flags, seed=3, rht_seed=7)
+        ref = o.nvfp4(bits, ref_flags, seed=3, rht_seed=7)
+        for name in ("row", "col"):
+            eq(codes(getattr(q, name)), ref[name])
+            eq(plain_scales(getattr(q, name)), ref[name + "_sf"])
+            assert scalar(getattr(q, name).tensor_scale) == np.float32(ref[name + "_ts"])
+    q = lpq.quantize(z, lpq.NVFP4_2D, BOTH)
+    ref = o.nvfp4(bits, o.NV_ROW | o.NV_COL | o.NV_2D)
+    for name in ("row", "col"):
+        eq(codes(getattr(q, name)), ref[name])
+        eq(plain_scales(getattr(q, name)), ref[name + "_sf"])
+    for fmt, br in ((lpq.FP8_BLOCK_1x128, 1), (lpq.FP8_BLOCK_128x128, 128)):
+        zz = torch.zeros((128, 256), dtype=torch.bfloat16, device="cuda")
+        zz[1, 5], zz[100, 200] = 2.0 ** -123, 2.0 ** -133
+        b2 = synth.host_bits(zz)
+        q = lpq.quantize(zz, fmt, BOTH, sf_layout=lpq.SF_PLAIN)
+        ref = o.fp8_block(b2, br)
+        eq(codes(q.row), ref["row"])
+        eq(plain_scales(q.row), ref["row_sinv"])
+        eq(codes(q.col), ref["col"])
+
+
+def test_mx_amax_outputs_for_either_view():
+    """The MX formats' optional amax: written for whichever view asks (row,
+    column or both), each starting from zero rather than a stale value."""
+    x, bits = bf16_input((64, 128), std=2.0, seed=23)
+    want = np.float32(o.amax(bits))
+    for flags in (lpq.ROWWISE, lpq.COLWISE, BOTH):
+        q = lpq.alloc(lpq.MXFP8, 64, 128, flags)
+        for c in (q.row, q.col):
+            if c is not None:
+                c.amax = torch.full((1,), 1e30, dtype=torch.float32, device="cuda")  # stale
+        lpq.quantize(x, lpq.MXFP8, flags, out=q)
+        for c in (q.row, q.col):
+            if c is not None:
+                assert scalar(c.amax) == want
+
+
+def test_delayed_position_outside_the_ring_wraps():
+    """A restored state whose pos is outside [0, len) writes slot pos mod len
+    (as the oracle does) and never outside the history."""
+    st, ref = lpq.DelayedState(16), o.DelayedState(16)
+    st.pos.fill_(37)
+    ref.pos[0] = 37
+    a = torch.tensor([3.0], device="cuda")
+    lpq.scale_update(st, a, 448.0)
+    ref.update(3.0, 448.0)
+    eq(st.hist.cpu().numpy(), ref.hist)
+    assert int(st.pos.item()) == int(ref.pos[0]) == 6
+
+
 def test_empty_input():
     x = torch.empty((0, 128), dtype=torch.bfloat16, device="cuda")
     q = lpq.quantize(x, lpq.NVFP4, lpq.ROWWISE)

@@ -306,3 +306,100 @@ def test_fp8_block_scales_and_error(block_rows):
     else:
         t = o.fp8_block(np.ascontiguousarray(x.T), 1, colwise=False)
         assert np.array_equal(r["col"], t["row"]) and np.array_equal(r["col_sinv"], t["row_sinv"])
+
+
+# ------------------------------------------------------------------ tiny amax: scale quotients clamped
+FLT_MAX = np.float32(3.4028234663852886e38)
+
+
+def _torch_fp8_code(y, fmt):
+    """RNE float8 code of float32 values by torch's own conversion (in range only)."""
+    import torch
+    dt = torch.float8_e4m3fn if fmt == o.E4M3 else torch.float8_e5m2
+    return torch.tensor(np.asarray(y, np.float32)).to(dt).view(torch.uint8).numpy()
+
+
+def _nearest_e2m1(y):
+    """E2M1 code of |y| < 6 by exhaustive nearest search (no ties in the values used)."""
+    grid = np.array([0, 0.5, 1, 1.5, 2, 3, 4, 6], np.float64)
+    return int(np.argmin(np.abs(grid - abs(float(y)))))
+
+
+@pytest.mark.parametrize("fmt", [o.E4M3, o.E5M2])
+def test_tiny_amax_fp8_scale_clamped_to_largest_float(fmt):
+    """An amax below fmax / FLT_MAX (bf16 holds it: 2^-123 ~ 9.4e-38) makes
+    fmax / amax overflow; the scale is then the largest finite float (the
+    reading for a case the pages leave open).  Worked with numpy float32
+    arithmetic and torch's float8 conversion: zeros stay +0 instead of becoming
+    NaN codes, the tiny value encodes as RNE(t * FLT_MAX), scale_inv is the
+    float32 1 / FLT_MAX rather than 0."""
+    t = np.float32(2.0 ** -123)
+    x = np.zeros((4, 32), np.float32)
+    x[1, 5], x[2, 7] = t, -t
+    bits = bf16_bits(x)
+    with np.errstate(over="ignore"):
+        assert np.isinf(np.float32(o.FMAX[fmt]) / t)  # the unclamped quotient overflows
+    r = o.fp8_pertensor(bits, fmt)
+    assert r["amax"] == t and r["scale"] == FLT_MAX
+    assert r["scale_inv"] == np.float32(1) / FLT_MAX and r["scale_inv"] > 0
+    want = _torch_fp8_code(x * FLT_MAX, fmt)
+    assert np.array_equal(r["row"], want) and np.array_equal(r["col"], want.T)
+    assert (r["row"] == 0).sum() == x.size - 2  # every zero encodes as +0
+    # delayed scaling: a history whose max is t gives the same clamped scale
+    st = o.DelayedState(16)
+    st.update(t, o.FMAX[fmt])
+    assert st.scale[0] == FLT_MAX and st.scale_inv[0] == np.float32(1) / FLT_MAX
+    assert np.array_equal(o.fp8_pertensor(bits, fmt, scale=float(st.scale[0]))["row"], want)
+
+
+def test_tiny_amax_nvfp4_encode_and_block_factors_clamped():
+    """NVFP4 with A = 2^-123: s_enc = 2688 / A overflows and is clamped to
+    FLT_MAX; a block whose max is the smallest bf16 subnormal 2^-133 gets a
+    subnormal E4M3 scale S, whose factor s_enc / dec(S) overflows too and is
+    clamped.  Zeros stay 0 in both blocks (an infinite factor would make them
+    NaN, encoded as +6)."""
+    t, u = np.float32(2.0 ** -123), np.float32(2.0 ** -133)
+    x = np.zeros((1, 32), np.float32)
+    x[0, 0], x[0, 16] = t, u
+    r = o.nvfp4(bf16_bits(x), o.NV_ROW)
+    assert r["row_amax"] == t and r["row_ts"] == t / np.float32(2688)
+    s_enc = FLT_MAX  # 2688 / t overflows
+    want_sf, want_codes = [], []
+    for v in (t, u):
+        d = (v / np.float32(6)) * s_enc
+        S = int(_torch_fp8_code([d], o.E4M3)[0])
+        dec = np.float32(o.decode(o.E4M3, [S])[0])
+        with np.errstate(over="ignore"):
+            f = np.float32(s_enc / dec)
+        f = min(f, FLT_MAX)
+        want_sf.append(S)
+        want_codes.append(_nearest_e2m1(v * f))
+    assert want_sf[1] < 8  # the second block's scale is an E4M3 subnormal
+    assert list(r["row_sf"][0]) == want_sf
+    codes = [(r["row"][0, j // 2] >> (4 * (j % 2))) & 0xF for j in range(32)]
+    assert codes[0] == want_codes[0] == 7 and codes[16] == want_codes[1] == 0
+    assert all(c == 0 for j, c in enumerate(codes) if j not in (0, 16))
+
+
+def test_tiny_amax_subchannel_scale_clamped():
+    """1x128 block whose max is 2^-123: 448 / m overflows, the block scale is
+    FLT_MAX and its FP32 factor 1 / FLT_MAX; zeros encode as +0."""
+    t = np.float32(2.0 ** -123)
+    x = np.zeros((2, 128), np.float32)
+    x[0, 3] = t
+    r = o.fp8_block(bf16_bits(x), 1, colwise=False)
+    assert r["row_sinv"][0, 0] == np.float32(1) / FLT_MAX
+    assert np.array_equal(r["row"][0], _torch_fp8_code(x[0] * FLT_MAX, o.E4M3))
+    assert r["row_sinv"][1, 0] == 1.0 and not r["row"][1].any()  # all-zero block: scale 1
+
+
+def test_delayed_position_outside_ring_is_taken_modulo_len():
+    """A state restored with pos outside [0, len) writes slot pos mod len."""
+    st = o.DelayedState(16)
+    st.pos[0] = 37
+    st.update(2.0, 448.0)
+    assert st.hist[5] == 2.0 and int(st.pos[0]) == 6 and st.hist.sum() == 2.0
+    st.pos[0] = -1
+    st.update(4.0, 448.0)
+    assert st.hist[15] == 4.0 and int(st.pos[0]) == 0
+    assert st.scale[0] == np.float32(448.0) / np.float32(4.0)
