@@ -193,6 +193,23 @@ lpq_status lpq_quantize(const void *x, int64_t rows, int64_t cols, int32_t fmt, 
                         uint32_t flags, uint64_t seed, uint64_t counter_offset, uint32_t rht_seed,
                         const lpq_delayed_state *state, lpq_qtensor *out, lpq_stream_t stream);
 
+/* The global amax pass ([TE] "interpreting real-model results": the extra
+ * memory pass for the per-tensor amax; [FP8] per-tensor scaling from the
+ * tensor's amax): *amax = max |x| over x [rows, cols] bf16 (NaN ignored,
+ * infinities counted), overwritten (not accumulated).  With LPQ_RHT_COLWISE
+ * in flags, *rht_amax gets max |RHT16(v)| over the column-wise copy (each
+ * column's 16-runs of rows transformed with the signs of rht_seed, as in
+ * lpq_quantize), the amax an NVFP4 RHT column copy is scaled with; rows must
+ * then be a multiple of 16.  amax and rht_amax are device FP32 pointers;
+ * either may be NULL, not both (rht_amax is ignored without the flag).  cols
+ * must be a multiple of 16 and x 16-byte aligned; an empty x gives 0.  This is
+ * the pass lpq_quantize runs before current-scaled FP8 and NVFP4 copies: a
+ * token-sharded caller runs it on its own shard, combines the shards' values
+ * with a MAX all-reduce and quantizes with LPQ_GIVEN_AMAX.  flags other than
+ * LPQ_RHT_COLWISE give LPQ_ERR_INVALID_ARG. */
+lpq_status lpq_amax(const void *x, int64_t rows, int64_t cols, uint32_t flags, uint32_t rht_seed, float *amax,
+                    float *rht_amax, lpq_stream_t stream);
+
 /* Delayed-scaling update (one CTA): history[pos] = *amax; pos = (pos+1) % len;
  * m = max(history); scale = fmax / m if m > 0 and finite (else unchanged),
  * clamped to the largest finite float if the quotient overflows;
@@ -288,6 +305,28 @@ lpq_status lpq_device_status(lpq_stream_t stream, int32_t *code);
  * returns; the CUDA context stays usable.  No fault, trap or hang is involved. */
 lpq_status lpq_selftest_wait(uint64_t limit_ns, lpq_stream_t stream);
 
+/* Arithmetic self-check of the quantizers' device helpers against their
+ * definitions, for the test suite.  Counts mismatches over indices i in
+ * [begin, begin + count):
+ *   which 0: x = the float with bits i (i <= 0x7F800000: every non-negative
+ *            float and +inf): the block-max division by 6 (a product with
+ *            RN(1/6) corrected by one fused multiply-add of the exact
+ *            residual) against the IEEE quotient x / 6;
+ *   which 1: |y| = the float with bits i >> 3 and the (i & 7)-th of eight
+ *            probe words r (r >> 8 = 0, 1, 2^23 - 2, 2^23, 2^24 - 3,
+ *            2^24 - 2, 2^24 - 1, 2^24 - 1, low bytes 0x00 or 0xFF): the
+ *            stochastic E2M1 rounding of y and -y against the definition
+ *            (round up to the next grid magnitude iff float(r >> 8) <
+ *            frac * 2^24; 6 at and beyond 6 and for NaN);
+ *   which 2: y = the float with bits `param` and r = i << 8 | (i * 37 mod
+ *            256), i < 2^24 (every threshold value for one y), y and -y.
+ * result (device, two int64, 8-byte aligned) receives the mismatch count and
+ * the smallest mismatching index (-1 if none); the call returns at once, read
+ * result after synchronising `stream`.  Ranges beyond the mode's index limit
+ * give LPQ_ERR_INVALID_ARG. */
+lpq_status lpq_selftest_arith(int32_t which, uint64_t begin, uint64_t count, uint32_t param, int64_t *result,
+                              lpq_stream_t stream);
+
 /* Tensor-core rate measurement (the dense peaks the roofline divides by):
  * one CTA per SM issues `iters` k-steps of four 128 x 256 tcgen05.mma on
  * zero operands resident in shared memory; kind 0 = kind::f16 (bf16, K 16),
@@ -302,8 +341,10 @@ lpq_status lpq_selftest_wait(uint64_t limit_ns, lpq_stream_t stream);
  * CTAs, each pair issuing four 256 x 256 MMAs per k-step, each SM holding
  * 128 rows of A and of B, the shape of the product GEMM; any kind), 7 = CTA
  * pairs with the scale columns rewritten by four warps per CTA with
- * tcgen05.st while the MMAs run (kinds 2, 3).  Other values give
- * LPQ_ERR_INVALID_ARG.  Modes 6 and 7 launch SMs rounded down to even CTAs.
+ * tcgen05.st while the MMAs run (kinds 2, 3), 8 = CTA pairs issuing each
+ * k-step as eight 256 x 128 MMAs (two column halves into two TMEM regions;
+ * any kind).  Other values give LPQ_ERR_INVALID_ARG.  Modes 6 to 8 launch SMs
+ * rounded down to even CTAs.
  * FLOPs = CTAs * iters * 4 * 2 * 128 * 256 * K;
  * the caller times the launch with events on `stream`. */
 lpq_status lpq_mma_peak(int32_t kind, int32_t iters, int32_t with_scale_copies, lpq_stream_t stream);

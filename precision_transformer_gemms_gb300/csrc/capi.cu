@@ -221,6 +221,24 @@ lpq_status lpq_quantize(const void* x, int64_t rows, int64_t cols, int32_t fmt, 
                          reinterpret_cast<cudaStream_t>(stream));
 }
 
+lpq_status lpq_amax(const void* x, int64_t rows, int64_t cols, uint32_t flags, uint32_t rht_seed, float* amax,
+                    float* rht_amax, lpq_stream_t stream) {
+  if (flags & ~uint32_t(LPQ_RHT_COLWISE)) return set_error(LPQ_ERR_INVALID_ARG, "lpq_amax flags 0x%x", flags);
+  const bool rht = flags & LPQ_RHT_COLWISE;
+  if (!amax && !(rht && rht_amax)) return set_error(LPQ_ERR_INVALID_ARG, "no amax output");
+  if (rht && !rht_amax) return set_error(LPQ_ERR_INVALID_ARG, "LPQ_RHT_COLWISE needs rht_amax");
+  if (rows < 0 || cols < 0) return set_error(LPQ_ERR_SHAPE, "negative dimension");
+  if (cols % 16) return set_error(LPQ_ERR_SHAPE, "cols %lld not a multiple of 16", (long long)cols);
+  if (rht && rows % 16) return set_error(LPQ_ERR_SHAPE, "the RHT amax needs rows %% 16 == 0 (rows = %lld)", (long long)rows);
+  if (rows * cols > 0 && !x) return set_error(LPQ_ERR_INVALID_ARG, "x is NULL");
+  if (!aligned16(x)) return set_error(LPQ_ERR_ALIGN, "x not 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(amax) & 3u) || (reinterpret_cast<uintptr_t>(rht_amax) & 3u))
+    return set_error(LPQ_ERR_ALIGN, "amax outputs not 4-byte aligned");
+  lpq_status st = check_arch();
+  if (st != LPQ_OK) return st;
+  return launch_amax(x, rows, cols, rht, rht_seed, amax, rht_amax, reinterpret_cast<cudaStream_t>(stream));
+}
+
 lpq_status lpq_scale_update(const lpq_delayed_state* state, const float* amax, float fmax, lpq_stream_t stream) {
   if (!state || !amax || !state->scale || !state->scale_inv || !state->amax_history || !state->pos)
     return set_error(LPQ_ERR_INVALID_ARG, "NULL state or amax");
@@ -330,11 +348,24 @@ lpq_status lpq_selftest_wait(uint64_t limit_ns, lpq_stream_t stream) {
   return launch_selftest_wait(limit_ns, reinterpret_cast<cudaStream_t>(stream));
 }
 
+lpq_status lpq_selftest_arith(int32_t which, uint64_t begin, uint64_t count, uint32_t param, int64_t* result,
+                              lpq_stream_t stream) {
+  if (which < 0 || which > 2) return set_error(LPQ_ERR_INVALID_ARG, "which %d", which);
+  if (!result || (reinterpret_cast<uintptr_t>(result) & 7u)) return set_error(LPQ_ERR_INVALID_ARG, "result");
+  const uint64_t limit = which == 0 ? 0x7F800001ull : which == 1 ? 8ull * 0x100000000ull : 1ull << 24;
+  if (begin > limit || count > limit - begin) return set_error(LPQ_ERR_INVALID_ARG, "index range beyond %llu",
+                                                               (unsigned long long)limit);
+  lpq_status st = check_arch();
+  if (st != LPQ_OK) return st;
+  return launch_selftest_arith(which, begin, count, param, result, reinterpret_cast<cudaStream_t>(stream));
+}
+
 lpq_status lpq_mma_peak(int32_t kind, int32_t iters, int32_t with_scale_copies, lpq_stream_t stream) {
   if (kind < 0 || kind > 3) return set_error(LPQ_ERR_INVALID_ARG, "kind %d", kind);
   if (iters < 1 || iters > (1 << 24)) return set_error(LPQ_ERR_INVALID_ARG, "iters %d", iters);
   const bool ok_mode = (with_scale_copies >= 0 && with_scale_copies <= 1) ||
                        (with_scale_copies >= 2 && with_scale_copies <= 5 && kind == 3) || with_scale_copies == 6 ||
+                       with_scale_copies == 8 ||
                        (with_scale_copies == 7 && (kind == 2 || kind == 3));
   if (!ok_mode) return set_error(LPQ_ERR_INVALID_ARG, "with_scale_copies %d for kind %d", with_scale_copies, kind);
   lpq_status st = check_arch();

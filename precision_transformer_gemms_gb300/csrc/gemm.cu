@@ -899,7 +899,7 @@ lpq_status run_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensor
 // sub-channel scaling: 1x128 activation and 128x128 weight blocks with FP32
 // factors).  Every 128-deep K slice is one pipeline stage: the MMA warp
 // computes the slice's partial product sum_{k in slice} qa * qb with
-// kind::f8f6f4 into one of two TMEM buffers; the epilogue warps read it and
+// kind::f8f6f4 into one of four TMEM buffers; the epilogue warps read it and
 // accumulate partial * sa[m, slice] * sb[n, slice] in FP32 registers (the
 // tensor cores have no FP32 block scales), while the next slice runs.
 struct BlockArgs {
@@ -1445,6 +1445,9 @@ __global__ void __launch_bounds__(256, 1) mma_peak_kernel(int iters, uint32_t id
 // (unsynchronised; a rate probe).
 template <int KIND, int MODE>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1) mma_peak_pair_kernel(int iters, uint32_t idesc) {
+  // MODE 8: each k-step's four 256 x 256 MMAs issued as eight 256 x 128 MMAs
+  // (two column halves, each half's B rows 64 per CTA) into two TMEM regions.
+  constexpr bool kHalves = MODE == 8;
   using PC = PairCfg<KIND, true, false>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -1494,13 +1497,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1) mma_peak_pai
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const uint64_t ad = ((uint64_t)kHiSw << 32) | (alo + 2 * j);
-          const uint64_t bd = ((uint64_t)kHiSw << 32) | (blo + 2 * j);
           const uint32_t acc = (it > 0 || j > 0) ? 1u : 0u;
-          if constexpr (KIND == kKindF16 || KIND == kKindF8F6F4) {
-            mma_pair<KIND>(tbase, ad, bd, idesc, acc);
-          } else {
-            const int at = j * PC::kSfAtoms / 4;
-            mma_pair_bs<KIND>(tbase, ad, bd, idesc | sf_select<KIND>(j), tsfa + 4 * at, tsfb + 8 * at, acc);
+#pragma unroll
+          for (int h = 0; h < (kHalves ? 2 : 1); ++h) {
+            // half h: this CTA's B rows 64 h .. 64 h + 63 (8 KB into the swizzled tile)
+            const uint64_t bd = ((uint64_t)kHiSw << 32) | (blo + 2 * j + (kHalves ? h * (8192 >> 4) : 0));
+            const uint32_t d = tbase + (kHalves ? h * 128 : 0);
+            if constexpr (KIND == kKindF16 || KIND == kKindF8F6F4) {
+              mma_pair<KIND>(d, ad, bd, idesc, acc);
+            } else {
+              const int at = j * PC::kSfAtoms / 4;
+              mma_pair_bs<KIND>(d, ad, bd, idesc | sf_select<KIND>(j), tsfa + 4 * at, tsfb + 8 * at + (kHalves ? 4 * h : 0),
+                                acc);
+            }
           }
         }
       }
@@ -1523,7 +1532,9 @@ lpq_status run_peak_pair(int iters, uint32_t idesc, cudaStream_t s) {
   lpq_status st = set_smem_attr(reinterpret_cast<const void*>(mma_peak_pair_kernel<KIND, MODE>), smem);
   if (st != LPQ_OK) return st;
   const int sms = device_sms();
-  mma_peak_pair_kernel<KIND, MODE><<<sms & ~1, 256, smem, s>>>(iters, (idesc & ~(31u << 24)) | (16u << 24));
+  uint32_t id = (idesc & ~(31u << 24)) | (16u << 24);                   // M = 256
+  if (MODE == 8) id = (id & ~(63u << 17)) | ((uint32_t)(128 >> 3) << 17);  // N = 128
+  mma_peak_pair_kernel<KIND, MODE><<<sms & ~1, 256, smem, s>>>(iters, id);
   return cuda_check(cudaGetLastError(), "pair peak kernel launch");
 }
 
@@ -1546,6 +1557,15 @@ lpq_status launch_mma_peak(int32_t kind, int32_t iters, int32_t with_sf, cudaStr
       case kKindF8F6F4: return run_peak_pair<kKindF8F6F4, 6>(iters, idesc_dense(0, 0, 256), s);
       case kKindMXF8: return run_peak_pair<kKindMXF8, 6>(iters, mx, s);
       case kKindNVF4: return run_peak_pair<kKindNVF4, 6>(iters, nv, s);
+    }
+    return set_error(LPQ_ERR_INVALID_ARG, "kind %d", kind);
+  }
+  if (with_sf == 8) {  // CTA pairs, 256 x 128 MMAs (two column halves per k-step)
+    switch (kind) {
+      case kKindF16: return run_peak_pair<kKindF16, 8>(iters, idesc_dense(1, 1, 256), s);
+      case kKindF8F6F4: return run_peak_pair<kKindF8F6F4, 8>(iters, idesc_dense(0, 0, 256), s);
+      case kKindMXF8: return run_peak_pair<kKindMXF8, 8>(iters, mx, s);
+      case kKindNVF4: return run_peak_pair<kKindNVF4, 8>(iters, nv, s);
     }
     return set_error(LPQ_ERR_INVALID_ARG, "kind %d", kind);
   }

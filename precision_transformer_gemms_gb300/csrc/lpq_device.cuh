@@ -95,11 +95,15 @@ __device__ __forceinline__ int mx_exponent(float a) { return mx_exponent_t<8, 0x
 __device__ __forceinline__ int mx_exponent_e5m2(float a) { return mx_exponent_t<15, 0x600000u>(a); }  // E5M2
 __device__ __forceinline__ int mx_exponent_e2m1(float a) { return mx_exponent_t<2, 0x400000u>(a); }   // E2M1
 
-// Correctly rounded x / 6 for x >= 0 (a block max): the product with
-// RN(1/6), corrected once with the exact residual x - 6 q (an FMA).  Below
-// 2^-120, where the quotient can be subnormal and the correction is not
-// exact, and for infinity, the IEEE division itself.  Equal to the IEEE
-// quotient for every non-negative float (checked exhaustively on the device).
+// Correctly rounded x / 6 for x >= 0 (a block max) by division by a constant
+// with one fused-multiply-add correction (P. Markstein, "IA-64 and Elementary
+// Functions", 2000; N. Brisebarre and J.-M. Muller, "Correctly rounded
+// multiplication by arbitrary precision constants", IEEE TC 2008): q = the
+// product with RN(1/6), then q + RN(1/6) * (x - 6 q) with the exact residual
+// x - 6 q from an FMA.  Below 2^-120, where the quotient can be subnormal and
+// the correction is not exact, and for infinity, the IEEE division itself.
+// Equal to the IEEE quotient for every non-negative float: the test suite
+// checks all 2^31 of them on the device (lpq_selftest_arith, which 0).
 __device__ __forceinline__ float div6_rn(float x) {
   if (!(x >= 7.52316385e-37f && x < __int_as_float(0x7F800000))) return __fdiv_rn(x, 6.0f);  // 2^-120
   const float q = __fmul_rn(x, 0.16666667f);

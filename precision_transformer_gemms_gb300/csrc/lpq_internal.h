@@ -40,6 +40,10 @@ inline int64_t sf_row_groups(int64_t rows) { return (rows + 127) / 128; }
 lpq_status launch_quantize(const void* x, int64_t rows, int64_t cols, int32_t fmt, int32_t scaling,
                            uint32_t flags, uint64_t seed, uint64_t counter_offset, uint32_t rht_seed,
                            const lpq_delayed_state* state, lpq_qtensor* out, cudaStream_t stream);
+lpq_status launch_amax(const void* x, int64_t rows, int64_t cols, bool rht, uint32_t rht_seed, float* amax,
+                       float* rht_amax, cudaStream_t stream);
+lpq_status launch_selftest_arith(int32_t which, uint64_t begin, uint64_t count, uint32_t param, int64_t* out,
+                                 cudaStream_t stream);
 lpq_status launch_scale_update(const lpq_delayed_state* state, const float* amax, float fmax,
                                cudaStream_t stream);
 

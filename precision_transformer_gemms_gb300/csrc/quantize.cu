@@ -970,6 +970,97 @@ lpq_status launch_quantize(const void* xv, int64_t R, int64_t C, int32_t fmt, in
   return set_error(LPQ_ERR_UNSUPPORTED, "format %d", fmt);
 }
 
+// ---------------------------------------------------------------- arithmetic self-checks
+// Device helpers of the quantizers against their definitions, for the test
+// suite (lpq_selftest_arith).  out[0] counts mismatches, out[1] keeps the
+// smallest mismatching index.
+namespace {
+
+__global__ void selftest_init_kernel(unsigned long long* out) {
+  out[0] = 0ull;
+  out[1] = ~0ull;
+}
+
+// Stochastic E2M1 rounding stated directly: adjacent grid magnitudes
+// lo <= |y| < hi, frac = (|y| - lo) / (hi - lo) in double (exact: the spacing
+// is a power of two), round up iff float(r >> 8) < frac * 2^24; |y| >= 6 and
+// NaN give 6; the sign of y is kept.
+__device__ float sr_e2m1_definition(float y, uint32_t r) {
+  if (y != y) return 6.0f;
+  const float a = fabsf(y);
+  float v;
+  if (a >= 6.0f) {
+    v = 6.0f;
+  } else {
+    const float g[8] = {0.f, 0.5f, 1.f, 1.5f, 2.f, 3.f, 4.f, 6.f};
+    int j = 0;
+    while (j < 6 && g[j + 1] <= a) ++j;
+    const double lo = g[j], hi = g[j + 1];
+    const double thr = ((double)a - lo) / (hi - lo) * 16777216.0;
+    v = (double)(r >> 8) < thr ? (float)hi : (float)lo;
+  }
+  return copysignf(v, y);
+}
+
+__device__ __forceinline__ void selftest_record(unsigned long long* out, uint64_t i) {
+  atomicAdd(&out[0], 1ull);
+  atomicMin(&out[1], (unsigned long long)i);
+}
+
+// which 0: x = the float with bits i (i <= 0x7F800000: every non-negative
+//   float and +inf): div6_rn(x) against the IEEE quotient x / 6.
+// which 1: |y| = the float with bits i >> 3, r = the (i & 7)-th probe word
+//   (r >> 8 = 0, 1, 2^23 - 2, 2^23, 2^24 - 3, 2^24 - 2, 2^24 - 1, low bytes
+//   0x00 or 0xFF); y and -y as one pair through sr_e2m1_value2.
+// which 2: y = the float with bits `param`, r = i << 8 | (low byte i * 37),
+//   i < 2^24: every threshold word for one y, pairs (y, -y).
+__global__ void selftest_arith_kernel(int which, uint64_t begin, uint64_t count, uint32_t param,
+                                      unsigned long long* out) {
+  const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
+  for (uint64_t k = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; k < count; k += stride) {
+    const uint64_t i = begin + k;
+    if (which == 0) {
+      const float x = __uint_as_float((uint32_t)i);
+      if (__float_as_uint(div6_rn(x)) != __float_as_uint(__fdiv_rn(x, 6.0f))) selftest_record(out, i);
+    } else {
+      float y;
+      uint32_t r;
+      if (which == 1) {
+        y = __uint_as_float((uint32_t)(i >> 3));
+        const uint32_t probes[8] = {0x00000000u, 0x000001FFu, 0x7FFFFE00u, 0x800000FFu,
+                                    0xFFFFFD00u, 0xFFFFFEFFu, 0xFFFFFF00u, 0xFFFFFFFFu};
+        r = probes[i & 7];
+      } else {
+        y = __uint_as_float(param);
+        r = ((uint32_t)i << 8) | ((uint32_t)(i * 37u) & 0xFFu);
+      }
+      const float2 got = sr_e2m1_value2(make_float2(y, -y), r, r);
+      if (__float_as_uint(got.x) != __float_as_uint(sr_e2m1_definition(y, r)) ||
+          __float_as_uint(got.y) != __float_as_uint(sr_e2m1_definition(-y, r)))
+        selftest_record(out, i);
+    }
+  }
+}
+
+}  // namespace
+
+lpq_status launch_selftest_arith(int32_t which, uint64_t begin, uint64_t count, uint32_t param, int64_t* out,
+                                 cudaStream_t s) {
+  auto* o = reinterpret_cast<unsigned long long*>(out);
+  selftest_init_kernel<<<1, 1, 0, s>>>(o);
+  selftest_arith_kernel<<<device_sms() * 8, 256, 0, s>>>(which, begin, count, param, o);
+  return cuda_check(cudaGetLastError(), "arithmetic self-check launch");
+}
+
+lpq_status launch_amax(const void* x, int64_t R, int64_t C, bool rht, uint32_t rht_seed, float* amax, float* rht_amax,
+                       cudaStream_t s) {
+  float* rh = rht ? rht_amax : nullptr;
+  lpq_status st;
+  if ((st = zero_f32(amax, s)) != LPQ_OK || (st = zero_f32(rh, s)) != LPQ_OK) return st;
+  if (R == 0 || C == 0) return LPQ_OK;
+  return run_amax(static_cast<const uint16_t*>(x), R, C, amax, nullptr, rh, rht_seed, s);
+}
+
 lpq_status launch_scale_update(const lpq_delayed_state* st, const float* amax, float fmax, cudaStream_t s) {
   scale_update_kernel<<<1, 128, 0, s>>>(st->amax_history, st->pos, st->scale, st->scale_inv, st->len, amax, fmax);
   return cuda_check(cudaGetLastError(), "scale update launch");

@@ -97,6 +97,7 @@ def lib():
         L.lpq_quantize.argtypes = [P, I64, I64, I32, I32, U32, U64, U64, U32, ctypes.POINTER(DelayedStateC),
                                    ctypes.POINTER(QTensorC), P]
         L.lpq_scale_update.argtypes = [ctypes.POINTER(DelayedStateC), P, F, P]
+        L.lpq_amax.argtypes = [P, I64, I64, U32, U32, P, P, P]
         L.lpq_gemm.argtypes = [I32, ctypes.POINTER(QView), ctypes.POINTER(QView), P, I32, I64, I64, I64, P]
         L.lpq_gemm_ex.argtypes = [I32, ctypes.POINTER(QView), ctypes.POINTER(QView), P, I32, I64, I64, I64,
                                   ctypes.POINTER(GemmOpts), P]
@@ -106,9 +107,10 @@ def lib():
         L.lpq_device_status.argtypes = [P, ctypes.POINTER(I32)]
         L.lpq_selftest_wait.argtypes = [U64, P]
         L.lpq_mma_peak.argtypes = [I32, I32, I32, P]
+        L.lpq_selftest_arith.argtypes = [I32, U64, U64, U32, P, P]
         L.lpq_version.restype = I32
-        for name in ("lpq_copy_bytes", "lpq_quantize", "lpq_scale_update", "lpq_gemm", "lpq_gemm_ex", "lpq_layer_shapes",
-                     "lpq_device_status", "lpq_selftest_wait", "lpq_mma_peak"):
+        for name in ("lpq_copy_bytes", "lpq_quantize", "lpq_scale_update", "lpq_gemm", "lpq_gemm_ex", "lpq_amax", "lpq_layer_shapes",
+                     "lpq_device_status", "lpq_selftest_wait", "lpq_mma_peak", "lpq_selftest_arith"):
             getattr(L, name).restype = I32
         _lib = L
     return _lib
@@ -232,6 +234,20 @@ def quantize(x, fmt, flags, scaling=SCALING_CURRENT, seed=0, counter_offset=0, r
     return out
 
 
+def amax(x, rht=False, rht_seed=0, out=None, rht_out=None, stream=None):
+    """lpq_amax on a bf16 CUDA tensor x [rows, cols]: max |x| into `out` (and,
+    with rht, the column-wise RHT amax into `rht_out`); returns (out, rht_out)
+    as 1-element FP32 device tensors."""
+    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.is_contiguous()
+    if out is None:
+        out = torch.empty(1, dtype=torch.float32, device=x.device)
+    if rht and rht_out is None:
+        rht_out = torch.empty(1, dtype=torch.float32, device=x.device)
+    _check(lib().lpq_amax(_ptr(x), x.shape[0], x.shape[1], RHT_COLWISE if rht else 0, rht_seed, _ptr(out),
+                          _ptr(rht_out) if rht else None, _stream(stream)))
+    return out, (rht_out if rht else None)
+
+
 def scale_update(state, amax, fmax, stream=None):
     _check(lib().lpq_scale_update(ctypes.byref(state.c()), _ptr(amax), float(fmax), _stream(stream)))
 
@@ -264,13 +280,22 @@ def selftest_wait(limit_ns, stream=None):
     _check(lib().lpq_selftest_wait(int(limit_ns), _stream(stream)))
 
 
+def selftest_arith(which, begin, count, param=0, stream=None):
+    """lpq_selftest_arith: (mismatches, first mismatching index or -1)."""
+    out = torch.empty(2, dtype=torch.int64, device="cuda")
+    _check(lib().lpq_selftest_arith(which, begin, count, param, _ptr(out), _stream(stream)))
+    torch.cuda.synchronize()
+    n, first = out.tolist()
+    return n, (-1 if n == 0 else first)
+
+
 MMA_KINDS = {"bf16": 0, "fp8": 1, "mxfp8": 2, "nvfp4": 3}
 MMA_K = {0: 16, 1: 32, 2: 32, 3: 64}
 
 
 def mma_peak(kind, iters=20000, with_scale_copies=True, stream=None):
-    """Dense tcgen05 rate in TFLOP/s for `kind` (see lpq_mma_peak; modes 6 and
-    7 run on CTA pairs)."""
+    """Dense tcgen05 rate in TFLOP/s for `kind` (see lpq_mma_peak; modes 6 to
+    8 run on CTA pairs)."""
     k = MMA_KINDS[kind] if isinstance(kind, str) else kind
     mode = int(with_scale_copies)
     st = stream if stream is not None else torch.cuda.current_stream()

@@ -132,12 +132,36 @@ def test_scale_update_and_selftest_validation():
     assert L.lpq_selftest_wait(5_000_000_000, None) == lpq.ERR_INVALID_ARG
 
 
+def test_amax_validation():
+    """lpq_amax checks flags, outputs, shapes and alignment before any device call."""
+    L = lpq.lib()
+    f = 16  # a 16-byte aligned fake device address: validation stops before the device check
+    assert L.lpq_amax(f, 4, 32, 8, 0, f, None, None) == lpq.ERR_INVALID_ARG      # unknown flag
+    assert L.lpq_amax(f, 4, 32, 0, 0, None, None, None) == lpq.ERR_INVALID_ARG   # no output
+    assert L.lpq_amax(f, 4, 32, lpq.RHT_COLWISE, 0, f, None, None) == lpq.ERR_INVALID_ARG  # RHT without output
+    assert L.lpq_amax(f, 4, 24, 0, 0, f, None, None) == lpq.ERR_SHAPE            # cols % 16
+    assert L.lpq_amax(f, 8, 32, lpq.RHT_COLWISE, 0, f, f, None) == lpq.ERR_SHAPE  # rows % 16 for the RHT amax
+    assert L.lpq_amax(8, 4, 32, 0, 0, f, None, None) == lpq.ERR_ALIGN           # x not 16-byte aligned
+    assert L.lpq_amax(None, 4, 32, 0, 0, f, None, None) == lpq.ERR_INVALID_ARG
+    ok = L.lpq_amax(f, 16, 32, lpq.RHT_COLWISE, 0, f, f, None)
+    assert ok not in (lpq.ERR_INVALID_ARG, lpq.ERR_SHAPE, lpq.ERR_ALIGN)
+
+
+def test_selftest_arith_validation():
+    L = lpq.lib()
+    assert L.lpq_selftest_arith(3, 0, 1, 0, 16, None) == lpq.ERR_INVALID_ARG        # no such check
+    assert L.lpq_selftest_arith(0, 0, 0x7F800002, 0, 16, None) == lpq.ERR_INVALID_ARG  # past +inf
+    assert L.lpq_selftest_arith(2, 1, 1 << 24, 0, 16, None) == lpq.ERR_INVALID_ARG  # past 2^24 words
+    assert L.lpq_selftest_arith(0, 0, 1, 0, None, None) == lpq.ERR_INVALID_ARG
+    assert L.lpq_selftest_arith(0, 0, 1, 0, 12, None) == lpq.ERR_INVALID_ARG        # result not 8-byte aligned
+
+
 def test_mma_peak_validation():
     """Rate-probe arguments are checked before any device call."""
     L = lpq.lib()
     assert L.lpq_mma_peak(4, 10, 0, None) == lpq.ERR_INVALID_ARG     # no such kind
     assert L.lpq_mma_peak(3, 0, 0, None) == lpq.ERR_INVALID_ARG      # iters
-    assert L.lpq_mma_peak(3, 10, 8, None) == lpq.ERR_INVALID_ARG     # no such mode
+    assert L.lpq_mma_peak(3, 10, 9, None) == lpq.ERR_INVALID_ARG     # no such mode
     assert L.lpq_mma_peak(2, 10, 4, None) == lpq.ERR_INVALID_ARG     # modes 2..5 are NVFP4 only
     assert L.lpq_mma_peak(0, 10, 7, None) == lpq.ERR_INVALID_ARG     # mode 7 is for the block-scaled kinds
     assert L.lpq_mma_peak(1, 10, -1, None) == lpq.ERR_INVALID_ARG

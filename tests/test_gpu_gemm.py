@@ -212,7 +212,7 @@ def test_bounded_wait_reports_timeout_and_context_survives():
 @pytest.mark.parametrize("kind,mode", [("bf16", 0), ("fp8", 0), ("mxfp8", 0), ("mxfp8", 1), ("nvfp4", 0), ("nvfp4", 1),
                                        ("nvfp4", 2), ("nvfp4", 3), ("nvfp4", 4), ("nvfp4", 5),
                                        ("bf16", 6), ("fp8", 6), ("mxfp8", 6), ("nvfp4", 6), ("mxfp8", 7),
-                                       ("nvfp4", 7)])
+                                       ("nvfp4", 7), ("bf16", 8), ("fp8", 8), ("mxfp8", 8), ("nvfp4", 8)])
 def test_mma_peak_modes_run(kind, mode):
     """Every rate-probe mode runs to completion with a clean device status and
     a rate below the nominal dense peak of its kind (x1.2 for clock slack)."""

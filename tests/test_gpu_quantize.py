@@ -354,6 +354,22 @@ def test_delayed_position_outside_the_ring_wraps():
     assert int(st.pos.item()) == int(ref.pos[0]) == 6
 
 
+@pytest.mark.parametrize("shape", [(64, 128), (176, 272), (4096, 1040)])
+def test_amax_entry_point(shape):
+    """lpq_amax: max |x| and the column-wise RHT amax equal the oracle's (the
+    amax an NVFP4 copy records), overwriting whatever the outputs held."""
+    x, bits = bf16_input(shape, std=2.0, seed=31, outlier_frac=0.001, outlier_scale=40)
+    stale = torch.full((1,), 1e30, dtype=torch.float32, device="cuda")
+    a, r = lpq.amax(x, rht=True, rht_seed=7, out=stale.clone(), rht_out=stale.clone())
+    ref = o.nvfp4(bits, o.NV_ROW | o.NV_COL | o.NV_RHT, rht_seed=7)
+    assert scalar(a) == np.float32(o.amax(bits)) == ref["row_amax"]
+    assert scalar(r) == ref["col_amax"]
+    a2, none = lpq.amax(x)
+    assert none is None and scalar(a2) == scalar(a)
+    e = torch.empty((0, 128), dtype=torch.bfloat16, device="cuda")
+    assert scalar(lpq.amax(e, out=stale.clone())[0]) == 0.0
+
+
 def test_empty_input():
     x = torch.empty((0, 128), dtype=torch.bfloat16, device="cuda")
     q = lpq.quantize(x, lpq.NVFP4, lpq.ROWWISE)
