@@ -1,7 +1,9 @@
 """World-size-2 gloo tests (CPU) of the host logic of the data-parallel path:
 the benchmark's max-over-ranks timing, and the token-sharded quantize + Wgrad
-with its two exchange steps (all-reduce MAX of the amax, all-reduce SUM of
-dW), checked against the unsharded oracle."""
+through the product module's shard split and its two exchange steps
+(precision_transformer_gemms_gb300.dp: exchange_amax = all-reduce MAX of the
+shard amaxes, exchange_wgrad = all-reduce SUM of dW), with the oracle standing
+in for the CUDA kernels, checked against the unsharded oracle."""
 import os
 import socket
 
@@ -56,24 +58,25 @@ def test_max_over_ranks_gloo():
 def _shard_worker(rank, world, port, q):
     _init(rank, world, port)
     import oracle as o
-    from precision_transformer_gemms_gb300 import synth
+    from precision_transformer_gemms_gb300 import dp, synth
     M, K, N = 64, 32, 16
     X = synth.host_bits(synth.bf16_normal((M, K), 1.0, 1, "cpu"))
     dY = synth.host_bits(synth.bf16_normal((M, N), 1e-3, 2, "cpu"))
-    rows = slice(rank * M // world, (rank + 1) * M // world)
-    xs, ds = np.ascontiguousarray(X[rows]), np.ascontiguousarray(dY[rows])
-    # exchange 1: all-reduce MAX of the shard amax -> the global per-tensor scale
-    a = torch.tensor([o.amax(xs)], dtype=torch.float32)
-    dist.all_reduce(a, op=dist.ReduceOp.MAX)
-    scale = float(np.float32(448.0) / np.float32(a.item()))
+    r0, r1 = dp.shard_rows(M, world, rank, granule=16)
+    xs, ds = np.ascontiguousarray(X[r0:r1]), np.ascontiguousarray(dY[r0:r1])
+    # exchange 1: all-reduce MAX of the shard amaxes (X raw, X RHT column, dY raw) in one call
+    a = torch.tensor([o.amax(xs), o.nvfp4(xs, o.NV_COL | o.NV_RHT, rht_seed=9)["col_amax"], o.amax(ds)],
+                     dtype=torch.float32)
+    dp.exchange_amax(a)
+    scale = float(np.float32(448.0) / np.float32(a[0].item()))
     codes = o.fp8_pertensor(xs, o.E4M3, scale=scale, colwise=False)["row"]
     # exchange 2: all-reduce SUM of the shard's dW = dY^T X (FP64 oracle GEMM on bf16)
     A = o.Operand(o.K_BF16, np.ascontiguousarray(ds.T))
     B = o.Operand(o.K_BF16, np.ascontiguousarray(xs.T))
     dw, _ = o.gemm(A, B, N, K, xs.shape[0])
     t = torch.from_numpy(dw.copy())
-    dist.all_reduce(t, op=dist.ReduceOp.SUM)
-    q.put((rank, a.item(), codes, t.numpy()))
+    dp.exchange_wgrad(t)
+    q.put((rank, a.numpy().copy(), codes, t.numpy()))
     dist.destroy_process_group()
 
 
@@ -94,9 +97,31 @@ def test_sharded_quantize_and_wgrad_match_unsharded():
     X = synth.host_bits(synth.bf16_normal((M, K), 1.0, 1, "cpu"))
     dY = synth.host_bits(synth.bf16_normal((M, N), 1e-3, 2, "cpu"))
     full = o.fp8_pertensor(X, o.E4M3, colwise=False)
-    assert res[0][0] == res[1][0] == full["amax"]
+    want = [full["amax"], o.nvfp4(X, o.NV_COL | o.NV_RHT, rht_seed=9)["col_amax"], o.amax(dY)]
+    assert np.array_equal(res[0][0], np.float32(want)) and np.array_equal(res[1][0], res[0][0])
     assert np.array_equal(np.concatenate([res[0][1], res[1][1]]), full["row"])  # codes bit-identical
     ref, _ = o.gemm(o.Operand(o.K_BF16, np.ascontiguousarray(dY.T)), o.Operand(o.K_BF16, np.ascontiguousarray(X.T)),
                     N, K, M)
     assert np.allclose(res[0][2], ref, rtol=1e-12, atol=1e-18)  # only the summation order differs
     assert np.array_equal(res[0][2], res[1][2])
+
+
+def test_shard_rows_cover_the_tokens_in_whole_groups():
+    from precision_transformer_gemms_gb300 import dp
+    for total, world in ((15872, 1), (15872, 2), (15872, 4), (15872, 8), (300, 3), (64, 8), (0, 2)):
+        spans = [dp.shard_rows(total, world, r) for r in range(world)]
+        assert spans[0][0] == 0 and spans[-1][1] == total
+        assert all(a[1] == b[0] for a, b in zip(spans, spans[1:]))
+        assert all(r0 % 128 == 0 for r0, r1 in spans if r1 > r0)  # empty shards sit at the end
+        sizes = [r1 - r0 for r0, r1 in spans]
+        assert max(sizes) - min(sizes) <= 128
+    assert dp.shard_rows(15872, 8, 0) == (0, 2048) and dp.shard_rows(15872, 8, 7) == (13952, 15872)
+    with pytest.raises(ValueError):
+        dp.shard_rows(128, 2, 2)
+
+
+def test_exchanges_are_noops_without_a_process_group():
+    from precision_transformer_gemms_gb300 import dp
+    a = torch.tensor([1.0, 2.0])
+    assert dp.exchange_amax(a) is a and a.tolist() == [1.0, 2.0]
+    assert dp.exchange_wgrad(a) is a and a.tolist() == [1.0, 2.0]
