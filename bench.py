@@ -72,7 +72,29 @@ def parse():
                    help="layer: the contract line; ksweep / drift: the K-sweep and the FP8 drift runs")
     p.add_argument("--mma-peaks", action="store_true",
                    help="only measure the dense tcgen05 rates (shared-memory-resident operands) and exit")
+    p.add_argument("--parallel", choices=["replicas", "tokens"], default="replicas",
+                   help="N > 1: replicas (each rank its own layer, no exchange) or tokens (data parallelism: "
+                        "each rank its own micro-batch of tokens, all-reduce MAX of the amaxes and SUM of dW)")
+    p.add_argument("--no-drift", action="store_true", help="skip the FP8 drift summary in the layer run")
+    p.add_argument("--no-ksweep", action="store_true", help="skip the K-sweep summary in the layer run")
+    p.add_argument("--no-quant-kinds", action="store_true", help="skip the per-kind quantizer roofline")
     return p.parse_args()
+
+
+# ------------------------------------------------------------------ contract line
+METRIC = "quantize+GEMM TFLOP/s & % of FP8/FP4 peak; ms/layer (CodonFM-5B shape)"
+
+
+def contract_config(args, world, recipe, autocast):
+    """The `config` object of the JSON line, identical for both arms."""
+    M = args.micro_batch_size * args.sequence_length
+    mode = "autocast" if autocast else "pre-quantize"
+    par = ("token-sharded data parallel (all-reduce MAX of amaxes, SUM of dW)" if args.parallel == "tokens"
+           else "replicas") + f" x{world}"
+    return {"workload": f"CodonFM-5B layer, 12 GEMMs, {recipe} {mode} (M={M}, hidden {args.hidden_size}, "
+                        f"intermediate {args.intermediate_size})",
+            "global_batch": args.micro_batch_size * world, "seq_len": args.sequence_length, "parallelism": par,
+            "l2": "inputs larger than L2 (working set > 4 GB)"}
 
 
 # ------------------------------------------------------------------ distributed
@@ -346,6 +368,27 @@ def time_steps(layer, recipe, autocast, steps, warmup, world, per_kernel=False):
     return ms / steps, events
 
 
+def time_fn(step_fn, steps, warmup, world):
+    """ms per call of step_fn(s) over `steps` calls after `warmup`, CUDA
+    events on the current stream, barrier + synchronize on both sides, the
+    max over ranks."""
+    import torch
+    for w in range(warmup):
+        step_fn(w)
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for s in range(steps):
+        step_fn(warmup + s)
+    e1.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    return max_over_ranks(e0.elapsed_time(e1), world) / steps
+
+
 def summarize_events(layer, events, steps):
     """Per GEMM: mean GEMM ms and quantize ms over the timed steps."""
     acc = {}
@@ -445,22 +488,138 @@ def run_reference(args, rank, world):
     wall = time.perf_counter() - t0
     sec = statistics.mean(proj)
     value = flops / sec / 1e12
-    line = {"impl": "reference", "metric": "quantize+GEMM TFLOP/s & % of FP8/FP4 peak; ms/layer (CodonFM-5B shape)",
-            "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": sec * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+    # ms_per_step is the measured wall time of one step's bounded sample; the
+    # value is the layer throughput that sample projects to (whole layer:
+    # projected_ms_per_step)
+    line = {"impl": "reference", "metric": METRIC,
+            "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": wall / args.steps * 1e3, "projected_ms_per_step": sec * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f64", "data": "synthetic",
-            "config": {"workload": "CodonFM-5B layer, 12 GEMMs, NVFP4 autocast (M=15872, hidden 4096, "
-                                   "intermediate 16384)", "global_batch": args.micro_batch_size,
-                       "seq_len": args.sequence_length, "parallelism": "replicas"},
+            "config": contract_config(args, world, "nvfp4", True),
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": o.num_threads(), "kind": "oracle",
                              "sample": "per step: per GEMM 2x128 outputs of the FP64 oracle GEMM on NVFP4 operands "
-                                       "and their NVFP4 quantization, projected to the full layer",
+                                       "and their NVFP4 quantization (a 2-row and a 128-row slab of the operands), "
+                                       "projected to the full layer",
                              "wall_s": wall},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
 
 # ------------------------------------------------------------------ main arm
+def check_device(stage):
+    """The device error word must be clean after a timed region: a GEMM whose
+    bounded wait gave up leaves early and only sets that word, so its step
+    would otherwise count as complete work."""
+    from precision_transformer_gemms_gb300 import lpq
+    code = lpq.device_status()
+    if code != 0:
+        raise RuntimeError(f"device error word {code} after {stage}: a bounded device wait gave up; "
+                           "the timed work is incomplete and no number is reported")
+    return code
+
+
+# Algorithmic bytes per input element of one quantize call that emits one
+# copy (the amax pass, where the recipe needs one, reads the input once more).
+QUANT_BYTES_PER_ELEM = {
+    "nvfp4": 2 + 2 + 0.5 + 1 / 16,         # amax pass + read + E2M1 codes and E4M3 scales
+    "fp8_current": 2 + 2 + 1,              # amax pass + read + codes
+    "fp8_delayed": 2 + 1,                  # amax fused into the quantize pass
+    "mxfp8": 2 + 1 + 1 / 32,               # read + codes + E8M0 scales
+    "mxfp8_e5m2": 2 + 1 + 1 / 32,
+    "mxfp4": 2 + 0.5 + 1 / 32,
+    "bf16": 0.0,
+}
+
+
+def quant_bytes_per_layer(layer, recipe):
+    """Per-GEMM autocast: every GEMM quantizes one copy of each operand."""
+    per = QUANT_BYTES_PER_ELEM[recipe]
+    return sum((m * k + n * k) * per for _, _, m, k, n in layer.shapes)
+
+
+def time_quant_kinds(layer, hbm_gbs, reps=10):
+    """Each quantizer kind of the NVFP4 recipe (and the plain FP8 / MXFP8
+    paths) timed alone with CUDA events around each launch, L2 flushed (a
+    256 MB write) before every timed call, on the layer's own tensors:
+    X = the QKV input 15872 x 4096, dY = the QKV gradient 15872 x 12288,
+    W = the MLP-up weight 16384 x 4096.  The quantize calls take the amax as
+    given (LPQ_GIVEN_AMAX), so the amax pass is timed on its own.  Bytes are
+    algorithmic: the bf16 read plus the codes and scales written."""
+    import torch
+    from precision_transformer_gemms_gb300 import lpq as L
+    X, dY, W = layer.inp["qkv"]["X"], layer.inp["qkv"]["dY"], layer.inp["mlp_up"]["W"]
+    dev = X.device
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    nv_w = 0.5 + 1 / 16
+
+    def nv_buf(t, fmt, flags, rht):
+        q = L.alloc(fmt, t.shape[0], t.shape[1], flags, L.SF_GEMM, dev)
+        a, r = L.amax(t, rht=rht, rht_seed=1234)
+        if q.row is not None:
+            q.row.amax.copy_(a)
+        if q.col is not None:
+            q.col.amax.copy_(r if rht else a)
+        return q
+
+    kinds = []
+    a_out = torch.empty(2, dtype=torch.float32, device=dev)
+    kinds.append(("amax", X, lambda: L.amax(X, out=a_out[0:1]), 2.0))
+    kinds.append(("amax_rht", X, lambda: L.amax(X, rht=True, rht_seed=1234, out=a_out[0:1], rht_out=a_out[1:2]), 2.0))
+    for name, t, fmt, flags, rht in (
+            ("nvfp4_row", X, L.NVFP4, L.ROWWISE, False),
+            ("nvfp4_col_rht", X, L.NVFP4, L.COLWISE | L.RHT_COLWISE, True),
+            ("nvfp4_row_sr", dY, L.NVFP4, L.ROWWISE | L.STOCHASTIC, False),
+            ("nvfp4_col_rht_sr", dY, L.NVFP4, L.COLWISE | L.RHT_COLWISE | L.STOCHASTIC, True),
+            ("nvfp4_2d_row", W, L.NVFP4_2D, L.ROWWISE, False),
+            ("nvfp4_2d_col", W, L.NVFP4_2D, L.COLWISE, False),
+            ("fp8_row", X, L.FP8_E4M3, L.ROWWISE, False),
+            ("fp8_col", X, L.FP8_E4M3, L.COLWISE, False)):
+        q = nv_buf(t, fmt, flags, rht)
+        per = 2 + (nv_w if fmt in (L.NVFP4, L.NVFP4_2D) else 1.0)
+        kinds.append((name, t, (lambda t=t, fmt=fmt, flags=flags, q=q:
+                                L.quantize(t, fmt, flags | L.GIVEN_AMAX, seed=7, rht_seed=1234, out=q)), per))
+    for name, flags in (("mxfp8_row", L.ROWWISE), ("mxfp8_col", L.COLWISE)):
+        q = L.alloc(L.MXFP8, X.shape[0], X.shape[1], flags, L.SF_GEMM, dev)
+        kinds.append((name, X, (lambda flags=flags, q=q: L.quantize(X, L.MXFP8, flags, out=q)), 2 + 1 + 1 / 32))
+    out = {}
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for name, t, fn, per in kinds:
+        fn()
+        total = 0.0
+        for _ in range(reps):
+            flush.zero_()
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            total += e0.elapsed_time(e1)
+        us = total / reps * 1e3
+        nbytes = t.numel() * per
+        gbs = nbytes / (us * 1e-6) / 1e9
+        out[name] = {"shape": list(t.shape), "us": round(us, 2), "bytes_per_elem": round(per, 4),
+                     "gbs": round(gbs, 1), "frac": round(gbs / hbm_gbs, 3)}
+    check_device("quantizer kinds")
+    del flush
+    return out
+
+
+def make_dp_linears(layer, recipe, first_row=0, group=None):
+    """The four linears of the layer as token-sharded data-parallel steps
+    (precision_transformer_gemms_gb300.dp) on this rank's inputs."""
+    from precision_transformer_gemms_gb300 import dp
+    return [dp.TokenShardedLinear(recipe, d["X"], d["W"], d["dY"], first_row=first_row, group=group)
+            for d in layer.inp.values()]
+
+
+def dp_kernels_per_step(recipe):
+    """liblpq kernels of one token-sharded layer step (4 linears)."""
+    per_lin = {"nvfp4": 2 + 2 + 2 + 3, "fp8_current": 2 + 2 + 2 + 3, "fp8_delayed": 3 + 3 + 3,
+               "mxfp8": 3 + 3, "mxfp8_e5m2": 3 + 3, "mxfp4": 3 + 3, "bf16": 3}[recipe]
+    # nvfp4 / fp8_current: W (amax + tile), 2 amax passes, X and dY tile passes, 3 GEMMs
+    return 4 * per_lin
+
+
 def run_lpq(args, rank, world, local):
     import torch
     from precision_transformer_gemms_gb300 import lpq
@@ -472,31 +631,52 @@ def run_lpq(args, rank, world, local):
     autocast = not args.prequant
     if recipe == "fp8_delayed":
         autocast = True  # delayed scaling needs the amax history: always dynamic
+    tokens = args.parallel == "tokens" and world > 1
     layer.prequantize(recipe)  # buffers exist before the timed region (pre-quantize mode reads them)
     torch.cuda.synchronize()
+    peaks = measured_peaks()
+    hbm = peaks["hbm_gbs"] if peaks else 6800.0
 
-    # headline: recipe/mode, whole-step CUDA events, K steps
+    # headline: K steps with whole-step CUDA events (replicas: the per-GEMM
+    # autocast layer step; tokens: the data-parallel step with its exchanges)
     clocks = ClockSampler(local)
-    clocks.start()
-    ms_step, _ = time_steps(layer, recipe, autocast, args.steps, args.warmup, world)
-    clk = clocks.stop()
-    # per-kernel durations (same steps, events around each launch)
+    if tokens:
+        lins = make_dp_linears(layer, recipe, first_row=rank * layer.M)
+        clocks.start()
+        ms_step = time_fn(lambda s: [lin.step(seed=s) for lin in lins], args.steps, args.warmup, world)
+        clk = clocks.stop()
+        launches = dp_kernels_per_step(recipe)
+        del lins
+    else:
+        clocks.start()
+        ms_step, _ = time_steps(layer, recipe, autocast, args.steps, args.warmup, world)
+        clk = clocks.stop()
+        launches = layer.kernels_per_step(recipe, autocast)
+    status = check_device("the headline steps")
+    # per-kernel durations (the layer step, events around each launch)
     _, events = time_steps(layer, recipe, autocast, max(3, args.steps // 2), 1, world, per_kernel=True)
+    check_device("the per-kernel steps")
     table = summarize_events(layer, events, max(3, args.steps // 2))
 
     value = layer.flops * world / (ms_step * 1e-3) / 1e12
-    peaks = measured_peaks()
     gemm_ms = sum(r["gemm_ms"] for r in table.values())
     quant_ms = sum(r["quant_ms"] for r in table.values())
     gemm_achieved = layer.flops / (gemm_ms * 1e-3) / 1e12
     ratio = {"bf16": 1, "fp8_current": 2, "fp8_delayed": 2, "mxfp8": 2, "mxfp8_e5m2": 2, "mxfp4": 6,
              "nvfp4": 6}[recipe]
+    # The timed region is well under a second at the maximum SM clock: the
+    # burst bf16 figure x the format's nominal dense ratio is the denominator.
     if peaks:
-        peak = peaks["bf16_tflops_sustained"] * ratio
-        peak_src = f"of measured: bf16_tflops_sustained x {ratio} (nominal dense ratio of the format)"
+        peak = peaks["bf16_tflops"] * ratio
+        peak_src = f"of measured: bf16_tflops (burst) x {ratio} (nominal dense ratio of the format)"
     else:
-        peak = 1700.0 * ratio
-        peak_src = f"of fallback: 1.7 PFLOP/s bf16 sustained x {ratio}"
+        peak = 1900.0 * ratio
+        peak_src = f"of fallback: 1.9 PFLOP/s bf16 burst x {ratio}"
+    # the tensor-core ceiling of the MMA shape the kernel issues, measured now
+    mma_kind = {"bf16": "bf16", "fp8_current": "fp8", "fp8_delayed": "fp8", "mxfp8": "mxfp8",
+                "mxfp8_e5m2": "mxfp8", "mxfp4": "nvfp4", "nvfp4": "nvfp4"}[recipe]
+    ceiling = lpq.mma_peak(mma_kind, iters=8000, with_scale_copies=6)
+    check_device("the tensor-core rate probe")
     algo_bytes = 0
     for name, lay, m, k, n in layer.shapes:
         per = {"nvfp4": 0.5 + 1 / 16, "mxfp8": 1 + 1 / 32, "mxfp8_e5m2": 1 + 1 / 32, "mxfp4": 0.5 + 1 / 32,
@@ -508,10 +688,22 @@ def run_lpq(args, rank, world, local):
     traffic = (profiled_traffic(os.path.join(ROOT, "precision_transformer_gemms_gb300", "csrc", "gemm.cu"), recipe)
                if default_layer and autocast else None)
     roof = {"bound": "tensor", "achieved": gemm_achieved, "peak": peak, "unit": "TFLOP/s",
-            "frac": gemm_achieved / peak, "traffic": traffic,
-            "kernel": f"gemm_pair_kernel ({recipe})",
-            "peak_source": peak_src, "algorithmic_bytes_per_launch": algo_bytes / len(layer.shapes)}
-    hbm = peaks["hbm_gbs"] if peaks else 6800.0
+            "frac": gemm_achieved / peak, "traffic": traffic, "kernel": f"gemm_pair_kernel ({recipe})",
+            "peak_source": peak_src, "algorithmic_bytes_per_launch": algo_bytes / len(layer.shapes),
+            "tcgen05_ceiling": {"value": ceiling, "unit": "TFLOP/s", "frac": gemm_achieved / ceiling,
+                                "how": f"lpq_mma_peak {mma_kind}, CTA pairs (256 x 256 MMAs), operands in shared "
+                                       "memory, measured in this run"}}
+    if recipe != "bf16" and autocast:
+        qb = quant_bytes_per_layer(layer, recipe)
+        roof["quantize"] = {"bound": "hbm", "bytes_per_layer": qb, "ms_per_layer": quant_ms,
+                            "achieved": qb / (quant_ms * 1e-3) / 1e9, "peak": hbm, "unit": "GB/s",
+                            "frac": qb / (quant_ms * 1e-3) / 1e9 / hbm,
+                            "how": "per-GEMM autocast: every GEMM quantizes one copy of each operand; bytes per "
+                                   f"element {QUANT_BYTES_PER_ELEM[recipe]:.4f} (amax pass where the recipe has one, "
+                                   "bf16 read, codes and scales written); time = CUDA events around the quantize "
+                                   "calls of the per-kernel steps"}
+        if not args.no_quant_kinds:
+            roof["quantize"]["kinds"] = time_quant_kinds(layer, hbm)
 
     # e2e (right after the headline, before the recipe sweep: after the sweep's tens of
     # seconds the host link was seen to run slower): every step copies its bf16 inputs
@@ -529,53 +721,43 @@ def run_lpq(args, rank, world, local):
         bi, bo = layer.step_io_bytes()
         steps = max(3, args.steps // 2)
         comp = torch.cuda.current_stream()
-        nlanes = int(os.environ.get("LPQ_E2E_COPY_STREAMS", "1"))  # copy streams per direction (more were slower)
-        s_in = [torch.cuda.Stream() for _ in range(nlanes)]
-        s_out = [torch.cuda.Stream() for _ in range(nlanes)]
-        ev_comp, ev_out = [None, None], [[], []]
+        s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+        ev_comp, ev_out = [None, None], [None, None]
         in_list = [(lin, r) for lin, d in layer.inp.items() for r in d]
         out_list = list(layer.out)
 
         def e2e_step(s):
             k = s % 2
-            ev_in = []
-            for j, st in enumerate(s_in):
-                with torch.cuda.stream(st):
-                    if ev_comp[k] is not None:
-                        st.wait_event(ev_comp[k])  # step s-2 no longer reads input set k
-                    for lin, r in in_list[j::nlanes]:
-                        inp_sets[k][lin][r].copy_(host_in[lin][r], non_blocking=True)
-                    ev = torch.cuda.Event()
-                    ev.record(st)
-                    ev_in.append(ev)
-            for ev in ev_in:
-                comp.wait_event(ev)
-            for ev in ev_out[k]:
-                comp.wait_event(ev)  # outputs of step s-2 have left output set k
+            with torch.cuda.stream(s_in):
+                if ev_comp[k] is not None:
+                    s_in.wait_event(ev_comp[k])  # step s-2 no longer reads input set k
+                for lin, r in in_list:
+                    inp_sets[k][lin][r].copy_(host_in[lin][r], non_blocking=True)
+                ev_in = torch.cuda.Event()
+                ev_in.record(s_in)
+            comp.wait_event(ev_in)
+            if ev_out[k] is not None:
+                comp.wait_event(ev_out[k])  # outputs of step s-2 have left output set k
             layer.inp, layer.out = inp_sets[k], out_sets[k]
             layer.step(recipe, autocast, s)
             ev_comp[k] = torch.cuda.Event()
             ev_comp[k].record(comp)
-            ev_out[k] = []
-            for j, st in enumerate(s_out):
-                with torch.cuda.stream(st):
-                    st.wait_event(ev_comp[k])
-                    for n in out_list[j::nlanes]:
-                        host_out[k][n].copy_(out_sets[k][n], non_blocking=True)
-                    ev = torch.cuda.Event()
-                    ev.record(st)
-                    ev_out[k].append(ev)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_comp[k])
+                for n in out_list:
+                    host_out[k][n].copy_(out_sets[k][n], non_blocking=True)
+                ev_out[k] = torch.cuda.Event()
+                ev_out[k].record(s_out)
 
         # warm-up: every buffer of both sets touched, and the host link past its slow first
         # copies on a fresh box (seen to last more than half a second): at least max(3, W)
-        # steps and at least three seconds of steps (LPQ_E2E_WARMUP overrides the count)
-        e2e_warm = int(os.environ.get("LPQ_E2E_WARMUP", str(max(3, args.warmup))))
+        # steps and at least three seconds of steps
         t_w = time.perf_counter()
         w = 0
-        while w < e2e_warm or (time.perf_counter() - t_w < 3.0 and w < 200):
+        while w < max(3, args.warmup) or (time.perf_counter() - t_w < 3.0 and w < 200):
             e2e_step(w)
             w += 1
-            if w >= e2e_warm:
+            if w >= max(3, args.warmup):
                 torch.cuda.synchronize()
         torch.cuda.synchronize()
         barrier(world)
@@ -585,12 +767,29 @@ def run_lpq(args, rank, world, local):
         torch.cuda.synchronize()
         barrier(world)
         dt = max_over_ranks((time.perf_counter() - t0) / steps, world)
+        check_device("the end-to-end steps")
         layer.inp, layer.out = inp_sets[0], out_sets[0]
         e2e = {"value": layer.flops * world / dt / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": bi,
                "d2h_bytes_per_step": bo, "ms_per_step": dt * 1e3,
-               "copies": f"pinned host <-> device on {nlanes} copy streams per direction, double-buffered against "
-                         "the compute stream"}
+               "copies": "pinned host <-> device, one copy stream per direction, double-buffered against the "
+                         "compute stream"}
         del host_in, host_out, inp_sets, out_sets
+
+    # the data-parallel step on this rank alone (exchanges are no-ops at N = 1):
+    # each tensor quantized once into both copies, then the three GEMMs
+    dp_step = None
+    if not tokens and recipe != "bf16":
+        lins = make_dp_linears(layer, recipe)
+        k = max(3, args.steps // 4)
+        ms = time_fn(lambda s: [lin.step(seed=s) for lin in lins], k, 2, 1)
+        check_device("the data-parallel step")
+        dp_step = {"ms_per_layer": ms, "tflops": layer.flops / (ms * 1e-3) / 1e12,
+                   "what": "precision_transformer_gemms_gb300.dp.TokenShardedLinear x 4 on one rank: amax passes, "
+                           "all-reduce MAX (a no-op on one rank), each tensor quantized once into both copies, "
+                           "Fprop, Dgrad, FP32 Wgrad partial, all-reduce SUM (no-op); under torchrun with "
+                           "--parallel tokens the same step runs with NCCL exchanges"}
+        del lins
+        torch.cuda.empty_cache()
 
     # recipe sweep (fewer steps each)
     recipes = {}
@@ -608,18 +807,9 @@ def run_lpq(args, rank, world, local):
                 res[f"{mode}_ms_per_layer"] = ms
                 res[f"{mode}_tflops"] = layer.flops / (ms * 1e-3) / 1e12
             if r != "bf16":
-                import torch
-                for w in range(2):
-                    layer.fused_step(r, w)
-                torch.cuda.synchronize()
-                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                e0.record()
-                for s_ in range(k):
-                    layer.fused_step(r, 10 + s_)
-                e1.record()
-                torch.cuda.synchronize()
-                res["fused_ms_per_layer"] = e0.elapsed_time(e1) / k
+                res["fused_ms_per_layer"] = time_fn(lambda s_: layer.fused_step(r, s_), k, 2, 1)
                 res["fused_tflops"] = layer.flops / (res["fused_ms_per_layer"] * 1e-3) / 1e12
+            check_device(f"the {r} sweep")
             recipes[r] = res
             # free this recipe's buffers before the next one
             for key in [k_ for k_ in layer.bufs if k_[0] == r and r != recipe]:
@@ -633,6 +823,27 @@ def run_lpq(args, rank, world, local):
                 for mode in ("autocast", "prequant", "fused"):
                     if f"{mode}_ms_per_layer" in res:
                         res[f"{mode}_speedup_vs_bf16"] = b / res[f"{mode}_ms_per_layer"]
+
+    # the FP8 drift run and the K-sweep (the other configurations' workloads), on rank 0
+    drift = ksweep = None
+    if rank == 0 and not args.no_drift:
+        d = drift_results(args)
+        drift = {sc: {"mean_ms_per_step": round(v["mean_ms"], 4),
+                      "saturated_per_step": [r["saturated"] for r in v["steps"]],
+                      "x_amax_first_last": [v["steps"][0]["x_amax"], v["steps"][-1]["x_amax"]]}
+                 for sc, v in d.items()}
+        drift["workload"] = (f"per-tensor FP8 (E4M3 X/W, E5M2 dY), attention-out GEMMs M={layer.M}, "
+                             f"K=N={args.hidden_size}, 20 steps, X std 1 -> 4, Fprop+Dgrad+Wgrad autocast")
+    if rank == 0 and not args.no_ksweep:
+        kres = ksweep_results(reps=5)
+        ksweep = {"workload": "8192 x K x 8192 GEMMs, speed-up vs the bf16 tcgen05 GEMM",
+                  "prequant_speedup": {K: {f: round(v[f]["prequant_speedup_vs_bf16"], 3) for f in v
+                                           if isinstance(v[f], dict)} for K, v in kres.items()},
+                  "autocast_speedup": {K: {f: round(v[f]["autocast_speedup_vs_bf16"], 3) for f in v
+                                           if isinstance(v[f], dict)} for K, v in kres.items()},
+                  "bf16_tflops": {K: round(v["bf16_tflops"], 1) for K, v in kres.items()},
+                  "prequant_tflops": {K: {f: round(v[f]["prequant_tflops"], 1) for f in v
+                                          if isinstance(v[f], dict)} for K, v in kres.items()}}
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -650,25 +861,26 @@ def run_lpq(args, rank, world, local):
 
     if rank == 0:
         line = {
-            "metric": "quantize+GEMM TFLOP/s & % of FP8/FP4 peak; ms/layer (CodonFM-5B shape)",
+            "metric": METRIC,
             "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": {"nvfp4": "e2m1", "mxfp8": "e4m3", "mxfp8_e5m2": "e4m3/e5m2", "mxfp4": "e2m1",
                       "fp8_current": "e4m3/e5m2", "fp8_delayed": "e4m3/e5m2", "bf16": "bf16"}[recipe],
             "data": "synthetic",
-            "config": {"workload": f"CodonFM-5B layer, 12 GEMMs, {recipe} {'autocast' if autocast else 'pre-quantize'}"
-                                   f" (M={layer.M}, hidden {args.hidden_size}, intermediate {args.intermediate_size})",
-                       "global_batch": args.micro_batch_size * world, "seq_len": args.sequence_length,
-                       "parallelism": f"replicas x{world}", "l2": "inputs larger than L2 (working set > 4 GB)"},
+            "config": contract_config(args, world, recipe, autocast),
             "roofline": roof,
             "quantize": {"ms_per_layer": quant_ms, "gemm_ms_per_layer": gemm_ms},
+            "device_status": status,
             "recipes": recipes,
+            "dp_step": dp_step,
+            "drift": drift,
+            "ksweep": ksweep,
             "gemms": {n: {kk: (round(v, 4) if isinstance(v, float) else v) for kk, v in r.items()}
                       for n, r in table.items()},
             "clocks": clk,
             "e2e": e2e,
             "cpu_baseline": cpu,
-            "gpu_launches": layer.kernels_per_step(recipe, autocast) * args.steps,
+            "gpu_launches": launches * args.steps,
             "hbm_peak_gbs": hbm,
         }
         if args.output:
@@ -696,6 +908,7 @@ def run_mma_peaks(args):
             out[kind + "_scale_copies_by_other_warp"] = lpq.mma_peak(kind, iters=iters, with_scale_copies=5)
         # CTA pairs (cta_group::2, 256 x 256 MMAs): the shape the product GEMM issues
         out[kind + "_pair"] = lpq.mma_peak(kind, iters=iters, with_scale_copies=6)
+        out[kind + "_pair_n128_halves"] = lpq.mma_peak(kind, iters=iters, with_scale_copies=8)
         if kind in ("mxfp8", "nvfp4"):
             out[kind + "_pair_scales_stored_by_warps"] = lpq.mma_peak(kind, iters=iters, with_scale_copies=7)
     out["clocks"] = clocks.stop()
@@ -716,27 +929,28 @@ def _event_ms(fn, reps):
     return e0.elapsed_time(e1) / reps
 
 
-def run_ksweep(args):
-    """Scaling-granularity K-sweep: 8192 x K x 8192 GEMMs (inputs ~N(0,1), 0.1%
-    entries x100) under per-tensor FP8, MXFP8, sub-channel FP8 (1x128 act,
-    128x128 weight), NVFP4 (1D act, 2D weight) and bf16; pre-quantize (GEMM
-    only) and autocast (quantize both operands + GEMM) times and speed-ups vs
-    the bf16 tcgen05 GEMM of the same shape."""
+def ksweep_results(reps=10, ks=(1024, 2048, 4096, 8192, 16384)):
+    """Scaling-granularity K-sweep ("Faster training throughput in FP8 with
+    NVIDIA NeMo", scaling up recipe granularity): 8192 x K x 8192 GEMMs
+    (inputs ~N(0,1), 0.1% entries x100) under per-tensor FP8, MXFP8,
+    sub-channel FP8 (1x128 act, 128x128 weight), NVFP4 (1D act, 2D weight),
+    MXFP4 and bf16; pre-quantize (GEMM only) and autocast (quantize both
+    operands + GEMM) times and speed-ups vs the bf16 tcgen05 GEMM of the same
+    shape.  The device error word is checked after each K."""
     import torch
     from precision_transformer_gemms_gb300 import lpq, synth
-    torch.cuda.set_device(0)
     M = N = 8192
     fmts = {"fp8_current": (lpq.FP8_E4M3, lpq.FP8_E4M3), "mxfp8": (lpq.MXFP8, lpq.MXFP8),
             "fp8_subchannel": (lpq.FP8_BLOCK_1x128, lpq.FP8_BLOCK_128x128), "nvfp4": (lpq.NVFP4, lpq.NVFP4_2D),
             "mxfp4": (lpq.MXFP4, lpq.MXFP4)}
     out = {}
-    for K in (1024, 2048, 4096, 8192, 16384):
+    for K in ks:
         A = synth.bf16_normal((M, K), 1.0, 50, "cuda", 0.001, 100.0)
         B = synth.bf16_normal((N, K), 1.0, 51, "cuda", 0.001, 100.0)
         C = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
         ca, cb = lpq.Copy.of_bf16(A), lpq.Copy.of_bf16(B)
         flops = 2 * M * N * K
-        row = {"bf16_ms": _event_ms(lambda: lpq.gemm(lpq.FPROP, ca, cb, c=C), 10)}
+        row = {"bf16_ms": _event_ms(lambda: lpq.gemm(lpq.FPROP, ca, cb, c=C), reps)}
         for name, (fa, fb) in fmts.items():
             qa, qb = lpq.alloc(fa, M, K, lpq.ROWWISE), lpq.alloc(fb, N, K, lpq.ROWWISE)
 
@@ -745,28 +959,36 @@ def run_ksweep(args):
                 lpq.quantize(B, fb, lpq.ROWWISE, out=qb)
 
             quant()
-            g = _event_ms(lambda: lpq.gemm(lpq.FPROP, qa.row, qb.row, c=C), 10)
-            ac = _event_ms(lambda: (quant(), lpq.gemm(lpq.FPROP, qa.row, qb.row, c=C)), 10)
+            g = _event_ms(lambda: lpq.gemm(lpq.FPROP, qa.row, qb.row, c=C), reps)
+            ac = _event_ms(lambda: (quant(), lpq.gemm(lpq.FPROP, qa.row, qb.row, c=C)), reps)
             row[name] = {"prequant_ms": g, "autocast_ms": ac, "prequant_tflops": flops / g / 1e9,
                          "prequant_speedup_vs_bf16": row["bf16_ms"] / g, "autocast_speedup_vs_bf16": row["bf16_ms"] / ac}
             del qa, qb
         row["bf16_tflops"] = flops / row["bf16_ms"] / 1e9
+        check_device(f"K-sweep K={K}")
         out[K] = row
         del A, B, C
         torch.cuda.empty_cache()
+    return out
+
+
+def run_ksweep(args):
+    import torch
+    torch.cuda.set_device(0)
+    out = ksweep_results()
     print(json.dumps({"workload": "K-sweep 8192 x K x 8192", "unit": "ms / TFLOP/s", "results": out}), flush=True)
 
 
-def run_drift(args):
+def drift_results(args, steps=20):
     """Per-tensor FP8 current vs delayed scaling on the attention-output GEMMs
-    (M = 15872, 4096 x 4096 weight) over 20 steps whose activation std drifts
-    1 -> 4 (gradients std 1e-3); Fprop + Dgrad + Wgrad each step, autocast.
-    Reports per step the ms, the amax, the scale in use and how many
-    activations exceed the E4M3 range at that scale (a device-side count).
-    Every step's codes are compared with the oracle in the GPU tests."""
+    (M = micro-batch x sequence tokens, hidden x hidden weight) over 20 steps
+    whose activation std drifts 1 -> 4 (gradients std 1e-3); Fprop + Dgrad +
+    Wgrad each step, autocast.  Per step: the ms, the amax, the scale in use
+    and how many activations exceed the E4M3 range at that scale (a
+    device-side count).  Every step's codes are compared with the oracle in
+    the GPU tests."""
     import torch
     from precision_transformer_gemms_gb300 import lpq, synth
-    torch.cuda.set_device(0)
     M, K, N = args.micro_batch_size * args.sequence_length, args.hidden_size, args.hidden_size
     W = synth.bf16_normal((N, K), synth.WEIGHT_STD, 1, "cuda")
     both = lpq.ROWWISE | lpq.COLWISE
@@ -779,8 +1001,8 @@ def run_drift(args):
         outs = [torch.empty((M, N), dtype=torch.bfloat16, device="cuda"),
                 torch.empty((M, K), dtype=torch.bfloat16, device="cuda"),
                 torch.empty((N, K), dtype=torch.bfloat16, device="cuda")]
-        steps = []
-        for t in range(20):
+        recs = []
+        for t in range(steps):
             X = synth.bf16_normal((M, K), synth.drift_std(t), 10 * t, "cuda")
             dY = synth.bf16_normal((M, N), synth.GRAD_STD, 10 * t + 2, "cuda")
             x_scale = st["X"].scale.clone() if sc else None  # the scale this step's X is quantized with
@@ -802,10 +1024,19 @@ def run_drift(args):
             # 448 / amax (current) or the delayed state's scale before this step's update
             scale = x_scale if sc else 448.0 / bufs["X"].row.amax
             rec["saturated"] = int(((X.float() * scale).abs() > 448.0).sum().item())
-            steps.append(rec)
-        res[scaling] = {"steps": steps, "mean_ms": statistics.mean(s["ms"] for s in steps[2:])}
+            recs.append(rec)
+        check_device(f"drift ({scaling})")
+        res[scaling] = {"steps": recs, "mean_ms": statistics.mean(r["ms"] for r in recs[2:])}
         del bufs, outs
         torch.cuda.empty_cache()
+    return res
+
+
+def run_drift(args):
+    import torch
+    torch.cuda.set_device(0)
+    res = drift_results(args)
+    M, K = args.micro_batch_size * args.sequence_length, args.hidden_size
     print(json.dumps({"workload": f"FP8 drift, attention-out M={M} K=N={K}, 20 steps", "results": res}), flush=True)
 
 

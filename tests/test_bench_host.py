@@ -68,3 +68,46 @@ def test_profiled_traffic_follows_the_kernel_source(tmp_path):
 
 def test_max_over_ranks_single_process():
     assert bench.max_over_ranks(1.5, 1) == pytest.approx(1.5)
+
+
+def _args(**kw):
+    ns = argparse.Namespace(micro_batch_size=31, sequence_length=512, hidden_size=4096, intermediate_size=16384,
+                            parallel="replicas")
+    for k, v in kw.items():
+        setattr(ns, k, v)
+    return ns
+
+
+def test_both_arms_print_the_same_config():
+    """The reference arm and the product arm build `config` with one function."""
+    a = bench.contract_config(_args(), 1, "nvfp4", True)
+    assert a == bench.contract_config(_args(), 1, "nvfp4", True)
+    assert a["workload"].startswith("CodonFM-5B layer, 12 GEMMs, nvfp4 autocast (M=15872")
+    assert a["global_batch"] == 31 and a["parallelism"] == "replicas x1"
+    t = bench.contract_config(_args(parallel="tokens"), 4, "nvfp4", True)
+    assert t["global_batch"] == 124 and t["parallelism"].startswith("token-sharded data parallel")
+
+
+def test_quantizer_bytes_per_layer():
+    """Per-GEMM autocast quantizes one copy of each GEMM operand: 2.483 G
+    operand elements per CodonFM-5B layer, x 4.5625 B for NVFP4 (amax pass 2,
+    read 2, E2M1 codes 0.5, E4M3 scales 1/16)."""
+    layer = bench.Layer.__new__(bench.Layer)
+    h, f, M = 4096, 16384, 15872
+    layer.shapes = []
+    for name, K, N in (("qkv", h, 3 * h), ("attn_out", h, h), ("mlp_up", h, f), ("mlp_down", f, h)):
+        layer.shapes += [(name + "_fprop", 0, M, K, N), (name + "_dgrad", 1, M, N, K), (name + "_wgrad", 2, N, M, K)]
+    elems = sum(m * k + n * k for _, _, m, k, n in layer.shapes)
+    assert elems == 2_483_027_968
+    assert bench.quant_bytes_per_layer(layer, "nvfp4") == pytest.approx(elems * 4.5625)
+    assert bench.quant_bytes_per_layer(layer, "fp8_delayed") == pytest.approx(elems * 3)
+    assert bench.quant_bytes_per_layer(layer, "bf16") == 0
+
+
+def test_dp_kernels_per_step():
+    """Token-sharded step per linear: W amax + tile pass, the X and dY amax
+    passes, their tile passes and three GEMMs (NVFP4); MX formats have no
+    amax passes."""
+    assert bench.dp_kernels_per_step("nvfp4") == 4 * 9
+    assert bench.dp_kernels_per_step("mxfp8") == 4 * 6
+    assert bench.dp_kernels_per_step("bf16") == 4 * 3
