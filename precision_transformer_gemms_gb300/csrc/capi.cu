@@ -8,6 +8,7 @@
 #include <string.h>
 
 #include <mutex>
+#include <map>
 #include <set>
 #include <utility>
 
@@ -107,6 +108,7 @@ std::mutex g_dev_mu;
 std::set<int>* g_sms_known = nullptr;  // devices whose SM count is cached
 int g_sms_of[256];
 std::set<std::pair<int, const void*>>* g_smem_set = nullptr;  // (device, kernel) pairs already raised
+std::map<std::pair<int, const void*>, int>* g_resident = nullptr;  // (device, kernel) -> CTAs per SM
 }  // namespace
 
 int device_sms() {
@@ -122,6 +124,19 @@ int device_sms() {
     g_sms_of[dev] = n;
     g_sms_known->insert(dev);
   }
+  return n;
+}
+
+int resident_ctas(const void* kernel, int threads) {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  std::lock_guard<std::mutex> lock(g_dev_mu);
+  if (!g_resident) g_resident = new std::map<std::pair<int, const void*>, int>();
+  auto it = g_resident->find({dev, kernel});
+  if (it != g_resident->end()) return it->second;
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, 0) != cudaSuccess || n < 1) n = 1;
+  (*g_resident)[{dev, kernel}] = n;
   return n;
 }
 

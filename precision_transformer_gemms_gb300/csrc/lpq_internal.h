@@ -24,6 +24,9 @@ lpq_status cuda_check(cudaError_t e, const char* what);
 // device only, so a second GPU in the same process needs its own call.
 int device_sms();
 lpq_status set_smem_attr(const void* kernel, int bytes);
+// CTAs of `kernel` (with `threads` threads, no dynamic shared memory) that fit
+// on one SM of the current device at once (at least 1); cached per device.
+int resident_ctas(const void* kernel, int threads);
 
 // Scale-factor geometry of the tensor-core layout.
 // Atoms (4 scales of 128 rows) per 128-row group: one per 128 columns for

@@ -22,6 +22,7 @@
 // Every float operation is an explicit round-to-nearest intrinsic so that no
 // multiply-add is contracted.
 #include <cuda_fp16.h>
+#include <algorithm>
 #include <stdio.h>
 
 #include "lpq_device.cuh"
@@ -205,11 +206,18 @@ __device__ __forceinline__ void store_col_staged(const QParams& p, const uint8_t
 
 // NVO (NVFP4 options, compile-time so that the plain paths carry none of the
 // registers of the others): bit 0 stochastic rounding, bit 1 RHT of the
-// column-wise copy.  CTAs per SM: six for the plain path (40 registers),
-// four for stochastic rounding alone (64 registers, no spills; faster than
-// five with spills), five with the RHT (47-48 registers).
+// column-wise copy.  The NVFP4 kernels run one tile per CTA at high occupancy
+// (six CTAs per SM for the plain path at 40 registers, four with stochastic
+// rounding at 64, five with the RHT at 47-48); the other kinds are persistent
+// with a prefetched next tile (their 62-110 registers allow fewer resident
+// CTAs, whose load latency the prefetch covers: FP8 column copy 63 -> 48 us
+// at 15872 x 4096).  Persistence made the NVFP4 kernels slower (fewer
+// resident CTAs with the prefetch registers).
+__host__ __device__ constexpr bool tile_persistent(int kind) { return kind != QK_NV; }
+__host__ __device__ constexpr int tile_min_ctas(int kind, int nvo) { return kind != QK_NV ? 1 : (nvo == 0 ? 6 : (nvo == 1 ? 4 : 5)); }
+
 template <int KIND, bool kE5M2, int NVO = 0>
-__global__ void __launch_bounds__(kThreads, KIND != QK_NV ? 1 : (NVO == 0 ? 6 : (NVO == 1 ? 4 : 5))) quant_tile_kernel(const QParams p) {
+__global__ void __launch_bounds__(kThreads, tile_min_ctas(KIND, NVO)) quant_tile_kernel(const QParams p) {
   constexpr bool kSR = (NVO & 1) != 0, kRHT = (NVO & 2) != 0;
   constexpr int TR = (KIND == QK_BLK1 || KIND == QK_BLK128) ? 128 : 64;
   __shared__ __align__(16) uint16_t tile[TR][kTC];
@@ -221,7 +229,6 @@ __global__ void __launch_bounds__(kThreads, KIND != QK_NV ? 1 : (NVO == 0 ? 6 : 
   __shared__ __align__(4) uint8_t sf_stage[KIND == QK_NV ? 128 * 4 : 4];
 
   const int t = threadIdx.x;
-  const int64_t r0 = (int64_t)blockIdx.y * TR, c0 = (int64_t)blockIdx.x * kTC;
   // The shared tile feeds the column-wise copy and the 2D / 128x128 scales.
   const bool kNeedTile = p.col_codes != nullptr || KIND == QK_BLK128;
   const int64_t R = p.R, C = p.C;
@@ -258,28 +265,74 @@ __global__ void __launch_bounds__(kThreads, KIND != QK_NV ? 1 : (NVO == 0 ? 6 : 
   }
   const PhiloxKeys keys(kSR ? p.seed : 0);  // dead (and free) without stochastic rounding
 
-  // ---------------------------------------------------------------- load (+ row-wise copy)
-  const int lr = t >> 4;        // row within a 16-row slab
-  const int lc = (t & 15) * 8;  // first of this thread's 8 columns
+  // ---------------------------------------------------------------- tiles
+  // CTA b takes tiles b, b + gridDim.x, ... (row-major over the [R / TR,
+  // C / 128] tiles).  Persistent kinds issue the next tile's 16-byte loads
+  // before the current tile is processed, so each CTA keeps a tile in flight
+  // while it quantizes; NVFP4 launches one CTA per tile.
+  const int lr = t >> 4;                     // row within a 16-row slab
+  const int lc = (t & 15) * 8;               // first of this thread's 8 columns
+  const int wr = t >> 3, wc = (t & 7) * 16;  // NVFP4: one thread per 16-value block, 32 rows a pass
+  const int64_t ntx = (C + kTC - 1) / kTC;
+  const int64_t ntiles = ntx * ((R + TR - 1) / TR);
+  constexpr int NLD = TR / 16;  // 16-byte loads per thread and tile
+  constexpr bool kPersist = tile_persistent(KIND);
+  // origin of tile tl (persistent kinds) or of this CTA's tile (blockIdx)
+  auto tile_origin = [&](int64_t tl, int64_t& r0, int64_t& c0) {
+    if constexpr (kPersist) {
+      const uint32_t ty = (uint32_t)tl / (uint32_t)ntx;  // fewer than 2^32 tiles (checked at launch)
+      r0 = (int64_t)ty * TR;
+      c0 = ((int64_t)tl - (int64_t)ty * ntx) * kTC;
+    } else {
+      r0 = (int64_t)blockIdx.y * TR;
+      c0 = (int64_t)blockIdx.x * kTC;
+    }
+  };
+  auto load_tile = [&](int64_t tl, uint4 (&v)[NLD]) {
+    int64_t r0, c0;
+    tile_origin(tl, r0, c0);
+    if constexpr (KIND == QK_NV) {
+      const bool wcol_ok = c0 + wc < C;  // C is a multiple of 16: whole blocks
+#pragma unroll
+      for (int it = 0; it < TR / 32; ++it) {
+        const int64_t r = r0 + it * 32 + wr;
+        const bool ok = wcol_ok && r < R;
+        const uint16_t* src = p.x + r * C + c0 + wc;
+        v[2 * it] = ok ? ld_stream(src) : make_uint4(0u, 0u, 0u, 0u);
+        v[2 * it + 1] = ok ? ld_stream(src + 8) : make_uint4(0u, 0u, 0u, 0u);
+      }
+    } else {
+      const bool col_ok = c0 + lc < C;
+#pragma unroll
+      for (int it = 0; it < TR / 16; ++it) {
+        const int64_t r = r0 + it * 16 + lr;
+        v[it] = (col_ok && r < R) ? ld_stream(p.x + r * C + c0 + lc) : make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+  };
+  float run_amax = 0.f;  // FP8 delayed scaling: the amax of every element this CTA reads
+  uint4 nxt[kPersist ? NLD : 1];
+  int64_t tl = kPersist ? (int64_t)blockIdx.x : 0;
+  const int64_t tl_end = kPersist ? ntiles : 1, tl_step = kPersist ? (int64_t)gridDim.x : 1;
+  if constexpr (kPersist) {
+    if (tl < tl_end) load_tile(tl, nxt);
+  }
+  for (; tl < tl_end; tl += tl_step) {
+  int64_t r0, c0;
+  tile_origin(tl, r0, c0);
+  uint4 vbuf[NLD];
+  if constexpr (kPersist) {
+#pragma unroll
+    for (int i = 0; i < NLD; ++i) vbuf[i] = nxt[i];
+    if (tl + tl_step < tl_end) load_tile(tl + tl_step, nxt);
+    __syncthreads();  // the previous tile's readers of the shared memory are done
+  } else {
+    load_tile(tl, vbuf);
+  }
   const bool col_ok = c0 + lc < C;
   float local_amax = 0.f;
-  // all of this thread's 16-byte loads first, so they are in flight together
-  uint4 vbuf[TR / 16];
   if constexpr (KIND == QK_NV) {
-    // NVFP4 1D: one thread per 16-value block (8 threads per 128-column row,
-    // 32 rows a pass), so each block's scale is computed once, without a
-    // shuffle, and the stochastic-rounding words come from four independent
-    // Philox blocks.
-    const int wr = t >> 3, wc = (t & 7) * 16;
-    const bool wcol_ok = c0 + wc < C;  // C is a multiple of 16: whole blocks
-#pragma unroll
-    for (int it = 0; it < TR / 32; ++it) {
-      const int64_t r = r0 + it * 32 + wr;
-      const bool ok = wcol_ok && r < R;
-      const uint16_t* src = p.x + r * C + c0 + wc;
-      vbuf[2 * it] = ok ? ld_stream(src) : make_uint4(0u, 0u, 0u, 0u);
-      vbuf[2 * it + 1] = ok ? ld_stream(src + 8) : make_uint4(0u, 0u, 0u, 0u);
-    }
+    const bool wcol_ok = c0 + wc < C;
 #pragma unroll
     for (int it = 0; it < TR / 32; ++it) {
       const int rl = it * 32 + wr;
@@ -314,11 +367,6 @@ __global__ void __launch_bounds__(kThreads, KIND != QK_NV ? 1 : (NVO == 0 ? 6 : 
       }
     }
   } else {
-#pragma unroll
-  for (int it = 0; it < TR / 16; ++it) {
-    const int64_t r = r0 + it * 16 + lr;
-    vbuf[it] = (col_ok && r < R) ? ld_stream(p.x + r * C + c0 + lc) : make_uint4(0u, 0u, 0u, 0u);
-  }
 #pragma unroll
   for (int it = 0; it < TR / 16; ++it) {
     const int rl = it * 16 + lr;
@@ -377,16 +425,8 @@ __global__ void __launch_bounds__(kThreads, KIND != QK_NV ? 1 : (NVO == 0 ? 6 : 
   }
 
   }  // load + row-wise copy, other kinds
-  if constexpr (KIND == QK_FP8) {
-    if (p.fused_amax0) {  // delayed scaling: amax measured in this pass
-      float m = block_max(local_amax, red);
-      if (t == 0) {
-        atomic_max_nonneg(p.fused_amax0, m);
-        if (p.fused_amax1) atomic_max_nonneg(p.fused_amax1, m);
-      }
-    }
-  }
-  if (!kNeedTile) return;
+  if constexpr (KIND == QK_FP8) run_amax = fmaxf(run_amax, local_amax);
+  if (!kNeedTile) continue;
   __syncthreads();
 
   // ---------------------------------------------------------------- 128x128 tiles
@@ -425,11 +465,11 @@ __global__ void __launch_bounds__(kThreads, KIND != QK_NV ? 1 : (NVO == 0 ? 6 : 
         }
       }
     }
-    return;
+    continue;
   }
 
   if constexpr (KIND == QK_BLK1) {
-    if (!p.col_codes) return;
+    if (!p.col_codes) continue;
     const int cl = t & 127, rh = t >> 7;
     const int64_t c = c0 + cl, rbase = r0 + rh * 64;
     float m = 0.f;
@@ -454,11 +494,11 @@ __global__ void __launch_bounds__(kThreads, KIND != QK_NV ? 1 : (NVO == 0 ? 6 : 
         p.col_sfinv[off] = __fdiv_rn(1.0f, s);
       }
     }
-    return;
+    continue;
   }
 
   // ---------------------------------------------------------------- column-wise copy
-  if (!p.col_codes) return;
+  if (!p.col_codes) continue;
   if constexpr (KIND == QK_NV) {
     // Two adjacent columns per thread (each 4-byte shared load holds a row's
     // values of both), one 16-row block: RHT, block scale and codes per
@@ -496,11 +536,11 @@ __global__ void __launch_bounds__(kThreads, KIND != QK_NV ? 1 : (NVO == 0 ? 6 : 
     }
     __syncthreads();
     store_col_staged(p, col_stage, sf_stage, c0, r0, t);
-    return;
+    continue;
   }
   const int cl = t & 127, rh = t >> 7;
   const int64_t c = c0 + cl, rbase = r0 + rh * 32;
-  if (c >= C || rbase >= R) return;
+  if (c >= C || rbase >= R) continue;
   const int nvalid = (R - rbase) >= 32 ? 32 : 16;  // R is a multiple of 16 here
   if constexpr (KIND == QK_MX4) {
     // R is a multiple of 32 here: the thread's 32 rows are one whole block.
@@ -553,7 +593,18 @@ __global__ void __launch_bounds__(kThreads, KIND != QK_NV ? 1 : (NVO == 0 ? 6 : 
     for (int j = 0; j < 4; ++j)
       if (j * 8 < nvalid) *reinterpret_cast<uint4*>(dst + 8 * j) = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
   }
+  }  // tiles
+  if constexpr (KIND == QK_FP8) {
+    if (p.fused_amax0) {  // delayed scaling: amax measured in this pass, one atomic per CTA
+      const float m = block_max(run_amax, red);
+      if (t == 0) {
+        atomic_max_nonneg(p.fused_amax0, m);
+        if (p.fused_amax1) atomic_max_nonneg(p.fused_amax1, m);
+      }
+    }
+  }
 }
+
 
 // ---------------------------------------------------------------- NVFP4 2D (16x16 weight tiles)
 // One CTA per 64 x 128 tile; warp w owns the 16 x 64 strip at rows
@@ -783,8 +834,18 @@ __global__ void scale_update_kernel(float* hist, int32_t* pos, float* scale, flo
 template <int KIND, bool kE5M2, int NVO = 0>
 lpq_status run_tile(const QParams& p, cudaStream_t s) {
   constexpr int TR = (KIND == QK_BLK1 || KIND == QK_BLK128) ? 128 : 64;
+  const int64_t tiles = ((p.C + kTC - 1) / kTC) * ((p.R + TR - 1) / TR);
+  if (tiles == 0) return LPQ_OK;
+  // persistent kinds: as many CTAs as fit on the GPU at once (each loops
+  // over tiles); NVFP4: one CTA per tile
   dim3 grid((unsigned)((p.C + kTC - 1) / kTC), (unsigned)((p.R + TR - 1) / TR));
-  if (grid.y > 65535u) return set_error(LPQ_ERR_SHAPE, "too many rows (%lld) for one launch", (long long)p.R);
+  if (tile_persistent(KIND)) {
+    if (tiles >= ((int64_t)1 << 32)) return set_error(LPQ_ERR_SHAPE, "too many tiles (%lld)", (long long)tiles);
+    const int per_sm = resident_ctas(reinterpret_cast<const void*>(quant_tile_kernel<KIND, kE5M2, NVO>), kThreads);
+    grid = dim3((unsigned)std::min<int64_t>(tiles, (int64_t)device_sms() * per_sm), 1);
+  } else if (grid.y > 65535u) {
+    return set_error(LPQ_ERR_SHAPE, "too many rows (%lld) for one launch", (long long)p.R);
+  }
   quant_tile_kernel<KIND, kE5M2, NVO><<<grid, kThreads, 0, s>>>(p);
   return cuda_check(cudaGetLastError(), "quantize kernel launch");
 }
