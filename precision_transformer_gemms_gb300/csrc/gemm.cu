@@ -1042,9 +1042,9 @@ __global__ void __launch_bounds__(kBlkThreads, 1)
       const int64_t row = (int64_t)mt * kBM + q * 32 + lane;
       const int64_t n0 = (int64_t)nt * BN;
       const int64_t ncol = n0 + half * HALF + 2 * lane;  // this lane's two B-factor columns
-      float acc[HALF];
+      float2 acc[HALF / 2];  // column pairs: the promotion runs as packed two-wide FMAs
 #pragma unroll
-      for (int i = 0; i < HALF; ++i) acc[i] = 0.f;
+      for (int i = 0; i < HALF / 2; ++i) acc[i] = make_float2(0.f, 0.f);
       // factors of the first kBlkAhead slices
       float fa_ring[kBlkAhead];
       float2 fb_ring[kBlkAhead];
@@ -1086,17 +1086,22 @@ __global__ void __launch_bounds__(kBlkThreads, 1)
 #pragma unroll
             for (int i4 = 0; i4 < 8; ++i4) {
               const float4 f4 = *reinterpret_cast<const float4*>(sbs + 32 * cc + 4 * i4);  // broadcast
-              const float f[4] = {f4.x, f4.y, f4.z, f4.w};
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const int i = 4 * i4 + e;
-                acc[32 * cc + i] = fmaf(__uint_as_float(v[i]), fa * f[e], acc[32 * cc + i]);
-              }
+              // row factor x the four columns' factors, then acc += partial x factor (packed)
+              const float2 w01 = __fmul2_rn(make_float2(fa, fa), make_float2(f4.x, f4.y));
+              const float2 w23 = __fmul2_rn(make_float2(fa, fa), make_float2(f4.z, f4.w));
+              const int i = 4 * i4;
+              float2& a01 = acc[16 * cc + 2 * i4];
+              float2& a23 = acc[16 * cc + 2 * i4 + 1];
+              a01 = __ffma2_rn(make_float2(__uint_as_float(v[i]), __uint_as_float(v[i + 1])), w01, a01);
+              a23 = __ffma2_rn(make_float2(__uint_as_float(v[i + 2]), __uint_as_float(v[i + 3])), w23, a23);
             }
           } else {
             const float f = fa * fbv.x;
+            const float2 w = make_float2(f, f);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) acc[32 * cc + i] = fmaf(__uint_as_float(v[i]), f, acc[32 * cc + i]);
+            for (int i = 0; i < 16; ++i)
+              acc[16 * cc + i] = __ffma2_rn(make_float2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])), w,
+                                            acc[16 * cc + i]);
           }
         }
       }
@@ -1109,11 +1114,13 @@ __global__ void __launch_bounds__(kBlkThreads, 1)
         if (vec_ok && ncols >= HALF) {
 #pragma unroll
           for (int i = 0; i < HALF / 4; ++i)
-            reinterpret_cast<float4*>(out)[i] = make_float4(acc[4 * i], acc[4 * i + 1], acc[4 * i + 2], acc[4 * i + 3]);
+            reinterpret_cast<float4*>(out)[i] = make_float4(acc[2 * i].x, acc[2 * i].y, acc[2 * i + 1].x, acc[2 * i + 1].y);
         } else {
 #pragma unroll
-          for (int i = 0; i < HALF; ++i)
-            if (i < ncols) out[i] = acc[i];
+          for (int i = 0; i < HALF / 2; ++i) {
+            if (2 * i < ncols) out[2 * i] = acc[i].x;
+            if (2 * i + 1 < ncols) out[2 * i + 1] = acc[i].y;
+          }
         }
       } else {
         __nv_bfloat16* out = static_cast<__nv_bfloat16*>(g.c) + row * g.N + c0;
@@ -1123,15 +1130,17 @@ __global__ void __launch_bounds__(kBlkThreads, 1)
             uint32_t w[4];
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-              __nv_bfloat162 h = __floats2bfloat162_rn(acc[8 * i + 2 * j], acc[8 * i + 2 * j + 1]);
+              __nv_bfloat162 h = __floats2bfloat162_rn(acc[4 * i + j].x, acc[4 * i + j].y);
               w[j] = *reinterpret_cast<uint32_t*>(&h);
             }
             reinterpret_cast<uint4*>(out)[i] = make_uint4(w[0], w[1], w[2], w[3]);
           }
         } else {
 #pragma unroll
-          for (int i = 0; i < HALF; ++i)
-            if (i < ncols) out[i] = __float2bfloat16_rn(acc[i]);
+          for (int i = 0; i < HALF / 2; ++i) {
+            if (2 * i < ncols) out[2 * i] = __float2bfloat16_rn(acc[i].x);
+            if (2 * i + 1 < ncols) out[2 * i + 1] = __float2bfloat16_rn(acc[i].y);
+          }
         }
       }
     }
