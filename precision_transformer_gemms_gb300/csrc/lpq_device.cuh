@@ -50,6 +50,19 @@ __device__ __forceinline__ uint32_t cvt_e2m1x2(float lo, float hi) {
       : "=r"(r) : "f"(hi), "f"(lo));
   return r;
 }
+// Eight fp32 -> eight E2M1 codes packed into 32 bits (nibble i = value i),
+// RNE, saturating: four paired conversions and one byte pack.
+__device__ __forceinline__ uint32_t cvt_e2m1x8(const float v[8]) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 t0, t1, t2, t3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 t0, %2, %1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 t1, %4, %3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 t2, %6, %5;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 t3, %8, %7;\n\t"
+      "mov.b32 %0, {t0, t1, t2, t3};\n\t}"
+      : "=r"(r) : "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]));
+  return r;
+}
 template <bool kE5M2>
 __device__ __forceinline__ uint16_t cvt_fp8x2(float lo, float hi) {
   if constexpr (kE5M2) return cvt_e5m2x2(lo, hi); else return cvt_e4m3x2(lo, hi);

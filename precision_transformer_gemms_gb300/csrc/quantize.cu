@@ -120,23 +120,25 @@ __device__ __forceinline__ void nv_factor_table(float* tab, float s_enc, int t) 
 // i).  f == 0 marks a block whose scale decoded to 0: all codes +0.
 __device__ __forceinline__ uint32_t nv_codes8(const float v[8], float f, bool sr, uint4 w0, uint4 w1) {
   if (f == 0.f) return 0u;
-  uint32_t out = 0;
+  float y[8];
   if (sr) {  // y = v * f and the rounding two values at a time (packed two-wide operations)
     const uint32_t w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const float2 yy = __fmul2_rn(make_float2(v[2 * i], v[2 * i + 1]), make_float2(f, f));
       const float2 r = sr_e2m1_value2(yy, w[2 * i], w[2 * i + 1]);
-      out |= cvt_e2m1x2(r.x, r.y) << (8 * i);
+      y[2 * i] = r.x;
+      y[2 * i + 1] = r.y;
     }
-    return out;
-  }
+  } else {
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {  // y = v * f two at a time (packed), RNE encode
-    const float2 yy = __fmul2_rn(make_float2(v[2 * i], v[2 * i + 1]), make_float2(f, f));
-    out |= cvt_e2m1x2(yy.x, yy.y) << (8 * i);
+    for (int i = 0; i < 4; ++i) {  // y = v * f two at a time (packed), RNE encode
+      const float2 yy = __fmul2_rn(make_float2(v[2 * i], v[2 * i + 1]), make_float2(f, f));
+      y[2 * i] = yy.x;
+      y[2 * i + 1] = yy.y;
+    }
   }
-  return out;
+  return cvt_e2m1x8(y);
 }
 
 template <bool kE5M2>
