@@ -138,3 +138,39 @@ def test_single_rank_step_equals_unsharded_quantization():
     assert np.array_equal(codes(lin.q["dY"].col), codes(wd.col))
     ref, bound = o.gemm(oracle_operand(lin.q["dY"].col), oracle_operand(lin.q["X"].col), N, K, M)
     assert gemm_gate(dW, ref, bound, False)[0] == 0
+
+
+@pytest.mark.parametrize("recipe", ["fp8_delayed", "mxfp8", "bf16"])
+def test_two_rank_exchange_other_recipes(recipe):
+    """The other branches of the exchange: delayed scaling all-reduces the amax
+    its quantize pass measured before the history update (both ranks then hold
+    the same state and tensor scales), MXFP8 exchanges no amax (block-local
+    scales; shard codes equal the unsharded tensor's rows), bf16 only sums
+    dW.  In every recipe the all-reduced dW is the same on both ranks and
+    within the gate of the oracle's FP64 sum of the shards' partials."""
+    res = _run(recipe)
+    assert all(r["status"] == 0 for r in res.values())
+    assert np.array_equal(res[0]["dW"], res[1]["dW"])
+    if recipe != "bf16":
+        for role in ("X", "dY"):
+            assert res[0][f"{role}_row_ts"] == res[1][f"{role}_row_ts"]
+        ref = np.zeros((N, K))
+        bound = np.zeros((N, K))
+        for r in res.values():
+            p, b = o.gemm(r["dY_col_op"], r["X_col_op"], N, K, r["r1"] - r["r0"])
+            ref += p
+            bound += b
+        nbad, worst = gemm_gate(torch.from_numpy(res[0]["dW"]), ref, bound, False)
+        assert nbad == 0, f"dW: {nbad} outside the gate ({worst:.3g}x)"
+    if recipe == "mxfp8":
+        X, W, dY = _inputs("cuda")
+        whole = lpq.quantize(X, lpq.MXFP8, lpq.ROWWISE | lpq.COLWISE, sf_layout=lpq.SF_PLAIN)
+        for r in res.values():
+            assert np.array_equal(r["X_row"], codes(whole.row)[r["r0"]:r["r1"]])
+            assert np.array_equal(r["X_col"], codes(whole.col)[:, r["r0"]:r["r1"]])
+    if recipe == "bf16":
+        X, W, dY = _inputs("cuda")
+        ref, bound = o.gemm(o.Operand(o.K_BF16, synth.host_bits(dY.t().contiguous())),
+                            o.Operand(o.K_BF16, synth.host_bits(X.t().contiguous())), N, K, M)
+        nbad, worst = gemm_gate(torch.from_numpy(res[0]["dW"]), ref, bound, False)
+        assert nbad == 0, f"bf16 dW: {nbad} outside the gate ({worst:.3g}x)"
