@@ -259,6 +259,11 @@ lpq_status lpq_gemm(int32_t layout, const lpq_qview *a, const lpq_qview *b, void
  *                 MMA-issuing thread (tcgen05.cp).
  *   direct_store  CTA-pair kernel, bf16 output: 0 = TMA tile stores through
  *                 shared memory (when n % 8 == 0); 1 = stores from registers.
+ *   whole_tiles   CTA-pair kernel: 0 = when the tiles left for the last round
+ *                 of the persistent schedule fill at most half of the CTA
+ *                 pairs, each of them runs as two 256 x 128 halves (N = 128
+ *                 MMAs) on two pairs, so that the last round takes half as
+ *                 long; 1 = whole 256 x 256 tiles only.
  *   reserved      must be 0.
  * Values outside these sets give LPQ_ERR_INVALID_ARG. */
 typedef struct {
@@ -266,7 +271,8 @@ typedef struct {
   int32_t tile_n;
   int32_t scale_copies;
   int32_t direct_store;
-  int32_t reserved[4];
+  int32_t whole_tiles;
+  int32_t reserved[3];
 } lpq_gemm_opts;
 
 /* lpq_gemm with explicit kernel-path options (NULL = all defaults). */

@@ -274,9 +274,11 @@ lpq_status lpq_gemm_ex(int32_t layout, const lpq_qview* a, const lpq_qview* b, v
   if (!a || !b) return set_error(LPQ_ERR_INVALID_ARG, "NULL operand");
   if (opts) {
     if (opts->single_cta < 0 || opts->single_cta > 1 || opts->scale_copies < 0 || opts->scale_copies > 1 ||
-        opts->direct_store < 0 || opts->direct_store > 1 || !(opts->tile_n == 0 || opts->tile_n == 128 || opts->tile_n == 256))
-      return set_error(LPQ_ERR_INVALID_ARG, "lpq_gemm_opts: single_cta, scale_copies, direct_store 0/1; tile_n 0, 128 or 256");
-    for (int i = 0; i < 4; ++i)
+        opts->direct_store < 0 || opts->direct_store > 1 || opts->whole_tiles < 0 || opts->whole_tiles > 1 ||
+        !(opts->tile_n == 0 || opts->tile_n == 128 || opts->tile_n == 256))
+      return set_error(LPQ_ERR_INVALID_ARG,
+                       "lpq_gemm_opts: single_cta, scale_copies, direct_store, whole_tiles 0/1; tile_n 0, 128 or 256");
+    for (int i = 0; i < 3; ++i)
       if (opts->reserved[i]) return set_error(LPQ_ERR_INVALID_ARG, "lpq_gemm_opts.reserved must be 0");
   }
   if (layout < LPQ_FPROP || layout > LPQ_WGRAD) return set_error(LPQ_ERR_INVALID_ARG, "layout %d", layout);

@@ -96,8 +96,10 @@ struct GemmArgs {
   const float* alpha_a;  // per-tensor factors (may be NULL)
   const float* alpha_b;
   uint32_t idesc;
+  uint32_t idesc_half;  // CTA-pair kernel: the same with N = 128 (half tiles)
   int num_k;  // k-tiles of kKBytes
   int tiles_m, tiles_n;
+  int full_tiles, items;  // CTA-pair kernel: work items (whole tiles, then half tiles)
 };
 
 // Tile t of the persistent schedule -> (m tile, n tile): consecutive tiles
@@ -110,6 +112,22 @@ __device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int
   const int r = t - group * per_group;
   mt = first_m + r % gsize;
   nt = r / gsize;
+}
+
+// Work item w of the CTA-pair kernel's persistent schedule -> (m tile, n tile,
+// part): the first g.full_tiles items are whole 256 x 256 tiles in tile_coords
+// order; each item after them is one 256 x 128 half (part 0 or 1) of the
+// remaining tiles, two items per tile.  part = -1 for a whole tile.
+__device__ __forceinline__ void work_coords(int w, int full_tiles, int tiles_m, int tiles_n, int& mt, int& nt,
+                                            int& part) {
+  if (w < full_tiles) {
+    tile_coords(w, tiles_m, tiles_n, mt, nt);
+    part = -1;
+    return;
+  }
+  const int h = w - full_tiles;
+  tile_coords(full_tiles + (h >> 1), tiles_m, tiles_n, mt, nt);
+  part = h & 1;
 }
 
 // After an abort: wait (bounded, whatever the abort flag says) until the loads
@@ -534,8 +552,9 @@ __device__ __forceinline__ void tmem_cp_sf_pair(uint32_t taddr, uint64_t sdesc) 
 template <int KIND, bool kSfbFull, bool SFST>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm + (SFST ? 32 * kSfWarps : 0))
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                     const __grid_constant__ CUtensorMap tmSfa, const __grid_constant__ CUtensorMap tmSfb,
-                     const __grid_constant__ CUtensorMap tmC, const GemmArgs g) {
+                     const __grid_constant__ CUtensorMap tmBh, const __grid_constant__ CUtensorMap tmSfa,
+                     const __grid_constant__ CUtensorMap tmSfb, const __grid_constant__ CUtensorMap tmC,
+                     const GemmArgs g) {
   using PC = PairCfg<KIND, kSfbFull, SFST>;
   constexpr int S = PC::kStages, NACC = PC::kNacc;
   extern __shared__ uint8_t smem_raw[];
@@ -559,7 +578,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm + (SFST
   const uint32_t rank = cluster_ctarank();
   const bool leader = rank == 0;
   const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
-  const int total = g.tiles_m * g.tiles_n;  // tiles_m counts 256-row pair tiles
+  const int total = g.items;  // work items: whole tiles, then half tiles
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -577,6 +596,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm + (SFST
     fence_barrier_init();
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
+    if (g.full_tiles < g.items) prefetch_tmap(&tmBh);
   }
   if (warp == 1) tmem_alloc_pair(tmem_slot, 512);
   tc_fence_before();
@@ -602,25 +622,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm + (SFST
       uint32_t s = 0, ph = 0, it = 0;
       bool ok = true;
       for (int t = pair; t < total && ok; t += npairs) {
-        int mt, nt;
-        tile_coords(t, g.tiles_m, g.tiles_n, mt, nt);
-        const int32_t arow = mt * 256 + (int32_t)rank * 128, brow = nt * kPairBN + (int32_t)rank * 128;
+        int mt, nt, part;
+        work_coords(t, g.full_tiles, g.tiles_m, g.tiles_n, mt, nt, part);
+        // A half tile (part >= 0) has 128 B rows, 64 in each CTA, and the scale
+        // atoms of their one 128-row group (in the first group slot)
+        const bool hf = part >= 0;
+        const int32_t arow = mt * 256 + (int32_t)rank * 128;
+        const int32_t brow = hf ? nt * kPairBN + part * 128 + (int32_t)rank * 64 : nt * kPairBN + (int32_t)rank * 128;
+        const uint32_t kb = hf ? PC::kB / 2 : PC::kB;
+        const int ngb = hf ? 1 : PC::kSfbGroups;
+        const uint32_t ksfb = (uint32_t)ngb * PC::kSfAtoms * 512;
         for (int kt = 0; kt < g.num_k; ++kt) {
           if (!(ok = mbar_wait_bounded(&empty[s], ph ^ 1u, abort_flag, &g_device_error))) break;
-          if (leader) mbar_arrive_expect_tx(&full[s], SFST ? 2 * (PC::kA + PC::kB) : 2 * PC::kStage);
+          if (leader) mbar_arrive_expect_tx(&full[s], SFST ? 2 * (PC::kA + kb) : 2 * (PC::kA + kb + PC::kSfa + ksfb));
           const uint32_t fb = full_leader + 8 * s;
           if constexpr (PC::kSfAtoms > 0) {
             // scale atoms: rows of a 2D map are 512-byte atoms (128 x u32).  With
             // scale warps they land on this CTA's own barrier (its scale warps
             // read them); otherwise on the even CTA's full barrier (pair copies).
             const int32_t ga = mt * 2 + (int32_t)rank;
-            if constexpr (SFST) mbar_arrive_expect_tx(&sfd[s], PC::kSfa + PC::kSfb);
+            if constexpr (SFST) mbar_arrive_expect_tx(&sfd[s], PC::kSfa + ksfb);
             const int32_t ya = (int32_t)(ga * g.sfa_kt + kt * PC::kSfAtoms);
             if constexpr (SFST) tma_load_2d(sSfa + s * PC::kSfa, &tmSfa, 0, ya, &sfd[s]);
             else tma_load_2d_pair(sSfa + s * PC::kSfa, &tmSfa, 0, ya, fb);
 #pragma unroll
             for (int i = 0; i < PC::kSfbGroups; ++i) {
-              int64_t gb = kSfbFull ? (int64_t)nt * 2 + i : (int64_t)nt * 2 + rank;
+              if (i >= ngb) break;
+              int64_t gb = hf ? (int64_t)nt * 2 + part : kSfbFull ? (int64_t)nt * 2 + i : (int64_t)nt * 2 + rank;
               if (gb >= g.sfb_groups) gb = g.sfb_groups - 1;
               const int32_t yb = (int32_t)(gb * g.sfb_kt + kt * PC::kSfAtoms);
               if constexpr (SFST) tma_load_2d(sSfb + s * PC::kSfb + i * PC::kSfAtoms * 512, &tmSfb, 0, yb, &sfd[s]);
@@ -628,7 +656,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm + (SFST
             }
           }
           tma_load_2d_pair(sA + s * PC::kA, &tmA, kt * elem_per_kt, arow, fb);
-          tma_load_2d_pair(sB + s * PC::kB, &tmB, kt * elem_per_kt, brow, fb);
+          tma_load_2d_pair(sB + s * PC::kB, hf ? &tmBh : &tmB, kt * elem_per_kt, brow, fb);
           ++it;
           if (++s == (uint32_t)S) { s = 0; ph ^= 1u; }
         }
@@ -648,6 +676,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm + (SFST
       bool ok = true;
       for (int t = pair; t < total && ok; t += npairs, ++lt) {
         const uint32_t a = lt % NACC, aph = (lt / NACC) & 1u;
+        const uint32_t idesc = t < g.full_tiles ? g.idesc : g.idesc_half;  // N = 256 or 128
         if (!(ok = mbar_wait_bounded(&acc_empty[a], aph ^ 1u, abort_flag, &g_device_error))) break;
         tc_fence_after();
         const uint32_t tmem_d = tmem_base + a * kPairBN;
@@ -668,14 +697,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm + (SFST
             const uint64_t bd = ((uint64_t)kHiSw << 32) | (blo + 2 * j);
             const uint32_t acc = (kt > 0 || j > 0) ? 1u : 0u;
             if constexpr (KIND == kKindF16 || KIND == kKindF8F6F4) {
-              mma_pair<KIND>(tmem_d, ad, bd, g.idesc, acc);
+              mma_pair<KIND>(tmem_d, ad, bd, idesc, acc);
             } else if constexpr (KIND == kKindMXF8 && !SFST) {
-              mma_pair_bs<KIND>(tmem_d, ad, bd, g.idesc | ((uint32_t)j << 4) | ((uint32_t)j << 29), tmem_sfa, tmem_sfb,
+              mma_pair_bs<KIND>(tmem_d, ad, bd, idesc | ((uint32_t)j << 4) | ((uint32_t)j << 29), tmem_sfa, tmem_sfb,
                                 acc);
             } else if constexpr (SFST) {
               const int at = j * PC::kSfAtoms / 4;  // the MMA's scale atom
               const uint32_t base = tmem_sfa + s * (PC::kSfaCols + PC::kSfbCols);  // the stage's slot
-              mma_pair_bs<KIND>(tmem_d, ad, bd, g.idesc | sf_select<KIND>(j), base + 4 * at,
+              mma_pair_bs<KIND>(tmem_d, ad, bd, idesc | sf_select<KIND>(j), base + 4 * at,
                                 base + PC::kSfaCols + 4 * PC::kSfbGroups * at, acc);
             } else {
               const int at = j * PC::kSfAtoms / 4;
@@ -686,7 +715,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm + (SFST
                   tmem_cp_sf_pair(tmem_sfb + 4 * PC::kSfbGroups * at + 4 * i,
                                   ((uint64_t)kHiSf << 32) | (fblo + (i * PC::kSfAtoms + at) * 32));
               }
-              mma_pair_bs<KIND>(tmem_d, ad, bd, g.idesc | sf_select<KIND>(j), tmem_sfa + 4 * at,
+              mma_pair_bs<KIND>(tmem_d, ad, bd, idesc | sf_select<KIND>(j), tmem_sfa + 4 * at,
                                 tmem_sfb + 4 * PC::kSfbGroups * at, acc);
             }
           }
@@ -749,20 +778,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm + (SFST
     const bool vec_ok = g.c_fp32 ? (g.N % 4 == 0) : (g.N % 8 == 0);
     uint32_t lt = 0;
     for (int t = pair; t < total; t += npairs, ++lt) {
-      int mt, nt;
-      tile_coords(t, g.tiles_m, g.tiles_n, mt, nt);
+      int mt, nt, part;
+      work_coords(t, g.full_tiles, g.tiles_m, g.tiles_n, mt, nt, part);
+      // columns of this warp: 128 of a whole tile, 64 of a half tile (part >= 0)
+      const int width = part >= 0 ? HALF / 2 : HALF;
       const uint32_t a = lt % NACC, aph = (lt / NACC) & 1u;
       if (!mbar_wait_bounded(&acc_full[a], aph, abort_flag, &g_device_error)) break;
       __syncwarp();
       tc_fence_after();
       const int64_t row = (int64_t)mt * 256 + rank * 128 + q * 32 + lane;
-      const int64_t c0 = (int64_t)nt * kPairBN + half * HALF;
+      const int64_t c0 = (int64_t)nt * kPairBN + (part >= 0 ? part * 128 : 0) + half * width;
       const int64_t ncols = g.N - c0;
-      const uint32_t tbase = tmem_base + a * kPairBN + half * HALF + ((uint32_t)(q * 32) << 16);
+      const uint32_t tbase = tmem_base + a * kPairBN + half * width + ((uint32_t)(q * 32) << 16);
       if (!g.c_fp32) {
         uint32_t pk[HALF / 2];
 #pragma unroll
         for (int cc = 0; cc < HALF / 32; ++cc) {
+          if (cc * 32 >= width) break;
           uint32_t v[32];
           tmem_ld32(tbase + (uint32_t)(cc * 32), v);
 #pragma unroll
@@ -787,6 +819,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm + (SFST
           const int32_t y = mt * 256 + (int32_t)rank * 128 + q * 32;
 #pragma unroll
           for (int ch = 0; ch < 2; ++ch) {
+            if (ch * 64 >= width) break;
             if (lane == 0) bulk_wait_group_read0();  // the previous store has read the buffer
             __syncwarp();
 #pragma unroll
@@ -805,25 +838,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm + (SFST
         }
         if (row < g.M && ncols > 0) {
           __nv_bfloat16* out = static_cast<__nv_bfloat16*>(g.c) + row * g.N + c0;
-          if (vec_ok && ncols >= HALF) {
+          const int64_t nc = ncols < width ? ncols : width;
+          if (vec_ok && nc == width) {
 #pragma unroll
-            for (int i = 0; i < HALF / 8; ++i)
+            for (int i = 0; i < HALF / 8; ++i) {
+              if (i * 8 >= width) break;
               reinterpret_cast<uint4*>(out)[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+            }
           } else {
 #pragma unroll
             for (int i = 0; i < HALF / 2; ++i) {
-              if (2 * i < ncols) out[2 * i] = __ushort_as_bfloat16((unsigned short)(pk[i] & 0xFFFFu));
-              if (2 * i + 1 < ncols) out[2 * i + 1] = __ushort_as_bfloat16((unsigned short)(pk[i] >> 16));
+              if (2 * i < nc) out[2 * i] = __ushort_as_bfloat16((unsigned short)(pk[i] & 0xFFFFu));
+              if (2 * i + 1 < nc) out[2 * i + 1] = __ushort_as_bfloat16((unsigned short)(pk[i] >> 16));
             }
           }
         }
         continue;
       }
 #pragma unroll 1
-      for (int cc = 0; cc < HALF / 32; ++cc) {
+      for (int cc = 0; cc < width / 32; ++cc) {
         uint32_t v[32];
         tmem_ld32(tbase + (uint32_t)(cc * 32), v);
-        if (cc == HALF / 32 - 1) {
+        if (cc == width / 32 - 1) {
           tc_fence_before();
           __syncwarp();
           if (lane == 0) {
@@ -872,16 +908,26 @@ lpq_status make_sf_map(CUtensorMap* map, const void* base, int64_t total_atoms, 
 }
 
 template <int KIND, bool kSfbFull, bool SFST = false>
-lpq_status run_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tsa, const CUtensorMap& tsb,
-                    GemmArgs g, bool direct_store, cudaStream_t s) {
+lpq_status run_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tbh, const CUtensorMap& tsa,
+                    const CUtensorMap& tsb, GemmArgs g, bool direct_store, bool whole_tiles, cudaStream_t s) {
   using PC = PairCfg<KIND, kSfbFull, SFST>;
   lpq_status st = set_smem_attr(reinterpret_cast<const void*>(gemm_pair_kernel<KIND, kSfbFull, SFST>), PC::kSmem);
   if (st != LPQ_OK) return st;
   const int sms = device_sms();
   const int64_t tm = (g.M + 255) / 256, tn = (g.N + kPairBN - 1) / kPairBN;
+  if (tm * tn > (int64_t)1 << 29) return set_error(LPQ_ERR_SHAPE, "too many output tiles");
   g.tiles_m = (int)tm;
   g.tiles_n = (int)tn;
-  const int pairs = (int)std::min<int64_t>(tm * tn, sms / 2);
+  // Persistent schedule over work items: whole tiles, and, when the tiles of
+  // the last round fill at most half of the pairs, those tiles as two
+  // 256 x 128 halves each (the round then takes half as long).
+  const int64_t total = tm * tn, P = std::max(1, sms / 2);
+  const int64_t rem = total - ((total - 1) / P) * P;  // tiles in the last round, 1 .. P
+  const bool split = !whole_tiles && 2 * rem <= P;
+  g.full_tiles = (int)(split ? total - rem : total);
+  g.items = (int)(split ? total + rem : total);
+  g.idesc_half = (g.idesc & ~(63u << 17)) | ((uint32_t)(128 >> 3) << 17);
+  const int pairs = (int)std::min<int64_t>(g.items, P);
   // bf16 C leaves through TMA tile stores (32 x 64 boxes) when its row pitch
   // allows a tensor map (N % 8 == 0); otherwise the epilogue stores directly.
   CUtensorMap tc = ta;
@@ -891,7 +937,7 @@ lpq_status run_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensor
     g.c_tma = 1;
   }
   gemm_pair_kernel<KIND, kSfbFull, SFST>
-      <<<2 * pairs, kThreadsGemm + (SFST ? 32 * kSfWarps : 0), PC::kSmem, s>>>(ta, tb, tsa, tsb, tc, g);
+      <<<2 * pairs, kThreadsGemm + (SFST ? 32 * kSfWarps : 0), PC::kSmem, s>>>(ta, tb, tbh, tsa, tsb, tc, g);
   return cuda_check(cudaGetLastError(), "pair gemm launch");
 }
 
@@ -1192,6 +1238,8 @@ lpq_status launch_gemm(const lpq_qview* a, const lpq_qview* b, void* c, int32_t 
   const int nv_bn = (opts && opts->tile_n == 128) ? 128 : 256;
   const bool cp = opts && opts->scale_copies;
   const bool direct = opts && opts->direct_store;
+  const bool whole = opts && opts->whole_tiles;
+  CUtensorMap tbh;  // CTA-pair kernel: B boxes of 64 rows for the half tiles
   if (fa == LPQ_BF16) {
     g.num_k = (int)((k * 2 + kKBytes - 1) / kKBytes);
     if ((st = make_map(&ta, a->codes, true, k, m, k * 2, 64, kBM)) != LPQ_OK) return st;
@@ -1200,8 +1248,9 @@ lpq_status launch_gemm(const lpq_qview* a, const lpq_qview* b, void* c, int32_t 
     if (pair_ok) {
       if ((st = make_map(&ta, a->codes, true, k, m, k * 2, 64, kBM)) != LPQ_OK) return st;
       if ((st = make_map(&tb, b->codes, true, k, n, k * 2, 64, kPairBN / 2)) != LPQ_OK) return st;
+      if ((st = make_map(&tbh, b->codes, true, k, n, k * 2, 64, kPairBN / 4)) != LPQ_OK) return st;
       g.idesc = idesc_dense(1, 1, kPairBN) & ~(31u << 24) | (16u << 24);  // M = 256
-      return run_pair<kKindF16, true>(ta, tb, ta, tb, g, direct, s);
+      return run_pair<kKindF16, true>(ta, tb, tbh, ta, tb, g, direct, whole, s);
     }
     return run<kKindF16, BN, 2>(ta, tb, g, s);
   }
@@ -1214,8 +1263,9 @@ lpq_status launch_gemm(const lpq_qview* a, const lpq_qview* b, void* c, int32_t 
     g.alpha_b = b->tensor_scale;
     if (pair_ok) {
       if ((st = make_map(&tb, b->codes, false, k, n, k, 128, kPairBN / 2)) != LPQ_OK) return st;
+      if ((st = make_map(&tbh, b->codes, false, k, n, k, 128, kPairBN / 4)) != LPQ_OK) return st;
       g.idesc = (g.idesc & ~(31u << 24)) | (16u << 24);  // M = 256
-      return run_pair<kKindF8F6F4, true>(ta, tb, ta, tb, g, direct, s);
+      return run_pair<kKindF8F6F4, true>(ta, tb, tbh, ta, tb, g, direct, whole, s);
     }
     return run<kKindF8F6F4, BN, 2>(ta, tb, g, s);
   }
@@ -1236,11 +1286,12 @@ lpq_status launch_gemm(const lpq_qview* a, const lpq_qview* b, void* c, int32_t 
     if (pair_ok) {
       CUtensorMap tsa, tsb;
       if ((st = make_map(&tb, b->codes, false, k, n, k, 128, kPairBN / 2)) != LPQ_OK) return st;
+      if ((st = make_map(&tbh, b->codes, false, k, n, k, 128, kPairBN / 4)) != LPQ_OK) return st;
       if ((st = make_sf_map(&tsa, g.sfa, sf_row_groups(m) * g.sfa_kt, 1)) != LPQ_OK) return st;
       if ((st = make_sf_map(&tsb, g.sfb, g.sfb_groups * g.sfb_kt, 1)) != LPQ_OK) return st;
       g.idesc = (g.idesc & ~(31u << 24)) | (16u << 24);
-      if (cp) return run_pair<kKindMXF8, true>(ta, tb, tsa, tsb, g, direct, s);
-      return run_pair<kKindMXF8, true, true>(ta, tb, tsa, tsb, g, direct, s);
+      if (cp) return run_pair<kKindMXF8, true>(ta, tb, tbh, tsa, tsb, g, direct, whole, s);
+      return run_pair<kKindMXF8, true, true>(ta, tb, tbh, tsa, tsb, g, direct, whole, s);
     }
     if (nv_bn == 128) {
       if ((st = make_map(&tb, b->codes, false, k, n, k, 128, 128)) != LPQ_OK) return st;
@@ -1267,11 +1318,12 @@ lpq_status launch_gemm(const lpq_qview* a, const lpq_qview* b, void* c, int32_t 
     if (pair_ok) {
       CUtensorMap tsa, tsb;
       if ((st = make_map(&tb, b->codes, false, k / 2, n, k / 2, 128, kPairBN / 2)) != LPQ_OK) return st;
+      if ((st = make_map(&tbh, b->codes, false, k / 2, n, k / 2, 128, kPairBN / 4)) != LPQ_OK) return st;
       if ((st = make_sf_map(&tsa, g.sfa, sf_row_groups(m) * g.sfa_kt, 2)) != LPQ_OK) return st;
       if ((st = make_sf_map(&tsb, g.sfb, g.sfb_groups * g.sfb_kt, 2)) != LPQ_OK) return st;
       g.idesc = (g.idesc & ~(31u << 24)) | (16u << 24);
-      if (cp) return run_pair<kKindMXF4, true>(ta, tb, tsa, tsb, g, direct, s);
-      return run_pair<kKindMXF4, true, true>(ta, tb, tsa, tsb, g, direct, s);
+      if (cp) return run_pair<kKindMXF4, true>(ta, tb, tbh, tsa, tsb, g, direct, whole, s);
+      return run_pair<kKindMXF4, true, true>(ta, tb, tbh, tsa, tsb, g, direct, whole, s);
     }
     if (nv_bn == 128) {
       if ((st = make_map(&tb, b->codes, false, k / 2, n, k / 2, 128, 128)) != LPQ_OK) return st;
@@ -1297,11 +1349,12 @@ lpq_status launch_gemm(const lpq_qview* a, const lpq_qview* b, void* c, int32_t 
     if (pair_ok) {
       CUtensorMap tsa, tsb;
       if ((st = make_map(&tb, b->codes, false, k / 2, n, k / 2, 128, kPairBN / 2)) != LPQ_OK) return st;
+      if ((st = make_map(&tbh, b->codes, false, k / 2, n, k / 2, 128, kPairBN / 4)) != LPQ_OK) return st;
       if ((st = make_sf_map(&tsa, g.sfa, sf_row_groups(m) * g.sfa_kt, 4)) != LPQ_OK) return st;
       if ((st = make_sf_map(&tsb, g.sfb, g.sfb_groups * g.sfb_kt, 4)) != LPQ_OK) return st;
       g.idesc = (g.idesc & ~(31u << 24)) | (16u << 24);
-      if (cp) return run_pair<kKindNVF4, true>(ta, tb, tsa, tsb, g, direct, s);
-      return run_pair<kKindNVF4, true, true>(ta, tb, tsa, tsb, g, direct, s);
+      if (cp) return run_pair<kKindNVF4, true>(ta, tb, tbh, tsa, tsb, g, direct, whole, s);
+      return run_pair<kKindNVF4, true, true>(ta, tb, tbh, tsa, tsb, g, direct, whole, s);
     }
     if (nv_bn == 128) {
       if ((st = make_map(&tb, b->codes, false, k / 2, n, k / 2, 128, 128)) != LPQ_OK) return st;

@@ -55,7 +55,7 @@ class DelayedStateC(ctypes.Structure):
 class GemmOpts(ctypes.Structure):
     """Kernel-path options of lpq_gemm_ex (all zero: the default path)."""
     _fields_ = [("single_cta", ctypes.c_int32), ("tile_n", ctypes.c_int32), ("scale_copies", ctypes.c_int32),
-                ("direct_store", ctypes.c_int32), ("reserved", ctypes.c_int32 * 4)]
+                ("direct_store", ctypes.c_int32), ("whole_tiles", ctypes.c_int32), ("reserved", ctypes.c_int32 * 3)]
 
 
 # Named kernel paths of the GEMM (every one computes the same result).
@@ -63,6 +63,7 @@ GEMM_PATHS = {
     "default": GemmOpts(),
     "pair": GemmOpts(),                               # CTA pairs where m >= 256 (the default)
     "pair_direct": GemmOpts(direct_store=1),          # CTA pairs, bf16 C stored from registers
+    "pair_whole": GemmOpts(whole_tiles=1),            # CTA pairs, no 256 x 128 halves in the last round
     "single": GemmOpts(single_cta=1),                 # one CTA per 128 x 256 tile
     "single_cp": GemmOpts(single_cta=1, scale_copies=1),  # scale factors copied by the MMA thread
     "single_bn128": GemmOpts(single_cta=1, tile_n=128),   # one CTA per 128 x 128 tile

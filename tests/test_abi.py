@@ -174,7 +174,8 @@ def test_gemm_options_validation():
     v = lambda rows, cols: lpq.QView(16, 16, 16, 16, rows, cols, lpq.MXFP8, lpq.SF_GEMM, 0, 0)
     a, b = v(128, 256), v(64, 256)
     bad = [lpq.GemmOpts(single_cta=2), lpq.GemmOpts(tile_n=64), lpq.GemmOpts(scale_copies=-1),
-           lpq.GemmOpts(direct_store=3), lpq.GemmOpts(reserved=(ctypes.c_int32 * 4)(0, 1, 0, 0))]
+           lpq.GemmOpts(direct_store=3), lpq.GemmOpts(whole_tiles=2),
+           lpq.GemmOpts(reserved=(ctypes.c_int32 * 3)(0, 1, 0))]
     for opts in bad:
         assert L.lpq_gemm_ex(0, ctypes.byref(a), ctypes.byref(b), 16, 0, 128, 64, 256, ctypes.byref(opts),
                              None) == lpq.ERR_INVALID_ARG

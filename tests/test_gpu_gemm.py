@@ -34,7 +34,7 @@ def check(a, b, M, N, K, out_fp32, layout=lpq.FPROP, path=None):
     assert nbad == 0, f"{nbad} elements outside the gate (worst {worst:.3g}x)"
 
 
-@pytest.mark.parametrize("path", ["single", "pair", "pair_direct", "single_cp", "single_bn128"])
+@pytest.mark.parametrize("path", ["single", "pair", "pair_whole", "pair_direct", "single_cp", "single_bn128"])
 @pytest.mark.parametrize("out_fp32", [True, False])
 @pytest.mark.parametrize("shape", SHAPES)
 @pytest.mark.parametrize("fmts", [(lpq.BF16, lpq.BF16), (lpq.FP8_E4M3, lpq.FP8_E4M3), (lpq.FP8_E5M2, lpq.FP8_E4M3),
@@ -46,7 +46,9 @@ def test_gemm_parity(fmts, shape, out_fp32, path):
     TMEM by scale warps, or copied by the MMA thread: single_cp), one CTA per
     128 x 128 tile with two accumulators (block-scaled kinds: single_bn128), and
     CTA pairs (cta_group::2) per 256 x 256 tile, whose bf16 output leaves
-    through TMA tile stores (pair) or direct stores (pair_direct)."""
+    through TMA tile stores (pair) or direct stores (pair_direct).  These
+    shapes have fewer tiles than half the CTA pairs, so pair and pair_direct
+    run every tile as two 256 x 128 halves; pair_whole keeps whole tiles."""
     if path == "single_cp" and fmts[0] not in (lpq.NVFP4, lpq.MXFP4, lpq.MXFP8, lpq.MXFP8_E5M2):
         pytest.skip("scale-copy variant exists for the block-scaled kinds only")
     if path == "single_bn128" and fmts[0] not in (lpq.NVFP4, lpq.MXFP8, lpq.MXFP8_E5M2, lpq.MXFP4):
@@ -232,3 +234,32 @@ def test_pair_gemm_ragged_n_direct_stores(fmts):
     a, b = quantize_pair(*fmts, M, K, N, seed=11)
     for out_fp32 in (False, True):
         check(a, b, M, N, K, out_fp32, path="pair")
+
+
+@pytest.mark.parametrize("fmts", [(lpq.BF16, lpq.BF16), (lpq.FP8_E4M3, lpq.FP8_E4M3), (lpq.MXFP8, lpq.MXFP8),
+                                  (lpq.MXFP4, lpq.MXFP4), (lpq.NVFP4, lpq.NVFP4_2D)])
+def test_pair_gemm_whole_and_half_tiles_mixed(fmts):
+    """Two tiles more than there are CTA pairs (M = 512: two tile rows): the
+    pair kernel runs one round of whole 256 x 256 tiles and splits the two
+    tiles of the last round (the last tile column) into four 256 x 128 halves
+    (N = 128 MMAs on 64 B rows per CTA, with the half's one group of B scale
+    atoms); whole_tiles = 1 runs them as whole tiles.  Every output of the last
+    tile column and 4096 others (seed 0) against the oracle, bf16 and FP32
+    outputs, both paths."""
+    pairs = torch.cuda.get_device_properties(0).multi_processor_count // 2
+    M, K, N = 512, 256, (pairs + 2) // 2 * 256 + (128 if pairs % 2 else 0)
+    a, b = quantize_pair(*fmts, M, K, N, seed=5)
+    n0 = (N - 1) // 256 * 256
+    rng = np.random.default_rng(0)
+    last = np.array([(m, n) for m in range(M) for n in range(n0, N)])
+    rand = np.stack([rng.integers(0, M, 4096), rng.integers(0, N, 4096)], 1)
+    pairs_mn = np.concatenate([last, rand]).astype(np.int64)
+    ref, bound = o.gemm(oracle_operand(a), oracle_operand(b), M, N, K, pairs_mn)
+    rows, cols = torch.from_numpy(pairs_mn[:, 0]).cuda(), torch.from_numpy(pairs_mn[:, 1]).cuda()
+    for out_fp32 in (False, True):
+        for path in ("pair", "pair_whole"):
+            c = lpq.gemm(lpq.FPROP, a, b, out_fp32=out_fp32, path=path)
+            torch.cuda.synchronize()
+            assert lpq.device_status() == 0
+            nbad, worst = gemm_gate(c[rows, cols], ref, bound, not out_fp32)
+            assert nbad == 0, f"{path} fp32={out_fp32}: {nbad} outside the gate (worst {worst:.3g}x)"
