@@ -494,19 +494,19 @@ lpq_status run(const CUtensorMap& ta, const CUtensorMap& tb, GemmArgs g, cudaStr
 // CTA's full barrier; MMA completion is multicast to both CTAs.  For the
 // block-scaled kinds each CTA also loads the scale atoms of its A rows and of
 // all 256 B rows of the tile (each CTA's accumulator spans every column, so
-// each TMEM needs every column's scales; kSfbFull = false, each CTA holding
-// only its own 128 B rows, does not match the pair MMA).  With scale warps
+// each TMEM needs every column's scales: with only its own 128 B rows' scales
+// in each CTA the results fail the parity tests).  With scale warps
 // (SFST, the default) each CTA's four scale warps write them into the
 // stage's TMEM slot with tcgen05.st and report to the even CTA's full
 // barrier; otherwise the pair copies (tcgen05.cp.cta_group::2) move them.
 constexpr int kPairBN = 256;
 
-template <int KIND, bool kSfbFull, bool SFST = false>
+template <int KIND, bool SFST = false>
 struct PairCfg {
   static constexpr int kSfAtoms = sf_atoms_per_step(KIND);
   static constexpr int kA = kBM * kKBytes;
   static constexpr int kB = (kPairBN / 2) * kKBytes;
-  static constexpr int kSfbGroups = kSfbFull ? 2 : 1;
+  static constexpr int kSfbGroups = 2;  // B scale atoms of both 128-row halves of the tile
   static constexpr int kSfa = kSfAtoms * 512;
   static constexpr int kSfb = kSfAtoms * 512 * kSfbGroups;
   static constexpr int kStage = kA + kB + kSfa + kSfb;
@@ -549,13 +549,13 @@ __device__ __forceinline__ void tmem_cp_sf_pair(uint32_t taddr, uint64_t sdesc) 
   asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
 }
 
-template <int KIND, bool kSfbFull, bool SFST>
+template <int KIND, bool SFST>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm + (SFST ? 32 * kSfWarps : 0))
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmBh, const __grid_constant__ CUtensorMap tmSfa,
                      const __grid_constant__ CUtensorMap tmSfb, const __grid_constant__ CUtensorMap tmC,
                      const GemmArgs g) {
-  using PC = PairCfg<KIND, kSfbFull, SFST>;
+  using PC = PairCfg<KIND, SFST>;
   constexpr int S = PC::kStages, NACC = PC::kNacc;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -648,7 +648,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm + (SFST
 #pragma unroll
             for (int i = 0; i < PC::kSfbGroups; ++i) {
               if (i >= ngb) break;
-              int64_t gb = hf ? (int64_t)nt * 2 + part : kSfbFull ? (int64_t)nt * 2 + i : (int64_t)nt * 2 + rank;
+              int64_t gb = hf ? (int64_t)nt * 2 + part : (int64_t)nt * 2 + i;
               if (gb >= g.sfb_groups) gb = g.sfb_groups - 1;
               const int32_t yb = (int32_t)(gb * g.sfb_kt + kt * PC::kSfAtoms);
               if constexpr (SFST) tma_load_2d(sSfb + s * PC::kSfb + i * PC::kSfAtoms * 512, &tmSfb, 0, yb, &sfd[s]);
@@ -907,11 +907,11 @@ lpq_status make_sf_map(CUtensorMap* map, const void* base, int64_t total_atoms, 
   return LPQ_OK;
 }
 
-template <int KIND, bool kSfbFull, bool SFST = false>
+template <int KIND, bool SFST = false>
 lpq_status run_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tbh, const CUtensorMap& tsa,
                     const CUtensorMap& tsb, GemmArgs g, bool direct_store, bool whole_tiles, cudaStream_t s) {
-  using PC = PairCfg<KIND, kSfbFull, SFST>;
-  lpq_status st = set_smem_attr(reinterpret_cast<const void*>(gemm_pair_kernel<KIND, kSfbFull, SFST>), PC::kSmem);
+  using PC = PairCfg<KIND, SFST>;
+  lpq_status st = set_smem_attr(reinterpret_cast<const void*>(gemm_pair_kernel<KIND, SFST>), PC::kSmem);
   if (st != LPQ_OK) return st;
   const int sms = device_sms();
   const int64_t tm = (g.M + 255) / 256, tn = (g.N + kPairBN - 1) / kPairBN;
@@ -936,7 +936,7 @@ lpq_status run_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensor
     if ((st = make_map(&tc, g.c, true, g.N, g.M, g.N * 2, 64, 32)) != LPQ_OK) return st;
     g.c_tma = 1;
   }
-  gemm_pair_kernel<KIND, kSfbFull, SFST>
+  gemm_pair_kernel<KIND, SFST>
       <<<2 * pairs, kThreadsGemm + (SFST ? 32 * kSfWarps : 0), PC::kSmem, s>>>(ta, tb, tbh, tsa, tsb, tc, g);
   return cuda_check(cudaGetLastError(), "pair gemm launch");
 }
@@ -1250,7 +1250,7 @@ lpq_status launch_gemm(const lpq_qview* a, const lpq_qview* b, void* c, int32_t 
       if ((st = make_map(&tb, b->codes, true, k, n, k * 2, 64, kPairBN / 2)) != LPQ_OK) return st;
       if ((st = make_map(&tbh, b->codes, true, k, n, k * 2, 64, kPairBN / 4)) != LPQ_OK) return st;
       g.idesc = idesc_dense(1, 1, kPairBN) & ~(31u << 24) | (16u << 24);  // M = 256
-      return run_pair<kKindF16, true>(ta, tb, tbh, ta, tb, g, direct, whole, s);
+      return run_pair<kKindF16>(ta, tb, tbh, ta, tb, g, direct, whole, s);
     }
     return run<kKindF16, BN, 2>(ta, tb, g, s);
   }
@@ -1265,7 +1265,7 @@ lpq_status launch_gemm(const lpq_qview* a, const lpq_qview* b, void* c, int32_t 
       if ((st = make_map(&tb, b->codes, false, k, n, k, 128, kPairBN / 2)) != LPQ_OK) return st;
       if ((st = make_map(&tbh, b->codes, false, k, n, k, 128, kPairBN / 4)) != LPQ_OK) return st;
       g.idesc = (g.idesc & ~(31u << 24)) | (16u << 24);  // M = 256
-      return run_pair<kKindF8F6F4, true>(ta, tb, tbh, ta, tb, g, direct, whole, s);
+      return run_pair<kKindF8F6F4>(ta, tb, tbh, ta, tb, g, direct, whole, s);
     }
     return run<kKindF8F6F4, BN, 2>(ta, tb, g, s);
   }
@@ -1290,8 +1290,8 @@ lpq_status launch_gemm(const lpq_qview* a, const lpq_qview* b, void* c, int32_t 
       if ((st = make_sf_map(&tsa, g.sfa, sf_row_groups(m) * g.sfa_kt, 1)) != LPQ_OK) return st;
       if ((st = make_sf_map(&tsb, g.sfb, g.sfb_groups * g.sfb_kt, 1)) != LPQ_OK) return st;
       g.idesc = (g.idesc & ~(31u << 24)) | (16u << 24);
-      if (cp) return run_pair<kKindMXF8, true>(ta, tb, tbh, tsa, tsb, g, direct, whole, s);
-      return run_pair<kKindMXF8, true, true>(ta, tb, tbh, tsa, tsb, g, direct, whole, s);
+      if (cp) return run_pair<kKindMXF8>(ta, tb, tbh, tsa, tsb, g, direct, whole, s);
+      return run_pair<kKindMXF8, true>(ta, tb, tbh, tsa, tsb, g, direct, whole, s);
     }
     if (nv_bn == 128) {
       if ((st = make_map(&tb, b->codes, false, k, n, k, 128, 128)) != LPQ_OK) return st;
@@ -1322,8 +1322,8 @@ lpq_status launch_gemm(const lpq_qview* a, const lpq_qview* b, void* c, int32_t 
       if ((st = make_sf_map(&tsa, g.sfa, sf_row_groups(m) * g.sfa_kt, 2)) != LPQ_OK) return st;
       if ((st = make_sf_map(&tsb, g.sfb, g.sfb_groups * g.sfb_kt, 2)) != LPQ_OK) return st;
       g.idesc = (g.idesc & ~(31u << 24)) | (16u << 24);
-      if (cp) return run_pair<kKindMXF4, true>(ta, tb, tbh, tsa, tsb, g, direct, whole, s);
-      return run_pair<kKindMXF4, true, true>(ta, tb, tbh, tsa, tsb, g, direct, whole, s);
+      if (cp) return run_pair<kKindMXF4>(ta, tb, tbh, tsa, tsb, g, direct, whole, s);
+      return run_pair<kKindMXF4, true>(ta, tb, tbh, tsa, tsb, g, direct, whole, s);
     }
     if (nv_bn == 128) {
       if ((st = make_map(&tb, b->codes, false, k / 2, n, k / 2, 128, 128)) != LPQ_OK) return st;
@@ -1353,8 +1353,8 @@ lpq_status launch_gemm(const lpq_qview* a, const lpq_qview* b, void* c, int32_t 
       if ((st = make_sf_map(&tsa, g.sfa, sf_row_groups(m) * g.sfa_kt, 4)) != LPQ_OK) return st;
       if ((st = make_sf_map(&tsb, g.sfb, g.sfb_groups * g.sfb_kt, 4)) != LPQ_OK) return st;
       g.idesc = (g.idesc & ~(31u << 24)) | (16u << 24);
-      if (cp) return run_pair<kKindNVF4, true>(ta, tb, tbh, tsa, tsb, g, direct, whole, s);
-      return run_pair<kKindNVF4, true, true>(ta, tb, tbh, tsa, tsb, g, direct, whole, s);
+      if (cp) return run_pair<kKindNVF4>(ta, tb, tbh, tsa, tsb, g, direct, whole, s);
+      return run_pair<kKindNVF4, true>(ta, tb, tbh, tsa, tsb, g, direct, whole, s);
     }
     if (nv_bn == 128) {
       if ((st = make_map(&tb, b->codes, false, k / 2, n, k / 2, 128, 128)) != LPQ_OK) return st;
@@ -1510,7 +1510,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1) mma_peak_pai
   // MODE 8: each k-step's four 256 x 256 MMAs issued as eight 256 x 128 MMAs
   // (two column halves, each half's B rows 64 per CTA) into two TMEM regions.
   constexpr bool kHalves = MODE == 8;
-  using PC = PairCfg<KIND, true, false>;
+  using PC = PairCfg<KIND, false>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
@@ -1589,7 +1589,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1) mma_peak_pai
 
 template <int KIND, int MODE>
 lpq_status run_peak_pair(int iters, uint32_t idesc, cudaStream_t s) {
-  using PC = PairCfg<KIND, true, false>;
+  using PC = PairCfg<KIND, false>;
   const int smem = PC::kA + PC::kB + PC::kSfa + PC::kSfb + 1024 + 256;
   lpq_status st = set_smem_attr(reinterpret_cast<const void*>(mma_peak_pair_kernel<KIND, MODE>), smem);
   if (st != LPQ_OK) return st;
