@@ -490,7 +490,8 @@ lpq_status run(const CUtensorMap& ta, const CUtensorMap& tb, GemmArgs g, cudaStr
 // 256 x 256 output tile: each CTA loads its own 128 rows of A and its own 128
 // rows of B (each SM streams half the B bytes of the single-CTA kernel), the
 // even CTA issues the pair MMAs, and each CTA's TMEM holds the accumulator
-// rows of its half.  Every A/B load is a TMA tile load that signals the even
+// rows of its half.  A short last round runs its tiles as 256 x 128 halves
+// (64 B rows per CTA, N = 128 MMAs; work_coords).  Every A/B load is a TMA tile load that signals the even
 // CTA's full barrier; MMA completion is multicast to both CTAs.  For the
 // block-scaled kinds each CTA also loads the scale atoms of its A rows and of
 // all 256 B rows of the tile (each CTA's accumulator spans every column, so
@@ -812,9 +813,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsGemm + (SFST
           if (leader) mbar_arrive(&acc_empty[a]); else mbar_arrive_remote_relaxed(acc_empty_leader + 8 * a);
         }
         if (g.c_tma) {
-          // The warp's 32 rows x 128 columns leave as two TMA stores of 32 x 64
-          // tiles staged in shared memory (128-byte swizzle: 16-byte chunk i of
-          // row r at chunk position i ^ (r & 7)); the stores clip at M and N.
+          // The warp's 32 rows x 128 columns (64 of a half tile) leave as TMA
+          // stores of 32 x 64 tiles staged in shared memory (128-byte swizzle:
+          // 16-byte chunk i of row r at chunk position i ^ (r & 7)); the
+          // stores clip at M and N.
           uint8_t* stg = stage_c + (warp - 2) * PC::kStgWarp;
           const int32_t y = mt * 256 + (int32_t)rank * 128 + q * 32;
 #pragma unroll
