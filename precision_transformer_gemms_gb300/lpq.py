@@ -64,6 +64,7 @@ GEMM_PATHS = {
     "pair": GemmOpts(),                               # CTA pairs where m >= 256 (the default)
     "pair_direct": GemmOpts(direct_store=1),          # CTA pairs, bf16 C stored from registers
     "pair_whole": GemmOpts(whole_tiles=1),            # CTA pairs, no 256 x 128 halves in the last round
+    "pair_cp": GemmOpts(scale_copies=1),              # CTA pairs, scale factors copied by the MMA thread
     "single": GemmOpts(single_cta=1),                 # one CTA per 128 x 256 tile
     "single_cp": GemmOpts(single_cta=1, scale_copies=1),  # scale factors copied by the MMA thread
     "single_bn128": GemmOpts(single_cta=1, tile_n=128),   # one CTA per 128 x 128 tile

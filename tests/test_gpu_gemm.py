@@ -34,7 +34,8 @@ def check(a, b, M, N, K, out_fp32, layout=lpq.FPROP, path=None):
     assert nbad == 0, f"{nbad} elements outside the gate (worst {worst:.3g}x)"
 
 
-@pytest.mark.parametrize("path", ["single", "pair", "pair_whole", "pair_direct", "single_cp", "single_bn128"])
+@pytest.mark.parametrize("path", ["single", "pair", "pair_whole", "pair_direct", "pair_cp", "single_cp",
+                                  "single_bn128"])
 @pytest.mark.parametrize("out_fp32", [True, False])
 @pytest.mark.parametrize("shape", SHAPES)
 @pytest.mark.parametrize("fmts", [(lpq.BF16, lpq.BF16), (lpq.FP8_E4M3, lpq.FP8_E4M3), (lpq.FP8_E5M2, lpq.FP8_E4M3),
@@ -43,13 +44,13 @@ def check(a, b, M, N, K, out_fp32, layout=lpq.FPROP, path=None):
                                   (lpq.NVFP4, lpq.NVFP4), (lpq.NVFP4, lpq.NVFP4_2D)])
 def test_gemm_parity(fmts, shape, out_fp32, path):
     """Every kernel path: one CTA per 128 x 256 tile (block scales stored into
-    TMEM by scale warps, or copied by the MMA thread: single_cp), one CTA per
+    TMEM by scale warps, or copied by the MMA thread: single_cp, pair_cp), one CTA per
     128 x 128 tile with two accumulators (block-scaled kinds: single_bn128), and
     CTA pairs (cta_group::2) per 256 x 256 tile, whose bf16 output leaves
     through TMA tile stores (pair) or direct stores (pair_direct).  These
     shapes have fewer tiles than half the CTA pairs, so pair and pair_direct
     run every tile as two 256 x 128 halves; pair_whole keeps whole tiles."""
-    if path == "single_cp" and fmts[0] not in (lpq.NVFP4, lpq.MXFP4, lpq.MXFP8, lpq.MXFP8_E5M2):
+    if path in ("single_cp", "pair_cp") and fmts[0] not in (lpq.NVFP4, lpq.MXFP4, lpq.MXFP8, lpq.MXFP8_E5M2):
         pytest.skip("scale-copy variant exists for the block-scaled kinds only")
     if path == "single_bn128" and fmts[0] not in (lpq.NVFP4, lpq.MXFP8, lpq.MXFP8_E5M2, lpq.MXFP4):
         pytest.skip("128-wide tiles exist for the block-scaled kinds only")
@@ -257,7 +258,7 @@ def test_pair_gemm_whole_and_half_tiles_mixed(fmts):
     ref, bound = o.gemm(oracle_operand(a), oracle_operand(b), M, N, K, pairs_mn)
     rows, cols = torch.from_numpy(pairs_mn[:, 0]).cuda(), torch.from_numpy(pairs_mn[:, 1]).cuda()
     for out_fp32 in (False, True):
-        for path in ("pair", "pair_whole"):
+        for path in ("pair", "pair_whole") + (("pair_cp",) if fmts[0] in (lpq.MXFP8, lpq.MXFP4, lpq.NVFP4) else ()):
             c = lpq.gemm(lpq.FPROP, a, b, out_fp32=out_fp32, path=path)
             torch.cuda.synchronize()
             assert lpq.device_status() == 0
