@@ -68,6 +68,7 @@ GEMM_PATHS = {
     "single": GemmOpts(single_cta=1),                 # one CTA per 128 x 256 tile
     "single_cp": GemmOpts(single_cta=1, scale_copies=1),  # scale factors copied by the MMA thread
     "single_bn128": GemmOpts(single_cta=1, tile_n=128),   # one CTA per 128 x 128 tile
+    "single_bn128_cp": GemmOpts(single_cta=1, tile_n=128, scale_copies=1),  # the same, scales copied
 }
 
 

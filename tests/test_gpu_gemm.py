@@ -35,7 +35,7 @@ def check(a, b, M, N, K, out_fp32, layout=lpq.FPROP, path=None):
 
 
 @pytest.mark.parametrize("path", ["single", "pair", "pair_whole", "pair_direct", "pair_cp", "single_cp",
-                                  "single_bn128"])
+                                  "single_bn128", "single_bn128_cp"])
 @pytest.mark.parametrize("out_fp32", [True, False])
 @pytest.mark.parametrize("shape", SHAPES)
 @pytest.mark.parametrize("fmts", [(lpq.BF16, lpq.BF16), (lpq.FP8_E4M3, lpq.FP8_E4M3), (lpq.FP8_E5M2, lpq.FP8_E4M3),
@@ -52,7 +52,8 @@ def test_gemm_parity(fmts, shape, out_fp32, path):
     run every tile as two 256 x 128 halves; pair_whole keeps whole tiles."""
     if path in ("single_cp", "pair_cp") and fmts[0] not in (lpq.NVFP4, lpq.MXFP4, lpq.MXFP8, lpq.MXFP8_E5M2):
         pytest.skip("scale-copy variant exists for the block-scaled kinds only")
-    if path == "single_bn128" and fmts[0] not in (lpq.NVFP4, lpq.MXFP8, lpq.MXFP8_E5M2, lpq.MXFP4):
+    if path in ("single_bn128", "single_bn128_cp") and fmts[0] not in (lpq.NVFP4, lpq.MXFP8, lpq.MXFP8_E5M2,
+                                                                      lpq.MXFP4):
         pytest.skip("128-wide tiles exist for the block-scaled kinds only")
     M, K, N = shape
     if fmts[1] == lpq.NVFP4_2D and N % 16:
