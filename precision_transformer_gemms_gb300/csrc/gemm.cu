@@ -965,30 +965,16 @@ struct BlockArgs {
 constexpr int kBlkBN = 128;
 constexpr int kBlkStages = 6;
 constexpr int kBlkBufs = 4;   // TMEM partial buffers (4 x 128 columns): the MMA warp runs up to 3 slices ahead
-constexpr int kBlkAhead = 2;  // slices ahead that the epilogue fetches its factors
 constexpr int kBlkStage = kBM * kKBytes + kBlkBN * kKBytes;
 constexpr int kBlkEpiWarps = 8;  // two per TMEM lane quarter, 64 columns each
-constexpr int kBlkSbRing = kBlkAhead + 1;  // per-warp ring of 1x128 B factors (64 per slice)
-constexpr int kBlkSmem = kBlkStages * kBlkStage + 1024 + 512 + kBlkEpiWarps * kBlkSbRing * 64 * 4;
-constexpr int kBlkThreads = 64 + 32 * kBlkEpiWarps;
-
-// Factor of slice kt for this thread's row (1x128 A: one per row; 128x128: one
-// per 128-row block) and the two 1x128 B factors of its lane (columns
-// 2 lane, 2 lane + 1 of the warp's 64); zeros past the matrix.
-__device__ __forceinline__ float blk_a_factor(const BlockArgs& g, int64_t KB, int64_t row, int mt, int kt) {
-  if (kt >= g.num_k) return 0.f;
-  if (g.a_rows == 1) return row < g.M ? g.sa[(int64_t)kt * g.M + row] : 0.f;
-  return g.sa[(int64_t)mt * KB + kt];
-}
-__device__ __forceinline__ float2 blk_b_factors(const BlockArgs& g, int64_t KB, int64_t ncol, int nt, int kt) {
-  if (kt >= g.num_k) return make_float2(0.f, 0.f);
-  if (g.b_rows == 1) {
-    const float* p = g.sb + (int64_t)kt * g.N;
-    return make_float2(ncol < g.N ? p[ncol] : 0.f, ncol + 1 < g.N ? p[ncol + 1] : 0.f);
-  }
-  const float f = g.sb[(int64_t)(nt * kBlkBN / 128) * KB + kt];
-  return make_float2(f, f);
-}
+// Shared-memory ring of the block factors of the slices in flight, filled by
+// the factor warp: per slice the tile's 128 A factors (one per row) and 128 B
+// factors (one per column).
+constexpr int kBlkFacSlots = 8;
+constexpr int kBlkFacSlot = 2 * 128;
+constexpr int kBlkSmem = kBlkStages * kBlkStage + 1024 + 512 + kBlkFacSlots * kBlkFacSlot * 4;
+constexpr int kBlkFacWarp = 2 + kBlkEpiWarps;  // the last warp
+constexpr int kBlkThreads = 32 * (kBlkFacWarp + 1);
 
 __global__ void __launch_bounds__(kBlkThreads, 1)
     block_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -998,12 +984,14 @@ __global__ void __launch_bounds__(kBlkThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
   uint8_t* sB = sA + S * kBM * kKBytes;
-  float* s_sb = reinterpret_cast<float*>(sB + S * BN * kKBytes);  // [warp][ring][64] 1x128 B factors
-  uint64_t* full = reinterpret_cast<uint64_t*>(s_sb + kBlkEpiWarps * kBlkSbRing * 64);
+  float* s_fac = reinterpret_cast<float*>(sB + S * BN * kKBytes);  // [kBlkFacSlots][128 A, 128 B factors]
+  uint64_t* full = reinterpret_cast<uint64_t*>(s_fac + kBlkFacSlots * kBlkFacSlot);
   uint64_t* empty = full + S;
   uint64_t* acc_full = empty + S;   // [NB]
   uint64_t* acc_empty = acc_full + NB;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + NB);
+  uint64_t* fac_full = acc_empty + NB;  // [kBlkFacSlots]: the slot's factor copies landed
+  uint64_t* fac_empty = fac_full + kBlkFacSlots;  // the epilogue warps are done with the slot
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(fac_empty + kBlkFacSlots);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1017,6 +1005,10 @@ __global__ void __launch_bounds__(kBlkThreads, 1)
     for (int a = 0; a < NB; ++a) {
       mbar_init(&acc_full[a], 1);
       mbar_init(&acc_empty[a], kBlkEpiWarps);
+    }
+    for (int f = 0; f < kBlkFacSlots; ++f) {
+      mbar_init(&fac_full[f], 32);  // one arrival per lane of the factor warp, when its copies land
+      mbar_init(&fac_empty[f], kBlkEpiWarps);
     }
     *abort_flag = 0;
     fence_barrier_init();
@@ -1072,15 +1064,43 @@ __global__ void __launch_bounds__(kBlkThreads, 1)
         }
       }
     }
+  } else if (warp == kBlkFacWarp) {
+    // Factor warp: for every slice, the tile's 128 A factors (1x128: its rows';
+    // 128x128: the block's, repeated) and 128 B factors (1x128: its columns';
+    // 128x128: the block's, repeated) into the slice's ring slot with cp.async,
+    // zeros past the matrix.  Each lane's copies arrive on the slot's full
+    // barrier when they land, so the warp never waits for a load; it runs up to
+    // kBlkFacSlots slices ahead of the epilogue.
+    uint32_t slice = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+      int mt, nt;
+      tile_coords(t, g.tiles_m, g.tiles_n, mt, nt);
+      for (int kt = 0; kt < g.num_k; ++kt, ++slice) {
+        const uint32_t f = slice % kBlkFacSlots, fph = (slice / kBlkFacSlots) & 1u;
+        if (!(ok = mbar_wait_bounded(&fac_empty[f], fph ^ 1u, abort_flag, &g_device_error))) break;
+        float* slot = s_fac + f * kBlkFacSlot;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int j = 4 * lane + i;
+          const int64_t row = (int64_t)mt * kBM + j, col = (int64_t)nt * BN + j;
+          const bool va = g.a_rows != 1 || row < g.M, vb = g.b_rows != 1 || col < g.N;
+          const float* pa = g.a_rows == 1 ? g.sa + (va ? (int64_t)kt * g.M + row : 0) : g.sa + (int64_t)mt * KB + kt;
+          const float* pb = g.b_rows == 1 ? g.sb + (vb ? (int64_t)kt * g.N + col : 0)
+                                          : g.sb + (int64_t)(nt * BN / 128) * KB + kt;
+          cp_async4(slot + j, pa, va);
+          cp_async4(slot + 128 + j, pb, vb);
+        }
+        cp_async_arrive_noinc(&fac_full[f]);
+      }
+    }
+    cp_async_wait_all();  // no copy is still in flight when the CTA exits
   } else {
     // Epilogue: per 128-deep slice, acc += partial * fa[row] * fb[col] in FP32
-    // registers.  The factors of slice kt + kBlkAhead are loaded while slice kt
-    // is processed; the warp's 64 B factors of a slice go through a ring in the
-    // warp's own shared memory (written by its lanes, read by all of them).
+    // registers, with the slice's factors from the factor warp's ring slot.
     const int ew = warp - 2;          // 0..7
     const int q = warp & 3;           // TMEM lane quarter
     const int half = ew >> 2;         // column half of the tile
-    float* my_sb = s_sb + ew * kBlkSbRing * 64;
     const bool vec_ok = g.c_fp32 ? (g.N % 4 == 0) : (g.N % 8 == 0);
     uint32_t slice = 0;
     bool ok = true;
@@ -1089,34 +1109,16 @@ __global__ void __launch_bounds__(kBlkThreads, 1)
       tile_coords(t, g.tiles_m, g.tiles_n, mt, nt);
       const int64_t row = (int64_t)mt * kBM + q * 32 + lane;
       const int64_t n0 = (int64_t)nt * BN;
-      const int64_t ncol = n0 + half * HALF + 2 * lane;  // this lane's two B-factor columns
       float2 acc[HALF / 2];  // column pairs: the promotion runs as packed two-wide FMAs
 #pragma unroll
       for (int i = 0; i < HALF / 2; ++i) acc[i] = make_float2(0.f, 0.f);
-      // factors of the first kBlkAhead slices
-      float fa_ring[kBlkAhead];
-      float2 fb_ring[kBlkAhead];
-#pragma unroll
-      for (int d = 0; d < kBlkAhead; ++d) {
-        fa_ring[d] = blk_a_factor(g, KB, row, mt, d);
-        fb_ring[d] = blk_b_factors(g, KB, ncol, nt, d);
-      }
       for (int kt = 0; kt < g.num_k; ++kt, ++slice) {
         const uint32_t a = slice % NB, aph = (slice / NB) & 1u;
-        const float fa = fa_ring[0];
-        const float2 fbv = fb_ring[0];
-#pragma unroll
-        for (int d = 0; d + 1 < kBlkAhead; ++d) {
-          fa_ring[d] = fa_ring[d + 1];
-          fb_ring[d] = fb_ring[d + 1];
-        }
-        fa_ring[kBlkAhead - 1] = blk_a_factor(g, KB, row, mt, kt + kBlkAhead);
-        fb_ring[kBlkAhead - 1] = blk_b_factors(g, KB, ncol, nt, kt + kBlkAhead);
-        float* sbs = my_sb + (kt % kBlkSbRing) * 64;
-        if (g.b_rows == 1) {
-          *reinterpret_cast<float2*>(sbs + 2 * lane) = fbv;
-          __syncwarp();
-        }
+        const uint32_t f = slice % kBlkFacSlots, fph = (slice / kBlkFacSlots) & 1u;
+        if (!(ok = mbar_wait_bounded(&fac_full[f], fph, abort_flag, &g_device_error))) break;
+        const float* slot = s_fac + f * kBlkFacSlot;
+        const float fa = slot[q * 32 + lane];          // this thread's row
+        const float* sbs = slot + 128 + half * HALF;   // the warp's 64 columns (128x128: all equal)
         if (!(ok = mbar_wait_bounded(&acc_full[a], aph, abort_flag, &g_device_error))) break;
         __syncwarp();
         tc_fence_after();
@@ -1144,7 +1146,7 @@ __global__ void __launch_bounds__(kBlkThreads, 1)
               a23 = __ffma2_rn(make_float2(__uint_as_float(v[i + 2]), __uint_as_float(v[i + 3])), w23, a23);
             }
           } else {
-            const float f = fa * fbv.x;
+            const float f = fa * sbs[0];
             const float2 w = make_float2(f, f);
 #pragma unroll
             for (int i = 0; i < 16; ++i)
@@ -1152,6 +1154,8 @@ __global__ void __launch_bounds__(kBlkThreads, 1)
                                             acc[16 * cc + i]);
           }
         }
+        __syncwarp();  // every lane is done with the slot
+        if (lane == 0) mbar_arrive(&fac_empty[f]);
       }
       if (!ok || row >= g.M) continue;
       const int64_t c0 = n0 + half * HALF;
