@@ -1040,8 +1040,28 @@ def run_drift(args):
     print(json.dumps({"workload": f"FP8 drift, attention-out M={M} K=N={K}, 20 steps", "results": res}), flush=True)
 
 
-def report_tables(per, shapes_list, linears):
-    """Tables of the speed-up analysis from per-GEMM times: per[recipe][mode][gemm] = ms."""
+# GEMM-only speed-up / step speed-up above which the overhead outside the GEMMs
+# is read as consuming the gain (the pages contrast "about equal" with "much
+# larger" and give no number).
+OVERHEAD_RATIO = 1.25
+
+
+def step_diagnostic(gemm_only, step):
+    """The pages' reading of a GEMM-only (pre-quantized) speed-up against the
+    step's (here: the autocast layer, quantization included), from [TE]
+    "interpreting real-model results"."""
+    if gemm_only < 1.0:
+        return "below 1.0 even kernel-only: not faster on these shapes (or a silent fallback)"
+    if gemm_only / step > OVERHEAD_RATIO:
+        return ("GEMM-only speed-up well above the step's: work outside the GEMMs (quantization: amax pass, "
+                "RHT, stochastic rounding, 2D weight scaling for NVFP4) consumes the gain")
+    return "GEMM-only speed-up close to the step's: the GEMMs dominate, as expected"
+
+
+def report_tables(per, shapes_list, linears, layers=None):
+    """Tables of the speed-up analysis from per-GEMM times: per[recipe][mode][gemm] = ms.
+    `layers` (the model's layer count) scales the per-layer times into the
+    end-to-end projection."""
     shapes = {n: (m, k, nn) for n, _, m, k, nn in shapes_list}
     names = [n for n, *_ in shapes_list]
     # BF16 does the same work in both modes; the faster of its two runs is the
@@ -1063,6 +1083,20 @@ def report_tables(per, shapes_list, linears):
         out["nvfp4_vs_mxfp8"] = ratios
     out["dgrad_vs_fprop"] = {r: {lin: per[r]["autocast"][f"{lin}_dgrad"] / per[r]["autocast"][f"{lin}_fprop"]
                                  for lin in linears} for r in per}
+    if base:
+        # End-to-end projection: the layer's 12 GEMMs (with their quantization in
+        # autocast) times the layer count, and the diagnostic of the GEMM-only
+        # (pre-quantized) speed-up against the step's (autocast).
+        base_layer = sum(base[n] for n in names)
+        proj = {}
+        for r in per:
+            lay = {m: sum(per[r][m][n] for n in names) for m in per[r]}
+            g_only, step = base_layer / lay["prequant"], base_layer / lay["autocast"]
+            proj[r] = {"layer_ms": lay, "gemm_only_speedup": g_only, "step_speedup": step,
+                       "diagnostic": "the baseline" if r == "bf16" else step_diagnostic(g_only, step)}
+            if layers:
+                proj[r]["model_ms"] = {m: layers * v for m, v in lay.items()}
+        out["projection"] = {"layers": layers, "recipes": proj}
     # human-readable tables
     lines = []
     for m in ("autocast", "prequant"):
@@ -1079,6 +1113,10 @@ def report_tables(per, shapes_list, linears):
         for m, rr in out["nvfp4_vs_mxfp8"].items():
             lines.append(f"NVFP4 vs MXFP8 Fprop ({m}): " + ", ".join(f"{n} {v:.2f}x" for n, v in rr.items()))
     if base:
+        for r, v in out["projection"]["recipes"].items():
+            model = f", {layers} layers {v['model_ms']['autocast']:.1f} ms" if layers else ""
+            lines.append(f"{r}: GEMM-only {v['gemm_only_speedup']:.2f}x, step {v['step_speedup']:.2f}x{model}: "
+                         f"{v['diagnostic']}")
         lines.append("below BF16: " + (", ".join(out["below_bf16"]) or "none"))
     return out, lines
 
@@ -1090,8 +1128,9 @@ def run_report(args):
     copies + GEMM) and pre-quantize (GEMM only) mode.  Prints per-shape tables
     and speed-ups vs BF16 on stderr, and one JSON line with the numbers:
     per-shape NVFP4 / MXFP8 Fprop ratios and their blend, Dgrad vs Fprop per
-    linear, and the shapes whose speed-up vs BF16 is below 1 (not faster, or
-    a silent fallback, which lpq does not have)."""
+    linear, the shapes whose speed-up vs BF16 is below 1 (not faster, or
+    a silent fallback, which lpq does not have), and the end-to-end projection
+    to the model's layer count with the GEMM-only vs step diagnostic."""
     import torch
     torch.cuda.set_device(0)
     layer = Layer(args, "cuda:0")
@@ -1109,7 +1148,7 @@ def run_report(args):
         for key in [k_ for k_ in layer.bufs if k_[0] == r]:
             del layer.bufs[key]
         torch.cuda.empty_cache()
-    out, lines = report_tables(per, layer.shapes, layer.linears)
+    out, lines = report_tables(per, layer.shapes, layer.linears, args.num_hidden_layers)
     print("\n".join(lines), file=sys.stderr, flush=True)
     print(json.dumps(out), flush=True)
 

@@ -43,3 +43,26 @@ def test_below_bf16_lists_only_slower_shapes():
     assert out["speedup_vs_bf16"]["nvfp4"]["prequant"]["qkv_fprop"] == 2.0
     assert out["dgrad_vs_fprop"]["nvfp4"]["attn_out"] == 0.5 / 1.25
     assert lines[-1].startswith("below BF16: nvfp4/autocast/attn_out_fprop")
+
+
+def test_projection_and_step_diagnostic():
+    """End-to-end projection: the layer's GEMM times (autocast: with their
+    quantization) x the layer count, and the pages' three readings of the
+    GEMM-only speed-up against the step's (about equal: the GEMMs dominate;
+    much larger: work outside the GEMMs eats the gain; below 1: not faster)."""
+    base = times("bf16")                                            # 12 ms per layer
+    per = {"bf16": base,
+           "dominant": {"autocast": {n: 0.55 for n, *_ in SHAPES}, "prequant": {n: 0.5 for n, *_ in SHAPES}},
+           "overhead": {"autocast": {n: 0.9 for n, *_ in SHAPES}, "prequant": {n: 0.3 for n, *_ in SHAPES}},
+           "slower": {"autocast": {n: 1.3 for n, *_ in SHAPES}, "prequant": {n: 1.2 for n, *_ in SHAPES}}}
+    out, lines = bench.report_tables(per, SHAPES, LINEARS, layers=24)
+    p = out["projection"]["recipes"]
+    assert out["projection"]["layers"] == 24
+    assert p["dominant"]["gemm_only_speedup"] == pytest.approx(2.0)
+    assert p["dominant"]["step_speedup"] == pytest.approx(1 / 0.55)
+    assert p["dominant"]["model_ms"]["autocast"] == pytest.approx(24 * 12 * 0.55)
+    assert "GEMMs dominate" in p["dominant"]["diagnostic"]
+    assert "consumes the gain" in p["overhead"]["diagnostic"]      # 3.33x GEMM-only vs 1.11x step
+    assert "below 1.0" in p["slower"]["diagnostic"]
+    assert p["bf16"]["diagnostic"] == "the baseline"
+    assert any(ln.startswith("overhead: GEMM-only 3.33x, step 1.11x, 24 layers") for ln in lines)
