@@ -599,6 +599,22 @@ def time_quant_kinds(layer, hbm_gbs, reps=10):
         gbs = nbytes / (us * 1e-6) / 1e9
         out[name] = {"shape": list(t.shape), "us": round(us, 2), "bytes_per_elem": round(per, 4),
                      "gbs": round(gbs, 1), "frac": round(gbs / hbm_gbs, 3)}
+    # The delayed-scaling update (amax history of 16, scale from its maximum):
+    # a single tiny kernel, latency-bound, reported in microseconds.  The flush
+    # write ahead of it keeps the GPU busy while the host enqueues the call, so
+    # the events time the kernel, not the host's submission.
+    st = L.DelayedState(16, dev)
+    a1 = torch.ones(1, dtype=torch.float32, device=dev)
+    L.scale_update(st, a1, L.FMAX[L.FP8_E4M3])
+    total = 0.0
+    for _ in range(reps):
+        flush.zero_()
+        e0.record()
+        L.scale_update(st, a1, L.FMAX[L.FP8_E4M3])
+        e1.record()
+        torch.cuda.synchronize()
+        total += e0.elapsed_time(e1)
+    out["scale_update"] = {"us": round(total / reps * 1e3, 2), "bound": "latency", "history": 16}
     check_device("quantizer kinds")
     del flush
     return out
