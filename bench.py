@@ -83,6 +83,8 @@ def parse():
 
 # ------------------------------------------------------------------ contract line
 METRIC = "quantize+GEMM TFLOP/s & % of FP8/FP4 peak; ms/layer (CodonFM-5B shape)"
+# Nominal dense per-GPU tensor rates of GB300 (without 2:4 sparsity), TFLOP/s.
+DATASHEET_DENSE_TFLOPS = {"bf16": 2250.0, "fp8": 4500.0, "mxfp8": 4500.0, "nvfp4": 13500.0}
 
 
 def contract_config(args, world, recipe, autocast):
@@ -708,7 +710,10 @@ def run_lpq(args, rank, world, local):
             "peak_source": peak_src, "algorithmic_bytes_per_launch": algo_bytes / len(layer.shapes),
             "tcgen05_ceiling": {"value": ceiling, "unit": "TFLOP/s", "frac": gemm_achieved / ceiling,
                                 "how": f"lpq_mma_peak {mma_kind}, CTA pairs (256 x 256 MMAs), operands in shared "
-                                       "memory, measured in this run"}}
+                                       "memory, measured in this run"},
+            "datasheet": {"value": DATASHEET_DENSE_TFLOPS[mma_kind], "unit": "TFLOP/s",
+                          "frac": gemm_achieved / DATASHEET_DENSE_TFLOPS[mma_kind],
+                          "how": "nominal dense (no 2:4 sparsity) per-GPU rate of the format"}}
     if recipe != "bf16" and autocast:
         qb = quant_bytes_per_layer(layer, recipe)
         roof["quantize"] = {"bound": "hbm", "bytes_per_layer": qb, "ms_per_layer": quant_ms,
