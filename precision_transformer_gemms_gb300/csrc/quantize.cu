@@ -236,37 +236,6 @@ __global__ void __launch_bounds__(kThreads, tile_min_ctas(KIND, NVO)) quant_tile
   const int64_t R = p.R, C = p.C;
   constexpr float kFmax = kE5M2 ? 57344.0f : 448.0f;
 
-  // ---------------------------------------------------------------- scales
-  float scale = 1.0f;  // per-tensor FP8
-  if constexpr (KIND == QK_FP8) {
-    if (p.delayed_scale) {
-      scale = *p.delayed_scale;
-    } else {
-      float a = *p.amax_row;
-      scale = finite_pos(a) ? scale_quotient(kFmax, a) : 1.0f;
-    }
-    if (blockIdx.x == 0 && blockIdx.y == 0 && t == 0) {
-      float sinv = __fdiv_rn(1.0f, scale);
-      if (p.row_ts) *p.row_ts = sinv;
-      if (p.col_ts) *p.col_ts = sinv;
-    }
-  }
-  float s_enc_row = 1.f, s_enc_col = 1.f;
-  uint32_t sgn_mask = 0;  // RHT signs as bits (flips of the sign bit; no registers of factors)
-  if constexpr (KIND == QK_NV) {
-    if (p.row_codes) s_enc_row = nv_s_enc(p.amax_row);
-    if (p.col_codes) s_enc_col = nv_s_enc(p.amax_col);
-    if (blockIdx.x == 0 && blockIdx.y == 0 && t == 0) {
-      if (p.row_ts) *p.row_ts = nv_ts_dec(p.amax_row);
-      if (p.col_ts) *p.col_ts = nv_ts_dec(p.amax_col);
-    }
-    if constexpr (kRHT) sgn_mask = rht_signs(p.rht_seed);
-    nv_factor_table(fb_tab[0], s_enc_row, t);
-    nv_factor_table(fb_tab[1], s_enc_col, t - 128);
-    __syncthreads();
-  }
-  const PhiloxKeys keys(kSR ? p.seed : 0);  // dead (and free) without stochastic rounding
-
   // ---------------------------------------------------------------- tiles
   // CTA b takes tiles b, b + gridDim.x, ... (row-major over the [R / TR,
   // C / 128] tiles).  Persistent kinds issue the next tile's 16-byte loads
@@ -313,12 +282,44 @@ __global__ void __launch_bounds__(kThreads, tile_min_ctas(KIND, NVO)) quant_tile
     }
   };
   float run_amax = 0.f;  // FP8 delayed scaling: the amax of every element this CTA reads
-  uint4 nxt[kPersist ? NLD : 1];
+  // The first tile's loads go out before the scales are set up (the amax read,
+  // the factor table, the barrier), so the two memory latencies overlap.
+  uint4 nxt[NLD];
   int64_t tl = kPersist ? (int64_t)blockIdx.x : 0;
   const int64_t tl_end = kPersist ? ntiles : 1, tl_step = kPersist ? (int64_t)gridDim.x : 1;
-  if constexpr (kPersist) {
-    if (tl < tl_end) load_tile(tl, nxt);
+  if (tl < tl_end) load_tile(tl, nxt);
+
+  // ---------------------------------------------------------------- scales
+  float scale = 1.0f;  // per-tensor FP8
+  if constexpr (KIND == QK_FP8) {
+    if (p.delayed_scale) {
+      scale = *p.delayed_scale;
+    } else {
+      float a = *p.amax_row;
+      scale = finite_pos(a) ? scale_quotient(kFmax, a) : 1.0f;
+    }
+    if (blockIdx.x == 0 && blockIdx.y == 0 && t == 0) {
+      float sinv = __fdiv_rn(1.0f, scale);
+      if (p.row_ts) *p.row_ts = sinv;
+      if (p.col_ts) *p.col_ts = sinv;
+    }
   }
+  float s_enc_row = 1.f, s_enc_col = 1.f;
+  uint32_t sgn_mask = 0;  // RHT signs as bits (flips of the sign bit; no registers of factors)
+  if constexpr (KIND == QK_NV) {
+    if (p.row_codes) s_enc_row = nv_s_enc(p.amax_row);
+    if (p.col_codes) s_enc_col = nv_s_enc(p.amax_col);
+    if (blockIdx.x == 0 && blockIdx.y == 0 && t == 0) {
+      if (p.row_ts) *p.row_ts = nv_ts_dec(p.amax_row);
+      if (p.col_ts) *p.col_ts = nv_ts_dec(p.amax_col);
+    }
+    if constexpr (kRHT) sgn_mask = rht_signs(p.rht_seed);
+    nv_factor_table(fb_tab[0], s_enc_row, t);
+    nv_factor_table(fb_tab[1], s_enc_col, t - 128);
+    __syncthreads();
+  }
+  const PhiloxKeys keys(kSR ? p.seed : 0);  // dead (and free) without stochastic rounding
+
   for (; tl < tl_end; tl += tl_step) {
   int64_t r0, c0;
   tile_origin(tl, r0, c0);
@@ -329,7 +330,8 @@ __global__ void __launch_bounds__(kThreads, tile_min_ctas(KIND, NVO)) quant_tile
     if (tl + tl_step < tl_end) load_tile(tl + tl_step, nxt);
     __syncthreads();  // the previous tile's readers of the shared memory are done
   } else {
-    load_tile(tl, vbuf);
+#pragma unroll
+    for (int i = 0; i < NLD; ++i) vbuf[i] = nxt[i];  // this CTA's one tile, loaded at the start
   }
   const bool col_ok = c0 + lc < C;
   float local_amax = 0.f;
