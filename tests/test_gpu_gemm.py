@@ -68,7 +68,9 @@ BLOCK_SHAPES = [(4, 128, 16), (256, 512, 384), (300, 640, 200), (520, 1024, 776)
 @pytest.mark.parametrize("out_fp32", [True, False])
 @pytest.mark.parametrize("shape", BLOCK_SHAPES)
 @pytest.mark.parametrize("fmts", [(lpq.FP8_BLOCK_1x128, lpq.FP8_BLOCK_128x128),
-                                  (lpq.FP8_BLOCK_1x128, lpq.FP8_BLOCK_1x128)])
+                                  (lpq.FP8_BLOCK_1x128, lpq.FP8_BLOCK_1x128),
+                                  (lpq.FP8_BLOCK_128x128, lpq.FP8_BLOCK_128x128),
+                                  (lpq.FP8_BLOCK_128x128, lpq.FP8_BLOCK_1x128)])
 def test_subchannel_gemm_parity(fmts, shape, out_fp32):
     """Sub-channel FP8: per 128-deep slice the tensor-core partial is scaled by
     the FP32 block factors and accumulated in FP32."""
