@@ -39,9 +39,10 @@ def check(a, b, M, N, K, out_fp32, layout=lpq.FPROP, path=None):
 @pytest.mark.parametrize("out_fp32", [True, False])
 @pytest.mark.parametrize("shape", SHAPES)
 @pytest.mark.parametrize("fmts", [(lpq.BF16, lpq.BF16), (lpq.FP8_E4M3, lpq.FP8_E4M3), (lpq.FP8_E5M2, lpq.FP8_E4M3),
-                                  (lpq.MXFP8, lpq.MXFP8), (lpq.MXFP8_E5M2, lpq.MXFP8),
+                                  (lpq.FP8_E4M3, lpq.FP8_E5M2), (lpq.FP8_E5M2, lpq.FP8_E5M2),
+                                  (lpq.MXFP8, lpq.MXFP8), (lpq.MXFP8_E5M2, lpq.MXFP8), (lpq.MXFP8, lpq.MXFP8_E5M2),
                                   (lpq.MXFP8_E5M2, lpq.MXFP8_E5M2), (lpq.MXFP4, lpq.MXFP4),
-                                  (lpq.NVFP4, lpq.NVFP4), (lpq.NVFP4, lpq.NVFP4_2D)])
+                                  (lpq.NVFP4, lpq.NVFP4), (lpq.NVFP4, lpq.NVFP4_2D), (lpq.NVFP4_2D, lpq.NVFP4)])
 def test_gemm_parity(fmts, shape, out_fp32, path):
     """Every kernel path: one CTA per 128 x 256 tile (block scales stored into
     TMEM by scale warps, or copied by the MMA thread: single_cp, pair_cp), one CTA per
@@ -58,6 +59,8 @@ def test_gemm_parity(fmts, shape, out_fp32, path):
     M, K, N = shape
     if fmts[1] == lpq.NVFP4_2D and N % 16:
         pytest.skip("2D weight tiles need N % 16 == 0")
+    if fmts[0] == lpq.NVFP4_2D and M % 16:
+        pytest.skip("2D tiles need M % 16 == 0")
     a, b = quantize_pair(*fmts, M, K, N)
     check(a, b, M, N, K, out_fp32, path=path)
 
